@@ -1,0 +1,498 @@
+/*
+ * cq_oracle.c -- plain CPU oracle for the MoE dispatch / combine hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the benchmark's
+ * CPU-baseline leg are the only callers; the CUDA library shares no code with
+ * this file. Single-threaded, sequential loops, in the order the pages give.
+ * Page titles behind the short tags [DV3] [DSN] [LLD] [PERF] are listed in
+ * cq_oracle.h.
+ *
+ * Build: gcc -std=c11 -O2 -ffp-contract=off -fPIC -shared (no fast-math), so
+ * every float operation below is one IEEE binary32 operation rounded to
+ * nearest-even, and fmaf() is the single-rounding fused multiply-add.
+ */
+#include "cq_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* Configuration rules.                                                      */
+/* ------------------------------------------------------------------------ */
+
+int32_t cqo_local_expert_num(const cqo_config* c) {
+  /* [DV3] Shape 格式说明: on an MoE-expert rank,
+   * local_expert_num = moe_expert_num / (ep_world_size - shared_expert_rank_num). */
+  return c->moe_expert_num / (c->ep_world_size - c->shared_expert_rank_num);
+}
+
+int32_t cqo_num_slots(const cqo_config* c) {
+  /* Each token has K routed slots, plus one slot per shared expert when
+   * shared-expert ranks exist ([DV3] 参数说明 shared_expert_num /
+   * shared_expert_rank_num). */
+  return c->topk + (c->shared_expert_rank_num > 0 ? c->shared_expert_num : 0);
+}
+
+int64_t cqo_max_rows(const cqo_config* c) {
+  return (int64_t)c->ep_world_size * c->max_bs * cqo_num_slots(c);
+}
+
+int32_t cqo_scale_cols(const cqo_config* c) {
+  /* [LLD] quant_mode 相关约束: mx modes give dynamic_scales shape (A, Align2(Ceil(H, 32))). */
+  int32_t blocks = (c->hidden + 31) / 32;
+  return (blocks + 1) / 2 * 2;
+}
+
+int cqo_check_config(const cqo_config* c) {
+  /* Ranges: [DV3] 约束说明 (Atlas A3 constraints and the torch._check list in
+   * the Python wrapper) and [LLD] shape variables. */
+  const int32_t W = c->ep_world_size, M = c->moe_expert_num;
+  const int32_t S = c->shared_expert_num, Sr = c->shared_expert_rank_num;
+  if (W < 2 || W > 768) return CQO_ERR_ARG;
+  if (c->hidden < 1024 || c->hidden > 8192) return CQO_ERR_ARG;
+  if (c->max_bs < 1 || c->max_bs > 512) return CQO_ERR_ARG;
+  if (M < 1 || M > 1024) return CQO_ERR_ARG;
+  if (c->topk < 1 || c->topk > 16) return CQO_ERR_ARG;
+  if (S < 0 || S > 4) return CQO_ERR_ARG;
+  /* [DV3] 参数说明 shared_expert_rank_num: in [0, W); zero requires S in {0, 1},
+   * non-zero requires S_r % S == 0. [DV3] 前置校验: W a multiple of S_r. */
+  if (Sr < 0 || Sr >= W) return CQO_ERR_ARG;
+  if (Sr == 0 && S > 1) return CQO_ERR_ARG;
+  if (Sr > 0 && (S == 0 || Sr % S != 0 || W % Sr != 0)) return CQO_ERR_ARG;
+  /* [DV3] 前置校验: moe_expert_num a multiple of W - S_r. */
+  if (M % (W - Sr) != 0) return CQO_ERR_ARG;
+  /* [LLD] local_expert_num * ep_world_size <= 2048. */
+  if ((int64_t)cqo_local_expert_num(c) * W > 2048) return CQO_ERR_ARG;
+  if (c->zero_expert_num < 0 || c->copy_expert_num < 0 || c->const_expert_num < 0)
+    return CQO_ERR_ARG;
+  /* [DV3] Shape 格式说明: 0 < K <= M + Z + C + Q, and that sum < MAX_INT32. */
+  int64_t all = (int64_t)M + c->zero_expert_num + c->copy_expert_num + c->const_expert_num;
+  if (all >= 2147483647LL) return CQO_ERR_ARG;
+  if (c->topk > all) return CQO_ERR_ARG;
+  /* [DV3] 参数说明 global_bs: 0 or max_bs * ep_world_size. */
+  if (c->global_bs != 0 && c->global_bs != c->max_bs * W) return CQO_ERR_ARG;
+  if (c->quant_mode == 1 || c->quant_mode == 3 || c->quant_mode == 4) return CQO_ERR_UNSUPPORTED;
+  if (c->quant_mode != 0 && c->quant_mode != 2 && c->quant_mode != 5) return CQO_ERR_ARG;
+  if (c->expert_token_nums_type != 0 && c->expert_token_nums_type != 1) return CQO_ERR_ARG;
+  if (c->mask_ndim < 0 || c->mask_ndim > 2) return CQO_ERR_ARG;
+  return CQO_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Number formats, written from their definitions.                           */
+/* ------------------------------------------------------------------------ */
+
+float cqo_bf16_to_f32(uint16_t b) {
+  /* bfloat16 is the upper half of a binary32. */
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+uint16_t cqo_bf16_from_f32(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return (uint16_t)((u >> 16) | 0x0040u); /* quiet NaN */
+  /* Round to nearest, ties to even, on the 16 discarded bits. */
+  uint32_t keep_lsb = (u >> 16) & 1u;
+  u += 0x7fffu + keep_lsb;
+  return (uint16_t)(u >> 16);
+}
+
+int32_t cqo_ceil_log2(float q) {
+  /* frexpf gives q = m * 2^e with m in [0.5, 1); q is a power of two exactly
+   * when m == 0.5, and then log2(q) = e - 1; otherwise ceil(log2(q)) = e. */
+  int e;
+  float m = frexpf(q, &e);
+  return (m == 0.5f) ? e - 1 : e;
+}
+
+float cqo_e4m3_decode(uint8_t b) {
+  /* FP8 E4M3 ("fn" variant): 1 sign, 4 exponent bits with bias 7, 3 mantissa
+   * bits, no infinities, only S.1111.111 is NaN; largest finite 448. */
+  int sign = b >> 7, e = (b >> 3) & 0xf, m = b & 7;
+  if (e == 15 && m == 7) return NAN;
+  float mag = (e == 0) ? ldexpf((float)m, -9) : ldexpf(1.0f + (float)m / 8.0f, e - 7);
+  return sign ? -mag : mag;
+}
+
+uint8_t cqo_e4m3_encode(float v) {
+  /* Round to nearest even; magnitudes beyond 448 saturate to 448
+   * (satfinite); NaN maps to the NaN code. */
+  if (isnan(v)) return 0x7f;
+  uint8_t sign = signbit(v) ? 0x80 : 0x00;
+  float a = fabsf(v);
+  if (a >= 448.0f) return sign | 0x7e;
+  if (a < 0x1p-6f) {
+    /* Subnormal range: value = m * 2^-9, m = 0..7; m == 8 is the smallest
+     * normal, whose code is also 8. a * 512 is exact. */
+    float m = rintf(a * 512.0f);
+    return sign | (uint8_t)m;
+  }
+  int e;
+  frexpf(a, &e); /* a = f * 2^e, f in [0.5, 1)  =>  a = (2f) * 2^(e-1) */
+  int ex = e - 1;  /* unbiased exponent, -6..8 */
+  float t = ldexpf(a, -ex);            /* in [1, 2), exact */
+  float mq = rintf((t - 1.0f) * 8.0f); /* 0..8, ties to even */
+  if (mq == 8.0f) {
+    mq = 0.0f;
+    ex += 1;
+  }
+  int code = ((ex + 7) << 3) | (int)mq;
+  if (code > 0x7e) code = 0x7e; /* rounding up past 448 saturates */
+  return sign | (uint8_t)code;
+}
+
+void cqo_e4m3_encode_n(const float* in, uint8_t* out, int64_t n) {
+  for (int64_t t = 0; t < n; ++t) out[t] = cqo_e4m3_encode(in[t]);
+}
+
+void cqo_bf16_from_f32_n(const float* in, uint16_t* out, int64_t n) {
+  for (int64_t t = 0; t < n; ++t) out[t] = cqo_bf16_from_f32(in[t]);
+}
+
+void cqo_ceil_log2_n(const float* in, int32_t* out, int64_t n) {
+  for (int64_t t = 0; t < n; ++t) out[t] = cqo_ceil_log2(in[t]);
+}
+
+static int8_t sat_rne_int8(float v) {
+  /* Round to nearest, ties to even (rintf under the default rounding mode),
+   * then saturate to the int8 range; NaN gives 0. */
+  if (isnan(v)) return 0;
+  float r = rintf(v);
+  if (r > 127.0f) r = 127.0f;
+  if (r < -128.0f) r = -128.0f;
+  return (int8_t)r;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Quantisation of one row, [LLD] 计算公式 and [DV3] 功能说明 情形 1 / 情形 2. */
+/* ------------------------------------------------------------------------ */
+
+int cqo_quant_row(int32_t mode, int32_t H, const uint16_t* x, const float* smooth, void* codes,
+                  void* scale) {
+  if (mode == 0) {
+    /* quant_out = x: the bf16 row travels unchanged. */
+    memcpy(codes, x, (size_t)H * sizeof(uint16_t));
+    return CQO_OK;
+  }
+  if (mode == 2) {
+    /* x_fp32 = CastToFp32(x) * smooth (when given);
+     * dynamic_scales_value = 127 / max|x_fp32|;
+     * quant_out = Cast(x_fp32 * dynamic_scales_value, int8);
+     * carried scale = 1.0 / dynamic_scales_value. */
+    float* xf = (float*)malloc((size_t)H * sizeof(float));
+    if (!xf) return CQO_ERR_NOMEM;
+    for (int32_t h = 0; h < H; ++h) {
+      float v = cqo_bf16_to_f32(x[h]);
+      xf[h] = smooth ? v * smooth[h] : v;
+    }
+    float amax = 0.0f;
+    for (int32_t h = 0; h < H; ++h) {
+      float a = fabsf(xf[h]);
+      if (a > amax) amax = a;
+    }
+    float s = 127.0f / amax; /* +inf for an all-zero row */
+    int8_t* q = (int8_t*)codes;
+    for (int32_t h = 0; h < H; ++h) q[h] = sat_rne_int8(xf[h] * s);
+    *(float*)scale = 1.0f / s;
+    free(xf);
+    return CQO_OK;
+  }
+  if (mode == 5) {
+    /* mx clip quantisation, per block of 32 elements:
+     * max_abs_clamp = max(max|x|, 1e-4);
+     * shared_exp = ceil(log2(max_abs_clamp / 448));
+     * quant_out = CastToFp8E4M3(x / 2^shared_exp);
+     * the block scale 2^shared_exp is stored as e8m0 (shared_exp + 127). */
+    uint8_t* q = (uint8_t*)codes;
+    uint8_t* sc = (uint8_t*)scale;
+    const int32_t nblk = (H + 31) / 32;
+    const int32_t cols = (nblk + 1) / 2 * 2;
+    for (int32_t b = 0; b < nblk; ++b) {
+      const int32_t h0 = b * 32, h1 = (h0 + 32 < H) ? h0 + 32 : H;
+      float amax = 0.0f;
+      for (int32_t h = h0; h < h1; ++h) {
+        float a = fabsf(cqo_bf16_to_f32(x[h]));
+        if (a > amax) amax = a;
+      }
+      if (amax < 1e-4f) amax = 1e-4f;
+      int32_t e = cqo_ceil_log2(amax / 448.0f);
+      for (int32_t h = h0; h < h1; ++h) {
+        /* x / 2^e; 2^-e is a normal binary32 here, so ldexpf is exact. */
+        float v = ldexpf(cqo_bf16_to_f32(x[h]), -e);
+        q[h] = cqo_e4m3_encode(v);
+      }
+      sc[b] = (uint8_t)(e + 127);
+    }
+    for (int32_t b = nblk; b < cols; ++b) sc[b] = 0; /* Align2 padding column */
+    return CQO_OK;
+  }
+  return CQO_ERR_UNSUPPORTED;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Routing: [DSN] §2.2.2 (sendStatus scan and expandIdx), §2.4 (receive-side  */
+/* metadata), [DV3] 参数说明 / Shape 格式说明 (shared ranks first, special     */
+/* expert id ranges, masks, expert_token_nums_type).                          */
+/* ------------------------------------------------------------------------ */
+
+/* Is pair (r, i, j) of an in-range token switched on by the mask? */
+static int pair_active(const cqo_config* c, const uint8_t* mask, int32_t r, int32_t i, int32_t j) {
+  if (c->mask_ndim == 0 || mask == NULL) return 1;
+  if (c->mask_ndim == 1) return mask[(int64_t)r * c->max_bs + i] != 0;
+  return mask[((int64_t)r * c->max_bs + i) * c->topk + j] != 0;
+}
+
+int64_t cqo_route(const cqo_config* c, const int32_t* expert_ids, const uint8_t* mask,
+                  const int32_t* bs_per_rank, int32_t* expand_idx, int32_t* ep_recv_count,
+                  int64_t* expert_token_nums, int64_t* rank_row_base, int32_t* assist,
+                  int32_t* inv, uint32_t* status) {
+  int rc = cqo_check_config(c);
+  if (rc != CQO_OK) return rc;
+  const int32_t W = c->ep_world_size, M = c->moe_expert_num, K = c->topk, BS = c->max_bs;
+  const int32_t Sr = c->shared_expert_rank_num;
+  const int32_t Seff = (Sr > 0) ? c->shared_expert_num : 0;
+  const int32_t L = cqo_local_expert_num(c);
+  const int32_t NS = K + Seff;
+  const int32_t R = (Sr > 0) ? Sr / c->shared_expert_num : 0; /* replicas per shared expert */
+  const int64_t z0 = M, c0 = z0 + c->zero_expert_num, q0 = c0 + c->copy_expert_num;
+  const int64_t q1 = q0 + c->const_expert_num;
+  const int64_t nslot = (int64_t)W * BS * NS;
+  uint32_t st = 0;
+
+  /* dest[] / local[] record, for every slot, the (destination rank, local
+   * expert) it is sent to, or -1. */
+  int32_t* dest = (int32_t*)malloc((size_t)nslot * sizeof(int32_t));
+  int32_t* local = (int32_t*)malloc((size_t)nslot * sizeof(int32_t));
+  int32_t* send_status = (int32_t*)malloc((size_t)(M + (Seff > 0 ? Seff : 1)) * sizeof(int32_t));
+  if (!dest || !local || !send_status) {
+    free(dest);
+    free(local);
+    free(send_status);
+    return CQO_ERR_NOMEM;
+  }
+
+  /* Step 1, per source rank r: traverse expertIds in row-major (token, then
+   * k) order. For a MoE expert id e the target rank is S_r + e / L (integer
+   * division; shared-expert ranks come first), the local index is e % L, and
+   * expandIdx is the running count of earlier pairs of this source sent to
+   * e, which is then incremented. Shared expert s is replicated on R ranks
+   * s*R .. s*R+R-1; source r uses replica r % R, in slot K + s. */
+  for (int32_t r = 0; r < W; ++r) {
+    const int32_t n_r = bs_per_rank ? bs_per_rank[r] : BS;
+    for (int32_t e = 0; e < M; ++e) send_status[e] = 0;
+    for (int32_t s = 0; s < Seff; ++s) send_status[M + s] = 0;
+    int seen_false = 0;
+    for (int32_t i = 0; i < BS; ++i) {
+      const int64_t tok = (int64_t)r * BS + i;
+      for (int32_t k = 0; k < NS; ++k) {
+        expand_idx[tok * NS + k] = -1;
+        inv[tok * NS + k] = CQO_INV_NONE;
+        dest[tok * NS + k] = -1;
+        local[tok * NS + k] = -1;
+      }
+      if (i >= n_r) continue;
+      if (c->mask_ndim == 1 && mask) {
+        /* [DV3] x_active_mask: in 1-D form the true entries must precede the false ones. */
+        int on = mask[tok] != 0;
+        if (!on) seen_false = 1;
+        else if (seen_false) st |= CQO_ST_BAD_MASK;
+      }
+      int any = 0;
+      for (int32_t j = 0; j < K; ++j) {
+        if (!pair_active(c, mask, r, i, j)) continue;
+        any = 1;
+        const int64_t sl = tok * NS + j;
+        const int64_t id = expert_ids[tok * K + j];
+        if (id >= 0 && id < M) {
+          expand_idx[sl] = send_status[id]++;
+          dest[sl] = Sr + (int32_t)(id / L);
+          local[sl] = (int32_t)(id % L);
+        } else if (id >= z0 && id < c0) {
+          inv[sl] = CQO_INV_NONE; /* zero expert: contributes nothing */
+        } else if (id >= c0 && id < q0) {
+          inv[sl] = CQO_INV_COPY;
+        } else if (id >= q0 && id < q1) {
+          inv[sl] = CQO_INV_CONST_BASE - (int32_t)(id - q0);
+        } else {
+          st |= CQO_ST_BAD_ID;
+        }
+      }
+      /* [DV3] x_active_mask: a token whose entries are all false does not
+       * take part, so it reaches no shared expert either. */
+      if (any) {
+        for (int32_t s = 0; s < Seff; ++s) {
+          const int64_t sl = tok * NS + K + s;
+          expand_idx[sl] = send_status[M + s]++;
+          dest[sl] = s * R + r % R;
+          local[sl] = 0;
+        }
+      }
+    }
+  }
+
+  /* Step 2, per destination rank d: the received rows are laid out expert by
+   * expert (local index ascending), within an expert source rank ascending,
+   * within a source in arrival order (expandIdx ascending, which is the scan
+   * order). The placement is written out literally, row by row.
+   * ep_recv_count[d] is the received-count matrix (source x local expert),
+   * transposed and prefix-summed in row-major order ([DSN] §2.4.1), i.e. the
+   * running row count at the end of each (local expert, source) block. */
+  const int32_t recv_stride = W * L;
+  for (int64_t t = 0; t < (int64_t)W * recv_stride; ++t) ep_recv_count[t] = 0;
+  for (int64_t t = 0; t < (int64_t)W * L; ++t) expert_token_nums[t] = 0;
+  int64_t row = 0;
+  for (int32_t d = 0; d < W; ++d) {
+    rank_row_base[d] = row;
+    const int32_t Ld = (d < Sr) ? 1 : L; /* a shared-expert rank hosts one expert */
+    int64_t cum = 0;
+    for (int32_t le = 0; le < Ld; ++le) {
+      int64_t expert_rows = 0;
+      for (int32_t src = 0; src < W; ++src) {
+        for (int32_t i = 0; i < BS; ++i) {
+          for (int32_t k = 0; k < NS; ++k) {
+            const int64_t sl = ((int64_t)src * BS + i) * NS + k;
+            if (dest[sl] != d || local[sl] != le) continue;
+            assist[row * 4 + 0] = src;
+            assist[row * 4 + 1] = i;
+            assist[row * 4 + 2] = k;
+            assist[row * 4 + 3] = 0;
+            inv[sl] = (int32_t)row;
+            ++row;
+            ++expert_rows;
+          }
+        }
+        ep_recv_count[(int64_t)d * recv_stride + (int64_t)le * W + src] =
+            (int32_t)(row - rank_row_base[d]);
+      }
+      cum += expert_rows;
+      /* [DV3] expert_token_nums_type: 0 = prefix sum, 1 = per-expert count. */
+      expert_token_nums[(int64_t)d * L + le] = (c->expert_token_nums_type == 0) ? cum : expert_rows;
+    }
+  }
+  rank_row_base[W] = row;
+
+  free(dest);
+  free(local);
+  free(send_status);
+  if (status) *status |= st;
+  return row;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Dispatch = routing + quantisation of each placed row.                     */
+/* ------------------------------------------------------------------------ */
+
+int64_t cqo_dispatch(const cqo_config* c, const uint16_t* x, const int32_t* expert_ids,
+                     const float* smooth, const uint8_t* mask, const int32_t* bs_per_rank,
+                     const float* expert_scales, void* expand_x, void* dynamic_scales,
+                     float* expand_scales, int32_t* expand_idx, int32_t* ep_recv_count,
+                     int64_t* expert_token_nums, int64_t* rank_row_base, int32_t* assist,
+                     int32_t* inv, uint32_t* status) {
+  if (c->quant_mode == 5 && smooth) return CQO_ERR_ARG; /* [LLD]: mx modes take no smooth scales */
+  int64_t rows = cqo_route(c, expert_ids, mask, bs_per_rank, expand_idx, ep_recv_count,
+                           expert_token_nums, rank_row_base, assist, inv, status);
+  if (rows < 0) return rows;
+  const int32_t H = c->hidden, K = c->topk, BS = c->max_bs;
+  const int32_t Seff = (c->shared_expert_rank_num > 0) ? c->shared_expert_num : 0;
+  const int32_t cols = cqo_scale_cols(c);
+  for (int64_t row = 0; row < rows; ++row) {
+    const int32_t src = assist[row * 4 + 0], i = assist[row * 4 + 1], k = assist[row * 4 + 2];
+    const int64_t tok = (int64_t)src * BS + i;
+    const uint16_t* xr = x + tok * H;
+    /* [LLD] quant_mode 相关约束: the smooth table is (S + M, H) when shared
+     * experts exist, else (M, H); shared expert s uses row s, MoE expert e
+     * uses row S + e. */
+    const float* sm = NULL;
+    if (smooth) {
+      int64_t srow = (k < K) ? (int64_t)Seff + expert_ids[tok * K + k] : (int64_t)(k - K);
+      sm = smooth + srow * H;
+    }
+    void* codes;
+    void* scale;
+    if (c->quant_mode == 0) {
+      codes = (uint16_t*)expand_x + row * H;
+      scale = NULL;
+    } else if (c->quant_mode == 2) {
+      codes = (int8_t*)expand_x + row * H;
+      scale = (float*)dynamic_scales + row;
+    } else {
+      codes = (uint8_t*)expand_x + row * H;
+      scale = (uint8_t*)dynamic_scales + row * cols;
+    }
+    int rc = cqo_quant_row(c->quant_mode, H, xr, sm, codes, scale);
+    if (rc != CQO_OK) return rc;
+    /* [DV3] expand_scales: the routing weight travels with its row; a shared
+     * expert row carries weight 1 (its output is added unweighted). */
+    if (expand_scales)
+      expand_scales[row] = (k < K) ? (expert_scales ? expert_scales[tok * K + k] : 0.0f) : 1.0f;
+  }
+  return rows;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Combine: [DSN] §3.4 (locate each expert output of token i, weighted sum),  */
+/* [PERF] Combine 计算步骤 (multiply each MoE output by its expert scale, sum  */
+/* in float, then add the shared-expert outputs), [LLD] 特殊专家场景.          */
+/* ------------------------------------------------------------------------ */
+
+int cqo_combine_token(const cqo_config* c, int32_t r, int32_t i, const uint16_t* ffn,
+                      const int32_t* inv, const float* expert_scales, const uint16_t* ori_x,
+                      const float* const_alpha1, const float* const_alpha2,
+                      const uint16_t* const_v, int32_t out_f32, void* y_row) {
+  const int32_t H = c->hidden, K = c->topk, BS = c->max_bs;
+  const int32_t Seff = (c->shared_expert_rank_num > 0) ? c->shared_expert_num : 0;
+  const int32_t NS = K + Seff;
+  const int64_t tok = (int64_t)r * BS + i;
+  const int32_t* slots = inv + tok * NS;
+  for (int32_t h = 0; h < H; ++h) {
+    float acc = 0.0f;
+    /* Routed slots in j order: acc = fma(w_j, v_j, acc). */
+    for (int32_t j = 0; j < K; ++j) {
+      const int32_t code = slots[j];
+      const float w = expert_scales[tok * K + j];
+      float v;
+      if (code >= 0) {
+        v = cqo_bf16_to_f32(ffn[(int64_t)code * H + h]);
+      } else if (code == CQO_INV_COPY) {
+        v = cqo_bf16_to_f32(ori_x[tok * H + h]); /* Moe(ori_x) = ori_x */
+      } else if (code <= CQO_INV_CONST_BASE) {
+        /* Moe(ori_x) = alpha1 * ori_x + alpha2 * v: two rounded products, one rounded sum. */
+        const int32_t q = CQO_INV_CONST_BASE - code;
+        const float p1 = const_alpha1[q] * cqo_bf16_to_f32(ori_x[tok * H + h]);
+        const float p2 = const_alpha2[q] * cqo_bf16_to_f32(const_v[(int64_t)q * H + h]);
+        v = p1 + p2;
+      } else {
+        continue; /* zero expert, masked pair, invalid id: Moe(ori_x) = 0 */
+      }
+      acc = fmaf(w, v, acc);
+    }
+    /* Shared experts, added unweighted after the routed ones. */
+    for (int32_t s = 0; s < Seff; ++s) {
+      const int32_t code = slots[K + s];
+      if (code >= 0) acc = acc + cqo_bf16_to_f32(ffn[(int64_t)code * H + h]);
+    }
+    if (out_f32) ((float*)y_row)[h] = acc;
+    else ((uint16_t*)y_row)[h] = cqo_bf16_from_f32(acc);
+  }
+  return CQO_OK;
+}
+
+int cqo_combine(const cqo_config* c, const uint16_t* ffn, const int32_t* inv,
+                const float* expert_scales, const uint16_t* ori_x, const float* const_alpha1,
+                const float* const_alpha2, const uint16_t* const_v, int32_t out_f32, void* y) {
+  const int32_t H = c->hidden;
+  for (int32_t r = 0; r < c->ep_world_size; ++r) {
+    for (int32_t i = 0; i < c->max_bs; ++i) {
+      const int64_t tok = (int64_t)r * c->max_bs + i;
+      void* yr = out_f32 ? (void*)((float*)y + tok * H) : (void*)((uint16_t*)y + tok * H);
+      int rc = cqo_combine_token(c, r, i, ffn, inv, expert_scales, ori_x, const_alpha1,
+                                 const_alpha2, const_v, out_f32, yr);
+      if (rc != CQO_OK) return rc;
+    }
+  }
+  return CQO_OK;
+}
