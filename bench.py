@@ -1,0 +1,436 @@
+#!/usr/bin/env python
+"""Benchmark of the MoE dispatch + combine hot path on one GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl cq|reference]
+
+A step is one pass of the whole path over one batch: the routing scan
+(cq_dispatch_route), the fused permute-quantise (cq_dispatch_permute) and the
+combine (cq_combine), on the DeepSeek-V3-shaped workload (32 logical EP ranks,
+256 experts, 8 per rank, top-8, 128 tokens per rank, hidden 7168, per-token
+dynamic int8). The expert FFN between dispatch and combine is outside the path;
+combine consumes a seeded stand-in for its output.
+
+Prints one JSON line: tokens/s over the K timed steps (device-resident inputs,
+L2 flushed between steps, CUDA events on the launching stream), an end-to-end
+figure through cq_dispatch / cq_combine with host buffers, the roofline of the
+dominant kernel, the oracle timed on the host cores, and the SM clocks seen
+during the timed region. Under torchrun (N > 1) every rank runs an independent
+replica on its own GPU (no collective on the data path); the reported value is
+all ranks' tokens over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "dispatch+combine tokens/s"
+UNIT = "tokens/s"
+L2_FLUSH_BYTES = 256 << 20
+
+# DRAM bytes per launch read from an ncu capture of the named kernel, keyed by
+# the SHA-256 of the kernel's source file when it was captured; reported only
+# while the source is unchanged.
+NCU_TRAFFIC = {}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["cq", "reference"], default="cq")
+    ap.add_argument("--workload", default="dsv3")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="host time budget of the oracle baseline")
+    return ap.parse_args(argv)
+
+
+def workload_desc(wl) -> str:
+    c = wl.cfg
+    L = c["moe_expert_num"] // (c["ep_world_size"] - c["shared_expert_rank_num"])
+    return (f"{wl.name}: W={c['ep_world_size']} logical EP ranks, M={c['moe_expert_num']} "
+            f"experts (L={L}/rank), K={c['topk']}, BS={c['max_bs']}/rank, H={c['hidden']}, "
+            f"quant_mode={c['quant_mode']}")
+
+
+# ---------------------------------------------------------------- clocks ----
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, enabled: bool = True):
+        self.gpu = gpu_index
+        self.enabled = enabled
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        if not self.enabled:
+            return
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        self.proc.wait()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# -------------------------------------------------------- byte accounting ----
+
+def algorithmic_bytes(cfg, rows: int, tokens_active: int, with_scales: bool) -> dict:
+    """Bytes each kernel must move per launch (reads + writes of HBM), given
+    the routed row count P and the active token count."""
+    W, BS, K, H = cfg.ep_world_size, cfg.max_bs, cfg.topk, cfg.hidden
+    NS, L = cfg.num_slots, cfg.local_expert_num
+    G = cfg.shared_expert_rank_num + cfg.moe_expert_num
+    T = W * BS
+    mode = cfg.quant_mode
+    b_code = 2 if mode == 0 else 1
+    b_scale = {0: 0, 2: 4, 5: cfg.scale_cols}[mode]
+    route = 4 * T * K + 4 * T * NS + 3 * 4 * G * W + 4 * W * W * L + 8 * W * L
+    permute = (2 * H * tokens_active            # x, read once per active token
+               + rows * (H * b_code + b_scale + 16)  # codes, scale, (src, token, slot) record
+               + 4 * T * NS * 2 + 4 * T * K     # eidx read, inv write, ids read
+               + (8 * rows if with_scales else 0))  # routing weight read + carried copy
+    combine = 2 * H * rows + 2 * H * T + 4 * T * NS + 4 * T * K
+    return {"route": route, "permute": permute, "combine": combine}
+
+
+def measured_peaks() -> tuple[float, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def source_sha(kernel: str) -> str:
+    path = os.path.join(ROOT, "combine_quant_gb300", "csrc", f"cq_{kernel}.cu")
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def ncu_traffic(kernel: str):
+    rec = NCU_TRAFFIC.get(kernel)
+    if not rec or rec.get("src_sha") != source_sha(kernel):
+        return None
+    return rec["bytes_per_launch"]
+
+
+# ------------------------------------------------------- oracle baseline ----
+
+def oracle_sample(wl, budget_s: float, max_tokens: int | None = None):
+    """Time the oracle (single-threaded C, as it stands) on a bounded sample of
+    the workload: the full routing scan, then quantisation of the rows of the
+    first n tokens and the combine of those n tokens, n growing until the
+    budget is spent. Returns (tokens/s, description, cores)."""
+    import oracle
+    from combine_quant_gb300 import workloads
+
+    oracle.build()
+    cfg = wl.cfg
+    W, BS, K, H = cfg["ep_world_size"], cfg["max_bs"], cfg["topk"], cfg["hidden"]
+    mode = cfg["quant_mode"]
+    pool = workloads.ffn_standin(wl.seed, 1024, H)
+    t0 = time.perf_counter()
+    route = oracle.route(cfg, wl.expert_ids, wl.mask, wl.bs_per_rank)
+    t_route = time.perf_counter() - t0
+    inv_pool = np.where(route.inv >= 0, route.inv.astype(np.int64) % pool.shape[0],
+                        route.inv).astype(np.int32)
+    order = [(r, i) for r in range(W) for i in range(BS)]
+    if max_tokens:
+        order = order[:max_tokens]
+    done = 0
+    t0 = time.perf_counter()
+    for r, i in order:
+        for k in range(route.inv.shape[2]):
+            row = route.inv[r, i, k]
+            if row >= 0:
+                sm = None
+                if wl.smooth is not None and mode == 2:
+                    sm = wl.smooth[wl.expert_ids[r, i, k]] if k < K else wl.smooth[k - K]
+                oracle.quant_row(mode, wl.x[r, i], sm)
+        oracle.combine_tokens(cfg, [(r, i)], pool, inv_pool, wl.expert_scales, wl.x,
+                              wl.const_alpha1, wl.const_alpha2, wl.const_v)
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    t_tok = time.perf_counter() - t0
+    # The routing scan is a whole-batch pass; charge it pro rata.
+    per_tok = t_tok / done + t_route / (W * BS)
+    desc = (f"oracle route over all {W * BS} tokens ({t_route:.3f} s) + quantise-and-combine of "
+            f"the first {done} tokens in rank-major order ({t_tok:.2f} s); value = tokens / "
+            f"(per-token time + route time pro rata)")
+    return 1.0 / per_tok, desc, 1
+
+
+# ------------------------------------------------------------- distributed ----
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def emit(obj):
+    print(json.dumps(obj), flush=True)
+
+
+# ----------------------------------------------------------- reference arm ----
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0  # the oracle arm runs once, on rank 0
+    from combine_quant_gb300 import workloads
+
+    wl = workloads.WORKLOADS[args.workload]()
+    W, BS = wl.cfg["ep_world_size"], wl.cfg["max_bs"]
+    # Each step is a bounded sample: enough tokens that K + W steps take about
+    # a minute of host time in total.
+    _, _, _ = oracle_sample(wl, 0.5, max_tokens=4)  # warm the library and caches
+    rate0, _, _ = oracle_sample(wl, 2.0)
+    per_step_tokens = max(1, min(W * BS, int(rate0 * 60.0 / max(1, args.steps + args.warmup))))
+    times = []
+    for s in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        rate, desc, cores = oracle_sample(wl, 1e9, max_tokens=per_step_tokens)
+        if s >= args.warmup:
+            times.append(per_step_tokens / rate)
+    total = sum(times)
+    value = per_step_tokens * len(times) / total
+    emit({"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+          "steps": args.steps, "warmup": args.warmup,
+          "ms_per_step": 1e3 * total / len(times), "higher_is_better": True,
+          "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+          "config": {"workload": workload_desc(wl), "tokens_per_step": per_step_tokens},
+          "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                           "sample": f"each step: {desc}"},
+          "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                  "d2h_bytes_per_step": 0}})
+    return 0
+
+
+# ------------------------------------------------------------------ cq arm ----
+
+def run_cq(args):
+    import torch
+
+    import combine_quant_gb300 as cq
+    from combine_quant_gb300 import workloads
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU (the CUDA path has no CPU fallback)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    wl = workloads.WORKLOADS[args.workload]()
+    cfg = cq.Config.from_dict(wl.cfg)
+    tdev = lambda a, dt: None if a is None else torch.from_numpy(  # noqa: E731
+        np.ascontiguousarray(a)).to(dev).view(dt)
+    x = tdev(wl.x, torch.bfloat16)
+    ids = tdev(wl.expert_ids, torch.int32)
+    w = tdev(wl.expert_scales, torch.float32)
+    sm = tdev(wl.smooth, torch.float32) if cfg.quant_mode == 2 else None
+    mask = tdev(wl.mask, torch.uint8)
+    bpr = tdev(wl.bs_per_rank, torch.int32)
+    ws = cq.alloc_workspace(cfg, dev)
+    out = cq.alloc_dispatch_outputs(cfg, dev)
+    pool = tdev(workloads.ffn_standin(wl.seed, 4096, cfg.hidden), torch.bfloat16)
+    ridx = (torch.arange(cfg.max_rows, device=dev, dtype=torch.int64) * 7919) % 4096
+    ffn = pool.index_select(0, ridx).contiguous()
+    y = torch.empty(cfg.ep_world_size, cfg.max_bs, cfg.hidden, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        cq.dispatch_route(cfg, ids, mask, bpr, workspace=ws, out=out)
+        if evs:
+            evs[1].record(stream)
+        cq.dispatch_permute(cfg, x, ids, sm, w, workspace=ws, out=out)
+        if evs:
+            evs[2].record(stream)
+        cq.combine(cfg, ffn, out.assist_info, w, out.ep_recv_count, ori_x=x, y=y)
+        if evs:
+            evs[3].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if cq.read_status(ws) != 0:
+        raise RuntimeError("device status reported a bad id or mask on the bench workload")
+    rows = int(cq.assist_views(cfg, out.assist_info)[2][-1].item())
+    tokens = wl.tokens
+    if wl.mask is not None:
+        tokens = int((wl.mask.reshape(cfg.ep_world_size, cfg.max_bs, -1).max(axis=2) > 0).sum())
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = ClockSampler(local, enabled=not args.no_clocks)
+    barrier()
+    clocks.start()
+    t_wall = time.perf_counter()
+    for k in range(args.steps):
+        flush.zero_()  # L2 flush between steps, outside the timed events
+        step(ev[k])
+    barrier()
+    t_wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    t_route = [e[0].elapsed_time(e[1]) for e in ev]
+    t_perm = [e[1].elapsed_time(e[2]) for e in ev]
+    t_comb = [e[2].elapsed_time(e[3]) for e in ev]
+    t_step = [e[0].elapsed_time(e[3]) for e in ev]
+    total_ms = sum(t_step)
+    if dist is not None:
+        tt = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / args.steps
+    value = world * tokens * args.steps / (total_ms / 1e3)
+
+    # End to end through cq_dispatch / cq_combine with host buffers: each step
+    # copies x, expert_ids and expert_scales from pinned memory and reads y back.
+    e2e = None
+    if not args.no_e2e:
+        hx = torch.from_numpy(np.ascontiguousarray(wl.x)).view(torch.bfloat16).pin_memory()
+        hids = torch.from_numpy(np.ascontiguousarray(wl.expert_ids)).pin_memory()
+        hw = torch.from_numpy(np.ascontiguousarray(wl.expert_scales)).pin_memory()
+        hy = torch.empty(y.shape, dtype=torch.bfloat16).pin_memory()
+        dx, dids, dw = torch.empty_like(x), torch.empty_like(ids), torch.empty_like(w)
+        n_e2e = max(10, min(args.steps, 500))
+
+        def e2e_step():
+            dx.copy_(hx, non_blocking=True)
+            dids.copy_(hids, non_blocking=True)
+            dw.copy_(hw, non_blocking=True)
+            o = cq.dispatch(cfg, dx, dids, smooth_scales=sm, x_active_mask=mask, bs_per_rank=bpr,
+                            expert_scales=dw, workspace=ws, out=out)
+            cq.combine(cfg, ffn, o.assist_info, dw, o.ep_recv_count, ori_x=dx, y=y)
+            hy.copy_(y, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        e_ms = e0.elapsed_time(e1)
+        if dist is not None:
+            tt = torch.tensor([e_ms], device=dev, dtype=torch.float64)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e_ms = float(tt.item())
+        e2e = {"value": world * tokens * n_e2e / (e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": hx.nbytes + hids.nbytes + hw.nbytes,
+               "d2h_bytes_per_step": hy.nbytes, "steps": n_e2e,
+               "api": "cq_dispatch + cq_combine (libcq C ABI via ctypes)"}
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    ab = algorithmic_bytes(cfg, rows, tokens, with_scales=True)
+    means = {"route": statistics.mean(t_route), "permute": statistics.mean(t_perm),
+             "combine": statistics.mean(t_comb)}
+    peak, peak_kind = measured_peaks()
+    kernels = {k: {"us": 1e3 * means[k], "alg_bytes": ab[k],
+                   "gbs": ab[k] / (means[k] * 1e-3) / 1e9,
+                   "frac": ab[k] / (means[k] * 1e-3) / 1e9 / peak} for k in means}
+    dom = max(("permute", "combine"), key=lambda k: means[k])
+    roof = {"kernel": dom, "bound": "hbm", "achieved": kernels[dom]["gbs"], "peak": peak,
+            "unit": "GB/s", "frac": kernels[dom]["frac"], "traffic": ncu_traffic(dom),
+            "peak_source": f"hbm_gbs of {peak_kind}"}
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        v, desc, cores = oracle_sample(wl, args.cpu_seconds)
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+
+    emit({"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+          "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+          "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+          "config": {"workload": workload_desc(wl), "tokens_per_step": tokens,
+                     "rows_per_step": rows, "io": "bf16 tokens in, int8 codes + f32 scales "
+                     "on the wire, bf16 out", "l2": "flushed between steps (256 MiB write)",
+                     "parallelism": f"{world} independent replica(s), logical ranks on-device"},
+          "per_call_us": {"dispatch": 1e3 * (means["route"] + means["permute"]),
+                          "combine": 1e3 * means["combine"]},
+          "kernels": kernels, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+          "gpu_launches": 3 * args.steps, "clocks": clk, "wall_s": t_wall})
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_cq(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

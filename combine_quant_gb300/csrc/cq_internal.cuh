@@ -1,0 +1,109 @@
+// cq_internal.cuh -- internal definitions shared by the libcq translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "cq.h"
+
+namespace cq {
+
+// Derived problem sizes, computed once on the host per call.
+struct Dims {
+  int32_t W, M, S_eff, S_r, R_rep;  // R_rep: replicas per shared expert (S_r / S)
+  int32_t Z, C, Q, BS, K, H, L, NS, G;  // G = S_r + M global expert slots
+  int32_t mode, etn_type, mask_ndim;
+  int32_t SC;                     // mx scale columns
+  int64_t R_max;
+};
+
+// Workspace layout (byte offsets, each segment 256-byte aligned).
+//   hdr      : uint32 status, uint32 done counter, int32 total rows, pad
+//   counts_t : int32 [G][W]  per (global expert slot, source rank) row counts
+//   blockoff : int32 [G][W]  first global row of each (slot, source) block
+//   eidx     : int32 [W*BS*NS] arrival ordinal of each slot, or a CQ_INV code
+struct Workspace {
+  uint32_t* status;
+  uint32_t* done;
+  int32_t* total;
+  int32_t* counts_t;
+  int32_t* blockoff;
+  int32_t* eidx;
+};
+
+constexpr size_t kHdrBytes = 256;
+inline size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
+
+inline size_t workspace_bytes(const Dims& d) {
+  size_t b = kHdrBytes;
+  b += align256(sizeof(int32_t) * (size_t)d.G * d.W);
+  b += align256(sizeof(int32_t) * (size_t)d.G * d.W);
+  b += align256(sizeof(int32_t) * (size_t)d.W * d.BS * d.NS);
+  return b;
+}
+
+inline Workspace carve(void* base, const Dims& d) {
+  char* p = static_cast<char*>(base);
+  Workspace w;
+  w.status = reinterpret_cast<uint32_t*>(p);
+  w.done = reinterpret_cast<uint32_t*>(p + 4);
+  w.total = reinterpret_cast<int32_t*>(p + 8);
+  p += kHdrBytes;
+  w.counts_t = reinterpret_cast<int32_t*>(p);
+  p += align256(sizeof(int32_t) * (size_t)d.G * d.W);
+  w.blockoff = reinterpret_cast<int32_t*>(p);
+  p += align256(sizeof(int32_t) * (size_t)d.G * d.W);
+  w.eidx = reinterpret_cast<int32_t*>(p);
+  return w;
+}
+
+// assist_info layout: [R_max][4] rows, then inv [W*BS*NS], then rank_row_base [W+1].
+inline int64_t assist_rows_off(const Dims&) { return 0; }
+inline int64_t assist_inv_off(const Dims& d) { return 4 * d.R_max; }
+inline int64_t assist_base_off(const Dims& d) { return 4 * d.R_max + (int64_t)d.W * d.BS * d.NS; }
+inline int64_t assist_size(const Dims& d) { return assist_base_off(d) + d.W + 1; }
+
+struct RouteArgs {
+  Dims d;
+  const int32_t* expert_ids;
+  const uint8_t* mask;
+  const int32_t* bs_per_rank;
+  int32_t* ep_recv_count;
+  int64_t* expert_token_nums;
+  int32_t* rank_row_base;  // inside assist_info
+  Workspace ws;
+};
+
+struct PermuteArgs {
+  Dims d;
+  const uint16_t* x;
+  const int32_t* expert_ids;
+  const float* smooth;
+  const float* expert_scales;
+  void* expand_x;
+  void* dynamic_scales;
+  int32_t* assist_rows;  // [R_max][4]
+  int32_t* inv;          // [W*BS*NS]
+  float* expand_scales;
+  Workspace ws;
+};
+
+struct CombineArgs {
+  Dims d;
+  const uint16_t* ffn;
+  const int32_t* inv;
+  const float* expert_scales;
+  const uint16_t* ori_x;
+  const float* alpha1;
+  const float* alpha2;
+  const uint16_t* const_v;
+  void* y;
+  int32_t out_f32;
+};
+
+// Launchers (each returns the cudaError_t of its launch).
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
+cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t s);
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);
+
+}  // namespace cq

@@ -150,8 +150,8 @@ def mxfp8(seed: int = 2, W: int = 64, BS: int = 512, M: int = 256, K: int = 8,
                     w.reshape(W, BS, K), seed=seed)
 
 
-def special(seed: int = 3, W: int = 16, BS: int = 256, H: int = 4096) -> Workload:
-    Sr, S, M, Z, C, Q, K = 2, 1, 112, 1, 1, 1, 6
+def special(seed: int = 3, W: int = 16, BS: int = 256, H: int = 4096, M: int = 112) -> Workload:
+    Sr, S, Z, C, Q, K = 2, 1, 1, 1, 1, 6
     rng = np.random.Generator(np.random.PCG64(seed))
     cfg = make_config(ep_world_size=W, moe_expert_num=M, shared_expert_num=S,
                       shared_expert_rank_num=Sr, zero_expert_num=Z, copy_expert_num=C,

@@ -1,0 +1,209 @@
+/*
+ * cq.h -- C ABI of libcq: MoE dispatch / combine with pre-communication
+ * quantisation, for one GB300 (sm_103a) holding every logical EP rank.
+ *
+ * The operation is the one described by these pages (cited by title and
+ * section throughout):
+ *   [DV3]  "CANN ops-transformer 算子解析：MoeDistributeDispatchV3 的 EP 域
+ *           Token 分发与动态量化通信实现"
+ *   [DSN]  "MoeDistributeDispatch和MoeDistributeCombine算子设计介绍"
+ *   [LLD]  "low_latency_dispatch" (CANN API reference page)
+ *   [PERF] "CANN MoE Dispatch/Combine 通信算子性能优化实践：Kernel 直调与
+ *           ACL SHMEM 实现专家分发与聚合"
+ *
+ * Logical ranks. ep_world_size = W ranks share one device. Every per-rank
+ * tensor of the pages gains a leading rank axis, and the all-to-all exchange
+ * becomes an on-device scatter: the rows received by rank d occupy the
+ * global row range [rank_row_base[d], rank_row_base[d+1]) of expand_x.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers, row-major, contiguous, owned
+ *     by the caller. The library never allocates or frees memory.
+ *   - `stream` is a cudaStream_t passed as void*. Work is enqueued on it and
+ *     the call returns without synchronising (except cq_read_status).
+ *   - Return 0 (CQ_OK) or a negative CQ_ERR_* code. Argument errors are found
+ *     on the host before anything is enqueued; nothing is enqueued then.
+ *   - Data-dependent problems found on the device (an out-of-range expert
+ *     id, a 1-D mask that is not a prefix) never trap: they set sticky bits in
+ *     the workspace status word, read with cq_read_status.
+ *
+ * Notation: W = ep_world_size, M = moe_expert_num, S = shared_expert_num,
+ * S_r = shared_expert_rank_num, L = M / (W - S_r) experts per MoE rank,
+ * BS = max_bs, K = topk, H = hidden, NS = K + (S_r > 0 ? S : 0) slots per
+ * token, R_max = W * BS * NS (bound on dispatched rows, all ranks together),
+ * SC = Align2(Ceil(H, 32)) mx scale columns.
+ */
+#ifndef CQ_H
+#define CQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Operator attributes, [DV3] 参数说明 / [LLD] parameter list. */
+typedef struct cq_config {
+  int32_t ep_world_size;          /* W in [2, 768] */
+  int32_t moe_expert_num;         /* M in [1, 1024], M % (W - S_r) == 0, L * W <= 2048 */
+  int32_t shared_expert_num;      /* S in [0, 4]; with S_r == 0 only 0 or 1 (ignored) */
+  int32_t shared_expert_rank_num; /* S_r in [0, W); S_r % S == 0 and W % S_r == 0 */
+  int32_t zero_expert_num;        /* Z >= 0: ids [M, M+Z) give Moe(x) = 0 */
+  int32_t copy_expert_num;        /* C >= 0: ids [M+Z, M+Z+C) give Moe(x) = x */
+  int32_t const_expert_num;       /* Q >= 0: ids [M+Z+C, M+Z+C+Q) give a1*x + a2*v */
+  int32_t max_bs;                 /* BS in [1, 512], tokens per rank (maximum) */
+  int32_t topk;                   /* K in [1, 16], K <= M + Z + C + Q */
+  int32_t hidden;                 /* H in [1024, 8192]; this build needs H % 16 == 0
+                                     (H % 32 == 0 for quant_mode 5) */
+  int32_t global_bs;              /* 0 or BS * W ([DV3] global_bs) */
+  int32_t quant_mode;             /* 0 none, 2 per-token int8, 5 mx-clip e4m3 */
+  int32_t expert_token_nums_type; /* 0 cumulative sums, 1 counts */
+  int32_t mask_ndim;              /* 0 none, 1 per token [W,BS], 2 per pair [W,BS,K] */
+} cq_config;
+
+enum {
+  CQ_OK = 0,
+  CQ_ERR_ARG = -1,         /* a range or divisibility rule broken, or a required pointer NULL */
+  CQ_ERR_UNSUPPORTED = -2, /* quant_mode 1/3/4, or H not a multiple of 16 (32 for mode 5) */
+  CQ_ERR_CUDA = -3,        /* a CUDA launch or query failed */
+  CQ_ERR_WORKSPACE = -4    /* workspace smaller than cq_workspace_size() or misaligned */
+};
+
+/* Sticky device status bits (cq_read_status). */
+enum {
+  CQ_ST_BAD_ID = 1,  /* an active pair named an id outside [0, M+Z+C+Q); it was skipped */
+  CQ_ST_BAD_MASK = 2, /* a 1-D x_active_mask had a true entry after a false one
+                         ([DV3] x_active_mask_optional); entries were honoured as given */
+  CQ_ST_INTERNAL = 4   /* a computed row or code fell outside its buffer (an internal
+                          consistency guard); the access was skipped */
+};
+
+/* Codes stored in the inverse map for slots that own no dispatched row. */
+enum { CQ_INV_NONE = -1, CQ_INV_COPY = -2, CQ_INV_CONST_BASE = -3 /* const c -> -3 - c */ };
+
+/* Validate a config; CQ_OK or CQ_ERR_ARG / CQ_ERR_UNSUPPORTED. */
+int cq_check_config(const cq_config* cfg);
+
+/* Derived sizes (no validation beyond what they need; 0 or -1 on NULL). */
+int32_t cq_local_expert_num(const cq_config* cfg); /* L */
+int32_t cq_num_slots(const cq_config* cfg);        /* NS */
+int64_t cq_max_rows(const cq_config* cfg);         /* R_max */
+int32_t cq_scale_cols(const cq_config* cfg);       /* SC */
+int64_t cq_assist_info_size(const cq_config* cfg); /* int32 elements of assist_info */
+size_t cq_workspace_size(const cq_config* cfg);    /* bytes */
+
+/* Zero-fill a freshly allocated workspace (enqueued on `stream`). Required
+ * once before its first use; the library keeps it consistent afterwards.
+ * Returns CQ_ERR_ARG if workspace is NULL. */
+int cq_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * cq_dispatch -- routing scan + permute + pre-communication quantisation.
+ * [DSN] §2.2 (sendStatus scan, expandIdx, MoePermute), §2.4 (ep_recv_count as
+ * the transposed received-count matrix prefix-summed row-major, expert token
+ * numbers), [DV3] 功能说明 情形 1 / 情形 2 and [LLD] 计算公式 quant_mode 0, 2, 5.
+ *
+ * Inputs:
+ *   x              bf16 [W, BS, H]  tokens of every logical rank
+ *   expert_ids     int32 [W, BS, K] routed expert ids (MoE, zero, copy, const ranges)
+ *   smooth_scales  f32 [(S_r>0 ? S : 0) + M, H] or NULL; mode 2 only. Shared
+ *                  expert s uses row s, MoE expert e row (S_r>0 ? S : 0) + e.
+ *   x_active_mask  uint8 [W, BS] (mask_ndim 1) or [W, BS, K] (2), or NULL
+ *   bs_per_rank    int32 [W] tokens of each rank (<= BS), or NULL for all BS
+ *   expert_scales  f32 [W, BS, K] routing weights, or NULL (expand_scales
+ *                  then unused)
+ * Outputs (rows past the true total are left untouched):
+ *   expand_x       [R_max, H]: bf16 (mode 0), int8 (mode 2), e4m3 bytes (mode 5).
+ *                  Rank d's rows, expert-contiguous (local expert ascending,
+ *                  then source rank ascending, then arrival order).
+ *   dynamic_scales f32 [R_max] dequantisation multipliers (mode 2), or
+ *                  uint8 e8m0 [R_max, SC] block scales 2^e stored as e+127
+ *                  (mode 5, pad column 0); ignored in mode 0 (may be NULL).
+ *   assist_info    int32 [cq_assist_info_size()]: pass unchanged to cq_combine.
+ *                  Layout: [R_max][4] rows (src_rank, src_token, slot, 0);
+ *                  then inv [W, BS, NS] (row of each slot or a CQ_INV_* code);
+ *                  then rank_row_base [W + 1].
+ *   ep_recv_count  int32 [W, W * L]: per destination rank d, the inclusive
+ *                  running row count over (local expert, source rank),
+ *                  local-expert major; a shared-expert rank fills W entries.
+ *   expert_token_nums int64 [W, L]: per rank, rows per local expert (type 1)
+ *                  or their running sum (type 0); shared ranks fill 1 entry.
+ *   expand_scales  f32 [R_max] or NULL: the routing weight of each row
+ *                  (1.0 on shared-expert rows).
+ *   workspace      >= cq_workspace_size() bytes, 256-byte aligned, zero-filled
+ *                  once by cq_workspace_init before first use.
+ */
+int cq_dispatch(const cq_config* cfg, const void* x, const int32_t* expert_ids,
+                const float* smooth_scales, const uint8_t* x_active_mask,
+                const int32_t* bs_per_rank, const float* expert_scales, void* expand_x,
+                void* dynamic_scales, int32_t* assist_info, int32_t* ep_recv_count,
+                int64_t* expert_token_nums, float* expand_scales, void* workspace,
+                size_t workspace_bytes, void* stream);
+
+/* The two halves of cq_dispatch, same arguments; calling cq_dispatch_route
+ * then cq_dispatch_permute on one stream is exactly cq_dispatch.
+ * route: scan, counts, prefix sums (writes ep_recv_count, expert_token_nums,
+ *        the rank_row_base part of assist_info, and the workspace);
+ * permute: row placement and quantisation (writes expand_x, dynamic_scales,
+ *        the rows and inv parts of assist_info, expand_scales). */
+int cq_dispatch_route(const cq_config* cfg, const int32_t* expert_ids,
+                      const uint8_t* x_active_mask, const int32_t* bs_per_rank,
+                      int32_t* assist_info, int32_t* ep_recv_count, int64_t* expert_token_nums,
+                      void* workspace, size_t workspace_bytes, void* stream);
+int cq_dispatch_permute(const cq_config* cfg, const void* x, const int32_t* expert_ids,
+                        const float* smooth_scales, const float* expert_scales,
+                        void* expand_x, void* dynamic_scales, int32_t* assist_info,
+                        float* expand_scales, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
+/*
+ * cq_combine -- inverse permute + top-K weighted sum.
+ * [DSN] §3.4 (locate each expert output of token i, weighted sum), [PERF]
+ * Combine 计算步骤 (multiply by expert_scales, sum in float, add the shared
+ * outputs), [LLD] 特殊专家场景 (zero / copy / const experts).
+ *
+ *   y[r,i,:] = cast( sum_{j<K} w[r,i,j] * v_j  +  sum_{s<S} shared_s )
+ * accumulated in fp32 with one fused multiply-add per j, j ascending, then
+ * the shared rows added in s order. v_j is expand_x_ffn[row] for a MoE
+ * expert, 0 for a zero expert, ori_x[r,i] for a copy expert, and
+ * alpha1[c]*ori_x + alpha2[c]*const_v[c] (products then sum, each rounded)
+ * for const expert c. Inactive tokens give 0.
+ *
+ *   expand_x_ffn   bf16 [R_max, H] expert outputs, row-aligned with expand_x
+ *   assist_info    as written by cq_dispatch
+ *   ep_recv_count  as written by cq_dispatch, or NULL (the row map inside
+ *                  assist_info already locates every row)
+ *   expert_scales  f32 [W, BS, K]
+ *   ori_x          bf16 [W, BS, H]; required when C + Q > 0, else may be NULL
+ *   const_alpha1, const_alpha2  f32 [Q]; const_v bf16 [Q, H]; required when Q > 0
+ *   out_dtype      0: y is bf16 [W, BS, H]; 1: y is f32 [W, BS, H]
+ */
+int cq_combine(const cq_config* cfg, const void* expand_x_ffn, const int32_t* assist_info,
+               const int32_t* ep_recv_count, const float* expert_scales, const void* ori_x,
+               const float* const_alpha1, const float* const_alpha2, const void* const_v,
+               int32_t out_dtype, void* y, void* stream);
+
+/* The spec names of the two operators: identical to cq_dispatch / cq_combine. */
+int moe_dispatch(const cq_config* cfg, const void* x, const int32_t* expert_ids,
+                 const float* smooth_scales, const uint8_t* x_active_mask,
+                 const int32_t* bs_per_rank, const float* expert_scales, void* expand_x,
+                 void* dynamic_scales, int32_t* assist_info, int32_t* ep_recv_count,
+                 int64_t* expert_token_nums, float* expand_scales, void* workspace,
+                 size_t workspace_bytes, void* stream);
+int moe_combine(const cq_config* cfg, const void* expand_x_ffn, const int32_t* assist_info,
+                const int32_t* ep_recv_count, const float* expert_scales, const void* ori_x,
+                const float* const_alpha1, const float* const_alpha2, const void* const_v,
+                int32_t out_dtype, void* y, void* stream);
+
+/* Synchronise `stream`, copy the workspace status word into *status and clear
+ * it. The only call in this library that waits for the device. */
+int cq_read_status(void* workspace, uint32_t* status, void* stream);
+
+/* Static description of an error code. */
+const char* cq_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CQ_H */

@@ -72,10 +72,12 @@ int cqo_check_config(const cqo_config* c) {
   if (c->topk > all) return CQO_ERR_ARG;
   /* [DV3] 参数说明 global_bs: 0 or max_bs * ep_world_size. */
   if (c->global_bs != 0 && c->global_bs != c->max_bs * W) return CQO_ERR_ARG;
-  if (c->quant_mode == 1 || c->quant_mode == 3 || c->quant_mode == 4) return CQO_ERR_UNSUPPORTED;
-  if (c->quant_mode != 0 && c->quant_mode != 2 && c->quant_mode != 5) return CQO_ERR_ARG;
   if (c->expert_token_nums_type != 0 && c->expert_token_nums_type != 1) return CQO_ERR_ARG;
   if (c->mask_ndim < 0 || c->mask_ndim > 2) return CQO_ERR_ARG;
+  /* Argument errors outrank "not implemented": modes 1, 3, 4 are defined by
+   * [LLD] but not built here. */
+  if (c->quant_mode == 1 || c->quant_mode == 3 || c->quant_mode == 4) return CQO_ERR_UNSUPPORTED;
+  if (c->quant_mode != 0 && c->quant_mode != 2 && c->quant_mode != 5) return CQO_ERR_ARG;
   return CQO_OK;
 }
 

@@ -1,0 +1,138 @@
+"""Helpers for the GPU parity tests: run the CUDA path through the C ABI and
+compare it with the oracle on the same seeded inputs."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import combine_quant_gb300 as cq
+import oracle
+from combine_quant_gb300 import workloads
+
+DEV = torch.device("cuda:0")
+
+
+def dev(a, dtype):
+    """numpy array (raw bits allowed) -> CUDA tensor of `dtype`."""
+    if a is None:
+        return None
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    return t.to(DEV).view(dtype)
+
+
+def host(t: torch.Tensor) -> np.ndarray:
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).cpu().numpy().view(np.uint16)
+    return t.cpu().numpy()
+
+
+def gpu_dispatch(wl: workloads.Workload):
+    cfg = cq.Config.from_dict(wl.cfg)
+    x = dev(wl.x, torch.bfloat16)
+    ids = dev(wl.expert_ids, torch.int32)
+    sm = dev(wl.smooth, torch.float32) if wl.cfg["quant_mode"] == 2 else None
+    mask = dev(wl.mask, torch.uint8)
+    bpr = dev(wl.bs_per_rank, torch.int32)
+    w = dev(wl.expert_scales, torch.float32)
+    ws = cq.alloc_workspace(cfg, DEV)
+    out = cq.dispatch(cfg, x, ids, smooth_scales=sm, x_active_mask=mask, bs_per_rank=bpr,
+                      expert_scales=w, workspace=ws)
+    status = cq.read_status(ws)
+    return cfg, out, status, ws
+
+
+def compare_route(wl, cfg, out, ref_route):
+    """Bit-exact comparison of every index / count output."""
+    rows, inv, base = cq.assist_views(cfg, out.assist_info)
+    R = ref_route.rows
+    assert int(host(base)[-1]) == R, "total rows"
+    assert np.array_equal(host(base), ref_route.rank_row_base.astype(np.int32))
+    assert np.array_equal(host(out.ep_recv_count), ref_route.ep_recv_count)
+    assert np.array_equal(host(out.expert_token_nums), ref_route.expert_token_nums)
+    assert np.array_equal(host(inv), ref_route.inv)
+    assert np.array_equal(host(rows[:R]), ref_route.assist[:R])
+
+
+def smooth_row(wl, src, tok, k):
+    if wl.smooth is None or wl.cfg["quant_mode"] != 2:
+        return None
+    K = wl.cfg["topk"]
+    s_eff = wl.cfg["shared_expert_num"] if wl.cfg["shared_expert_rank_num"] > 0 else 0
+    return wl.smooth[s_eff + wl.expert_ids[src, tok, k]] if k < K else wl.smooth[k - K]
+
+
+def compare_rows(wl, out, ref_route, sample):
+    """expand_x / dynamic_scales / expand_scales of the sampled rows against
+    the oracle's quantisation of their source tokens."""
+    mode = wl.cfg["quant_mode"]
+    K = wl.cfg["topk"]
+    sample = np.asarray(sorted(set(int(s) for s in sample)), np.int64)
+    if sample.size == 0:
+        return 0
+    idx = torch.from_numpy(sample).to(DEV)
+    ex = host(out.expand_x.index_select(0, idx))
+    dyn = host(out.dynamic_scales.index_select(0, idx)) if out.dynamic_scales is not None else None
+    es = host(out.expand_scales.index_select(0, idx)) if out.expand_scales is not None else None
+    for n, row in enumerate(sample):
+        src, tok, k = ref_route.assist[row, :3]
+        codes, scale = oracle.quant_row(mode, wl.x[src, tok], smooth_row(wl, src, tok, k))
+        assert np.array_equal(ex[n].view(codes.dtype), codes), f"expand_x row {row}"
+        if mode == 2:
+            assert dyn[n] == scale, f"dynamic_scales row {row}"
+        elif mode == 5:
+            assert np.array_equal(dyn[n], scale), f"mx scales row {row}"
+        if es is not None:
+            want = wl.expert_scales[src, tok, k] if k < K else np.float32(1.0)
+            assert es[n] == want, f"expand_scales row {row}"
+    return sample.size
+
+
+def sample_rows(ref_route, rng, n_random=256):
+    R = ref_route.rows
+    if R == 0:
+        return []
+    base = ref_route.rank_row_base
+    picks = list(range(min(32, R))) + list(range(max(0, R - 32), R))
+    picks += [int(b) for b in base[:-1] if b < R] + [int(b) - 1 for b in base[1:] if b > 0]
+    picks += list(rng.integers(0, R, n_random))
+    return picks
+
+
+class FfnStandin:
+    """Expert-output stand-in: row n of expand_x_ffn is pool[(n * 7919) % P]
+    for a seeded random pool of P bf16 rows. The device copy is gathered on
+    the GPU; the oracle reads the pool through a remapped row table, which
+    leaves its arithmetic unchanged."""
+
+    def __init__(self, wl, max_rows: int, pool_rows: int = 4096):
+        self.pool = workloads.ffn_standin(wl.seed, pool_rows, wl.cfg["hidden"])
+        self.P = pool_rows
+        idx = (torch.arange(max_rows, dtype=torch.int64, device=DEV) * 7919) % pool_rows
+        self.device_rows = dev(self.pool, torch.bfloat16).index_select(0, idx).contiguous()
+
+    def remap_inv(self, inv: np.ndarray) -> np.ndarray:
+        inv = inv.astype(np.int64)
+        return np.where(inv >= 0, (inv * 7919) % self.P, inv).astype(np.int32)
+
+
+def gpu_combine(wl, cfg, out, ffn: FfnStandin, out_dtype):
+    w = dev(wl.expert_scales, torch.float32)
+    return cq.combine(cfg, ffn.device_rows, out.assist_info, w, out.ep_recv_count,
+                      ori_x=dev(wl.x, torch.bfloat16),
+                      const_alpha1=dev(wl.const_alpha1, torch.float32),
+                      const_alpha2=dev(wl.const_alpha2, torch.float32),
+                      const_v=dev(wl.const_v, torch.bfloat16), out_dtype=out_dtype)
+
+
+def oracle_combine_tokens(wl, ref_route, ffn: FfnStandin, tokens, out_f32):
+    return oracle.combine_tokens(wl.cfg, tokens, ffn.pool, ffn.remap_inv(ref_route.inv),
+                                 wl.expert_scales, wl.x, wl.const_alpha1, wl.const_alpha2,
+                                 wl.const_v, out_f32=out_f32)
+
+
+def bf16_ulp_diff(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:
+    """Distance in units of bf16 ordering between two bf16 bit arrays."""
+    def key(b):
+        b = b.astype(np.int32)
+        return np.where(b & 0x8000, -(b & 0x7fff), b & 0x7fff)
+    return np.abs(key(a_bits) - key(b_bits))

@@ -1,0 +1,149 @@
+"""Host-side checks of the C ABI: the library loads, exports every symbol that
+include/cq.h declares, and its host logic (argument validation, derived
+sizes) behaves as specified. No call here touches a GPU."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+from combine_quant_gb300 import _lib, build as cqbuild
+from combine_quant_gb300.workloads import make_config
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cqbuild.build()
+    return _lib.load()
+
+
+def _declared():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if not f.endswith(".h"):
+            continue
+        txt = open(os.path.join(ROOT, "include", f)).read()
+        txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s+\*?([A-Za-z_]\w*)\s*\(",
+                             txt, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    declared = _declared()
+    assert set(_lib.EXPORTS) <= declared
+    for name in declared:
+        assert hasattr(lib, name), f"libcq.so does not export {name}"
+
+
+def _c(cfg):
+    return ctypes.byref(_lib.CqConfig(**cfg))
+
+
+def _random_cfg(rng):
+    W = int(rng.choice([2, 3, 4, 8, 16, 32, 64, 768, 769, 1]))
+    Sr = int(rng.choice([0, 0, 1, 2, W // 2, W]))
+    S = int(rng.choice([0, 1, 2, 3, 5]))
+    L = int(rng.choice([1, 2, 3, 8]))
+    M = int(max(1, (W - Sr) * L + int(rng.choice([0, 0, 0, 1]))))
+    return make_config(
+        ep_world_size=W, moe_expert_num=M, shared_expert_num=S, shared_expert_rank_num=Sr,
+        zero_expert_num=int(rng.choice([0, 1, -1])), copy_expert_num=int(rng.choice([0, 2])),
+        const_expert_num=int(rng.choice([0, 1])), max_bs=int(rng.choice([1, 128, 512, 513, 0])),
+        topk=int(rng.choice([1, 8, 16, 17])), hidden=int(rng.choice([1024, 7168, 8192, 1000, 8320])),
+        global_bs=int(rng.choice([0, 0, 5])), quant_mode=int(rng.choice([0, 1, 2, 3, 4, 5, 6])),
+        expert_token_nums_type=int(rng.choice([0, 1, 2])), mask_ndim=int(rng.choice([0, 1, 2, 3])))
+
+
+def test_validation_agrees_with_oracle(lib, oracle_lib):
+    """Two independent implementations of the pages' argument rules agree
+    (the CUDA library additionally needs H % 16 == 0, and H % 32 for mode 5)."""
+    rng = np.random.default_rng(0)
+    n_ok = 0
+    for _ in range(3000):
+        cfg = _random_cfg(rng)
+        want = oracle.check_config(cfg)
+        got = lib.cq_check_config(_c(cfg))
+        if want == 0 and (cfg["hidden"] % 16 or (cfg["quant_mode"] == 5 and cfg["hidden"] % 32)):
+            want = _lib.CQ_ERR_UNSUPPORTED
+        assert got == want, cfg
+        n_ok += got == 0
+    assert n_ok >= 5  # the sweep reaches valid configs too, not only rejections
+
+
+@pytest.mark.parametrize("name", ["dsv3", "mxfp8", "special", "skew"])
+def test_derived_sizes(lib, oracle_lib, name):
+    from combine_quant_gb300 import workloads
+    cfgs = {
+        "dsv3": make_config(ep_world_size=32, moe_expert_num=256, max_bs=128, topk=8, hidden=7168,
+                            quant_mode=2),
+        "mxfp8": make_config(ep_world_size=64, moe_expert_num=256, max_bs=512, topk=8,
+                             hidden=7168, quant_mode=5),
+        "special": make_config(ep_world_size=16, moe_expert_num=112, shared_expert_num=1,
+                               shared_expert_rank_num=2, zero_expert_num=1, copy_expert_num=1,
+                               const_expert_num=1, max_bs=256, topk=6, hidden=4096,
+                               expert_token_nums_type=0, mask_ndim=1),
+        "skew": make_config(ep_world_size=16, moe_expert_num=128, max_bs=512, topk=16,
+                            hidden=8192, global_bs=8192, quant_mode=2),
+    }
+    cfg = cfgs[name]
+    assert workloads.CONFIG_FIELDS == _lib.CONFIG_FIELDS
+    c = _c(cfg)
+    assert lib.cq_check_config(c) == 0
+    assert lib.cq_max_rows(c) == oracle.max_rows(cfg)
+    assert lib.cq_num_slots(c) == oracle.num_slots(cfg)
+    assert lib.cq_local_expert_num(c) == oracle.local_expert_num(cfg)
+    assert lib.cq_scale_cols(c) == oracle.scale_cols(cfg)
+    W, BS, NS = cfg["ep_world_size"], cfg["max_bs"], oracle.num_slots(cfg)
+    assert lib.cq_assist_info_size(c) == 4 * oracle.max_rows(cfg) + W * BS * NS + W + 1
+    assert lib.cq_workspace_size(c) > 0
+
+
+def test_host_errors_before_any_device_work(lib):
+    """Invalid arguments are rejected on the host (these calls would fault if
+    they reached the device: the pointers are fake)."""
+    cfg = make_config(ep_world_size=4, moe_expert_num=8, max_bs=8, topk=2, hidden=1024,
+                      quant_mode=2)
+    fake = ctypes.c_void_p(0x10000)
+    args = [fake] * 13
+    bad = dict(cfg, topk=0)
+    assert lib.cq_dispatch(_c(bad), *args, 1 << 20, None) == _lib.CQ_ERR_ARG
+    assert lib.cq_dispatch(_c(dict(cfg, quant_mode=3)), *args, 1 << 20, None) == \
+        _lib.CQ_ERR_UNSUPPORTED
+    # workspace too small
+    assert lib.cq_dispatch(_c(cfg), *args, 16, None) == _lib.CQ_ERR_WORKSPACE
+    # x missing
+    a2 = list(args)
+    a2[0] = None
+    assert lib.cq_dispatch(_c(cfg), *a2, 1 << 20, None) == _lib.CQ_ERR_ARG
+    # smooth scales with an mx mode
+    assert lib.cq_dispatch(_c(dict(cfg, quant_mode=5)), *args, 1 << 20, None) == _lib.CQ_ERR_ARG
+    # mask_ndim set without a mask
+    a3 = list(args)
+    a3[3] = None
+    assert lib.cq_dispatch(_c(dict(cfg, mask_ndim=1)), *a3, 1 << 20, None) == _lib.CQ_ERR_ARG
+    # combine: copy experts need ori_x
+    cargs = [fake] * 8
+    cargs[4] = None
+    assert lib.cq_combine(_c(dict(cfg, copy_expert_num=1)), *cargs, 0, fake, None) == \
+        _lib.CQ_ERR_ARG
+    assert lib.cq_combine(_c(cfg), *([fake] * 8), 2, fake, None) == _lib.CQ_ERR_ARG
+    assert lib.cq_read_status(None, None, None) == _lib.CQ_ERR_ARG
+    assert lib.cq_workspace_init(None, 0, None) == _lib.CQ_ERR_ARG
+    for code in (0, -1, -2, -3, -4, -99):
+        assert isinstance(lib.cq_strerror(code), bytes)
+
+
+def test_python_config_roundtrip(lib):
+    from combine_quant_gb300 import Config
+    cfg = make_config(ep_world_size=16, moe_expert_num=112, shared_expert_num=1,
+                      shared_expert_rank_num=2, max_bs=256, topk=6, hidden=4096)
+    c = Config.from_dict(cfg)
+    assert c.check() == 0
+    assert c.local_expert_num == 8 and c.num_slots == 7
+    assert c.max_rows == 16 * 256 * 7
