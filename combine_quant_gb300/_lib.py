@@ -22,6 +22,8 @@ CQ_ERR_ARG = -1
 CQ_ERR_UNSUPPORTED = -2
 CQ_ERR_CUDA = -3
 CQ_ERR_WORKSPACE = -4
+CQ_ERR_TOO_LARGE = -5
+NOALLOC_SCRATCH_BYTES = 4 << 20
 CQ_ST_BAD_ID = 1
 CQ_ST_BAD_MASK = 2
 CQ_ST_INTERNAL = 4
@@ -34,7 +36,7 @@ EXPORTS = (
     "cq_check_config", "cq_local_expert_num", "cq_num_slots", "cq_max_rows", "cq_scale_cols",
     "cq_assist_info_size", "cq_workspace_size", "cq_workspace_init", "cq_dispatch",
     "cq_dispatch_route", "cq_dispatch_permute", "cq_combine", "moe_dispatch", "moe_combine",
-    "cq_read_status", "cq_strerror",
+    "cq_read_status", "cq_strerror", "cq_dispatch_noalloc",
 )
 
 
@@ -79,6 +81,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "cq_combine": ([cfgp] + [P] * 8 + [i32, P, P], ctypes.c_int),
         "moe_combine": ([cfgp] + [P] * 8 + [i32, P, P], ctypes.c_int),
         "cq_read_status": ([P, P, P], ctypes.c_int),
+        "cq_dispatch_noalloc": ([cfgp] + [P] * 13, ctypes.c_int),
         "cq_strerror": ([ctypes.c_int], ctypes.c_char_p),
     }
     for name, (args, res) in sig.items():

@@ -21,7 +21,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libcq.so")
-SOURCES = ["cq_api.cu", "cq_route.cu", "cq_permute.cu", "cq_combine.cu"]
+SOURCES = ["cq_api.cu", "cq_route.cu", "cq_permute.cu", "cq_combine.cu", "cq_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -279,6 +279,7 @@ const char* cq_strerror(int code) {
     case CQ_ERR_UNSUPPORTED: return "unsupported configuration (quant_mode 1/3/4, or hidden size)";
     case CQ_ERR_CUDA: return "CUDA launch or query failed";
     case CQ_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case CQ_ERR_TOO_LARGE: return "problem needs more scratch than the built-in no-alloc buffer";
     default: return "unknown error";
   }
 }

@@ -67,7 +67,9 @@ enum {
   CQ_ERR_ARG = -1,         /* a range or divisibility rule broken, or a required pointer NULL */
   CQ_ERR_UNSUPPORTED = -2, /* quant_mode 1/3/4, or H not a multiple of 16 (32 for mode 5) */
   CQ_ERR_CUDA = -3,        /* a CUDA launch or query failed */
-  CQ_ERR_WORKSPACE = -4    /* workspace smaller than cq_workspace_size() or misaligned */
+  CQ_ERR_WORKSPACE = -4,   /* workspace smaller than cq_workspace_size() or misaligned */
+  CQ_ERR_TOO_LARGE = -5    /* cq_dispatch_noalloc: the problem needs more scratch than
+                              CQ_NOALLOC_SCRATCH_BYTES */
 };
 
 /* Sticky device status bits (cq_read_status). */
@@ -195,6 +197,39 @@ int moe_combine(const cq_config* cfg, const void* expand_x_ffn, const int32_t* a
                 const int32_t* ep_recv_count, const float* expert_scales, const void* ori_x,
                 const float* const_alpha1, const float* const_alpha2, const void* const_v,
                 int32_t out_dtype, void* y, void* stream);
+
+/*
+ * cq_dispatch_noalloc -- cq_dispatch for callers that cannot allocate device
+ * memory. The pages have no counterpart: it exists for this library's users.
+ *
+ * Who needs it: a caller that is handed only its input and output buffers and
+ * has no way to obtain a workspace -- a plugin inside a framework that owns
+ * every allocation, a serving process whose memory plan is fixed at start-up
+ * (cudaMalloc on the request path can synchronise the device and fragment the
+ * pool), an embedded deployment with a pre-planned memory map.
+ *
+ * Same arguments and outputs as cq_dispatch, minus the workspace: the scratch
+ * lives in a device array of CQ_NOALLOC_SCRATCH_BYTES built into libcq, which
+ * every GPU that loads the library holds until the process exits. The call
+ * allocates nothing and calls no allocating routine.
+ *   - Problems whose cq_workspace_size() exceeds CQ_NOALLOC_SCRATCH_BYTES are
+ *     rejected with CQ_ERR_TOO_LARGE before anything is enqueued (4 MiB covers
+ *     e.g. W=64, BS=512, K=8, M=256).
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current and caches it; make that
+ *     first call before any stream capture.
+ *   - All calls share the one array, and each call clears its header itself.
+ *     Calls that overlap on the GPU (other streams, other threads) race on it;
+ *     serialise them.
+ *   - The device status word of this variant is not reported; use cq_dispatch
+ *     with a workspace and cq_read_status when the status bits are needed.
+ */
+#define CQ_NOALLOC_SCRATCH_BYTES (4u << 20)
+int cq_dispatch_noalloc(const cq_config* cfg, const void* x, const int32_t* expert_ids,
+                        const float* smooth_scales, const uint8_t* x_active_mask,
+                        const int32_t* bs_per_rank, const float* expert_scales, void* expand_x,
+                        void* dynamic_scales, int32_t* assist_info, int32_t* ep_recv_count,
+                        int64_t* expert_token_nums, float* expand_scales, void* stream);
 
 /* Synchronise `stream`, copy the workspace status word into *status and clear
  * it. The only call in this library that waits for the device. */
