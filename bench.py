@@ -48,13 +48,17 @@ NCU_TRAFFIC = {}
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["cq", "reference"], default="cq")
     ap.add_argument("--workload", default="dsv3")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--flush", choices=["write+read", "write"], default="write+read",
+                    help="L2 flush between steps (outside the timed events)")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch each call directly instead of replaying CUDA graphs")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="host time budget of the oracle baseline")
     return ap.parse_args(argv)
@@ -298,21 +302,38 @@ def run_cq(args):
     ridx = (torch.arange(cfg.max_rows, device=dev, dtype=torch.int64) * 7919) % 4096
     ffn = pool.index_select(0, ridx).contiguous()
     y = torch.empty(cfg.ep_world_size, cfg.max_bs, cfg.hidden, dtype=torch.bfloat16, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    class _Flush:
+        """Between steps: write a buffer larger than L2, then (unless
+        --flush write) read another one, so that the next step starts with
+        no input resident in L2 and no dirty lines left to write back."""
+
+        @staticmethod
+        def zero_():
+            flush_w.zero_()
+            if args.flush == "write+read":
+                flush_r.amax()
+
+    flush = _Flush()
+
     def step(evs=None):
+        """One pass of the path. With 4 events, each kernel is bracketed (the
+        events between kernels also stop the next kernel from starting early);
+        with 2, only the step's start and end are recorded."""
         if evs:
             evs[0].record(stream)
         cq.dispatch_route(cfg, ids, mask, bpr, workspace=ws, out=out)
-        if evs:
+        if evs and len(evs) == 4:
             evs[1].record(stream)
-        cq.dispatch_permute(cfg, x, ids, sm, w, workspace=ws, out=out)
-        if evs:
+        cq.dispatch_permute(cfg, x, ids, sm, w, mask, bpr, workspace=ws, out=out)
+        if evs and len(evs) == 4:
             evs[2].record(stream)
         cq.combine(cfg, ffn, out.assist_info, w, out.ep_recv_count, ori_x=x, y=y)
         if evs:
-            evs[3].record(stream)
+            evs[-1].record(stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -325,21 +346,69 @@ def run_cq(args):
     if wl.mask is not None:
         tokens = int((wl.mask.reshape(cfg.ep_world_size, cfg.max_bs, -1).max(axis=2) > 0).sum())
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    # The launches of a step are captured into CUDA graphs (the whole step, and
+    # each kernel alone for the breakdown), so host-side enqueue time never
+    # shows up as device idle time inside the timed events.
+    use_graph = not args.no_graph
+    if use_graph:
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        graphs = {}
+        with torch.cuda.stream(side):
+            for name, fn in (
+                    ("step", step),
+                    ("route", lambda: cq.dispatch_route(cfg, ids, mask, bpr, workspace=ws,
+                                                        out=out)),
+                    ("permute", lambda: cq.dispatch_permute(cfg, x, ids, sm, w, mask, bpr,
+                                                            workspace=ws, out=out)),
+                    ("combine", lambda: cq.combine(cfg, ffn, out.assist_info, w,
+                                                   out.ep_recv_count, ori_x=x, y=y))):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=side):
+                    fn()
+                graphs[name] = g
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        run_step = graphs["step"].replay
+        parts = [graphs["route"].replay, graphs["permute"].replay, graphs["combine"].replay]
+    else:
+        run_step = step
+        parts = [lambda: cq.dispatch_route(cfg, ids, mask, bpr, workspace=ws, out=out),
+                 lambda: cq.dispatch_permute(cfg, x, ids, sm, w, mask, bpr, workspace=ws,
+                                             out=out),
+                 lambda: cq.combine(cfg, ffn, out.assist_info, w, out.ep_recv_count, ori_x=x,
+                                    y=y)]
+
+    # Per-kernel breakdown: events between the kernels.
+    n_bd = max(3, min(args.steps, 500))
+    evb = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_bd)]
+    barrier()
+    for k in range(n_bd):
+        flush.zero_()
+        for j, part in enumerate(parts):
+            evb[k][j].record(stream)
+            part()
+        evb[k][3].record(stream)
+    barrier()
+    t_route = [e[0].elapsed_time(e[1]) for e in evb]
+    t_perm = [e[1].elapsed_time(e[2]) for e in evb]
+    t_comb = [e[2].elapsed_time(e[3]) for e in evb]
+
+    # The timed region: K steps, events only at step boundaries.
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     clocks = ClockSampler(local, enabled=not args.no_clocks)
     barrier()
     clocks.start()
     t_wall = time.perf_counter()
     for k in range(args.steps):
         flush.zero_()  # L2 flush between steps, outside the timed events
-        step(ev[k])
+        ev[k][0].record(stream)
+        run_step()
+        ev[k][1].record(stream)
     barrier()
     t_wall = time.perf_counter() - t_wall
     clk = clocks.stop()
-    t_route = [e[0].elapsed_time(e[1]) for e in ev]
-    t_perm = [e[1].elapsed_time(e[2]) for e in ev]
-    t_comb = [e[2].elapsed_time(e[3]) for e in ev]
-    t_step = [e[0].elapsed_time(e[3]) for e in ev]
+    t_step = [e[0].elapsed_time(e[1]) for e in ev]
     total_ms = sum(t_step)
     if dist is not None:
         tt = torch.tensor([total_ms], device=dev, dtype=torch.float64)
@@ -414,10 +483,18 @@ def run_cq(args):
           "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
           "config": {"workload": workload_desc(wl), "tokens_per_step": tokens,
                      "rows_per_step": rows, "io": "bf16 tokens in, int8 codes + f32 scales "
-                     "on the wire, bf16 out", "l2": "flushed between steps (256 MiB write)",
-                     "parallelism": f"{world} independent replica(s), logical ranks on-device"},
+                     "on the wire, bf16 out",
+                     "l2": "flushed between steps: 256 MiB write" + (
+                         " then 256 MiB read (no dirty lines left)"
+                         if args.flush == "write+read" else ""),
+                     "parallelism": f"{world} independent replica(s), logical ranks on-device",
+                     "launch": "CUDA graph replay of the step's three libcq launches"
+                               if use_graph else "direct launches"},
           "per_call_us": {"dispatch": 1e3 * (means["route"] + means["permute"]),
-                          "combine": 1e3 * means["combine"]},
+                          "combine": 1e3 * means["combine"],
+                          "step_pipelined": 1e3 * ms_per_step,
+                          "note": "per-kernel figures come from a separate loop of "
+                                  f"{n_bd} steps with events between the kernels"},
           "kernels": kernels, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
           "gpu_launches": 3 * args.steps, "clocks": clk, "wall_s": t_wall})
     if dist is not None:

@@ -77,7 +77,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "cq_dispatch": ([cfgp] + [P] * 13 + [sz, P], ctypes.c_int),
         "moe_dispatch": ([cfgp] + [P] * 13 + [sz, P], ctypes.c_int),
         "cq_dispatch_route": ([cfgp] + [P] * 7 + [sz, P], ctypes.c_int),
-        "cq_dispatch_permute": ([cfgp] + [P] * 9 + [sz, P], ctypes.c_int),
+        "cq_dispatch_permute": ([cfgp] + [P] * 11 + [sz, P], ctypes.c_int),
         "cq_combine": ([cfgp] + [P] * 8 + [i32, P, P], ctypes.c_int),
         "moe_combine": ([cfgp] + [P] * 8 + [i32, P, P], ctypes.c_int),
         "cq_read_status": ([P, P, P], ctypes.c_int),

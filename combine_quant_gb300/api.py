@@ -7,6 +7,7 @@ passed in) and handed to the C entry points as raw pointers.
 from __future__ import annotations
 
 import ctypes
+import functools
 from dataclasses import asdict, dataclass, fields
 from typing import NamedTuple, Optional
 
@@ -39,7 +40,7 @@ class Config:
         return cls(**{k: int(v) for k, v in d.items() if k in names})
 
     def as_c(self) -> _lib.CqConfig:
-        return _lib.CqConfig(**asdict(self))
+        return _c_config(self)
 
     def _q(self, name):
         c = self.as_c()
@@ -74,6 +75,12 @@ class Config:
 
     def code_dtype(self) -> torch.dtype:
         return {0: torch.bfloat16, 2: torch.int8, 5: torch.uint8}[self.quant_mode]
+
+
+@functools.lru_cache(maxsize=256)
+def _c_config(cfg: Config) -> _lib.CqConfig:
+    """The C struct of a config, built once per distinct config (treat as read-only)."""
+    return _lib.CqConfig(**asdict(cfg))
 
 
 class DispatchResult(NamedTuple):
@@ -187,15 +194,20 @@ def dispatch_route(cfg: Config, expert_ids, x_active_mask=None, bs_per_rank=None
     _lib.check(rc, "cq_dispatch_route")
 
 
-def dispatch_permute(cfg: Config, x, expert_ids, smooth_scales=None, expert_scales=None, *,
-                     workspace, out: DispatchResult) -> None:
-    """Second half of dispatch (placement and quantisation)."""
-    dev = _check_inputs(cfg, x, expert_ids, smooth_scales, None, None, expert_scales)
+def dispatch_permute(cfg: Config, x, expert_ids, smooth_scales=None, expert_scales=None,
+                     x_active_mask=None, bs_per_rank=None, *, workspace,
+                     out: DispatchResult) -> None:
+    """Second half of dispatch (placement and quantisation). The mask and
+    per-rank BS, as given to dispatch_route, only let the kernel skip
+    prefetching rows of inactive tokens."""
+    dev = _check_inputs(cfg, x, expert_ids, smooth_scales, x_active_mask, bs_per_rank,
+                        expert_scales)
     c = cfg.as_c()
     rc = _lib.load().cq_dispatch_permute(
-        ctypes.byref(c), _ptr(x), _ptr(expert_ids), _ptr(smooth_scales), _ptr(expert_scales),
-        _ptr(out.expand_x), _ptr(out.dynamic_scales), _ptr(out.assist_info),
-        _ptr(out.expand_scales), _ptr(workspace), workspace.numel(), _stream(dev))
+        ctypes.byref(c), _ptr(x), _ptr(expert_ids), _ptr(smooth_scales), _ptr(x_active_mask),
+        _ptr(bs_per_rank), _ptr(expert_scales), _ptr(out.expand_x), _ptr(out.dynamic_scales),
+        _ptr(out.assist_info), _ptr(out.expand_scales), _ptr(workspace), workspace.numel(),
+        _stream(dev))
     _lib.check(rc, "cq_dispatch_permute")
 
 

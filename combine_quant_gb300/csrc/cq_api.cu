@@ -100,9 +100,10 @@ int route_impl(const cq_config* cfg, const int32_t* expert_ids, const uint8_t* m
 }
 
 int permute_impl(const cq_config* cfg, const void* x, const int32_t* expert_ids,
-                 const float* smooth, const float* expert_scales, void* expand_x,
-                 void* dynamic_scales, int32_t* assist_info, float* expand_scales,
-                 void* workspace, size_t workspace_bytes, void* stream) {
+                 const float* smooth, const uint8_t* mask, const int32_t* bs_per_rank,
+                 const float* expert_scales, void* expand_x, void* dynamic_scales,
+                 int32_t* assist_info, float* expand_scales, void* workspace,
+                 size_t workspace_bytes, void* stream) {
   int rc = validate(cfg);
   if (rc != CQ_OK) return rc;
   const Dims d = dims_of(cfg);
@@ -117,6 +118,8 @@ int permute_impl(const cq_config* cfg, const void* x, const int32_t* expert_ids,
   a.d = d;
   a.x = static_cast<const uint16_t*>(x);
   a.expert_ids = expert_ids;
+  a.mask = d.mask_ndim ? mask : nullptr;
+  a.bs_per_rank = bs_per_rank;
   a.smooth = smooth;
   a.expert_scales = expert_scales;
   a.expand_x = expand_x;
@@ -183,12 +186,13 @@ int cq_dispatch_route(const cq_config* cfg, const int32_t* expert_ids,
 }
 
 int cq_dispatch_permute(const cq_config* cfg, const void* x, const int32_t* expert_ids,
-                        const float* smooth_scales, const float* expert_scales, void* expand_x,
+                        const float* smooth_scales, const uint8_t* x_active_mask,
+                        const int32_t* bs_per_rank, const float* expert_scales, void* expand_x,
                         void* dynamic_scales, int32_t* assist_info, float* expand_scales,
                         void* workspace, size_t workspace_bytes, void* stream) {
-  return permute_impl(cfg, x, expert_ids, smooth_scales, expert_scales, expand_x,
-                      dynamic_scales, assist_info, expand_scales, workspace, workspace_bytes,
-                      stream);
+  return permute_impl(cfg, x, expert_ids, smooth_scales, x_active_mask, bs_per_rank,
+                      expert_scales, expand_x, dynamic_scales, assist_info, expand_scales,
+                      workspace, workspace_bytes, stream);
 }
 
 int cq_dispatch(const cq_config* cfg, const void* x, const int32_t* expert_ids,
@@ -205,9 +209,9 @@ int cq_dispatch(const cq_config* cfg, const void* x, const int32_t* expert_ids,
   rc = route_impl(cfg, expert_ids, x_active_mask, bs_per_rank, assist_info, ep_recv_count,
                   expert_token_nums, workspace, workspace_bytes, stream);
   if (rc != CQ_OK) return rc;
-  return permute_impl(cfg, x, expert_ids, smooth_scales, expert_scales, expand_x,
-                      dynamic_scales, assist_info, expand_scales, workspace, workspace_bytes,
-                      stream);
+  return permute_impl(cfg, x, expert_ids, smooth_scales, x_active_mask, bs_per_rank,
+                      expert_scales, expand_x, dynamic_scales, assist_info, expand_scales,
+                      workspace, workspace_bytes, stream);
 }
 
 int cq_combine(const cq_config* cfg, const void* expand_x_ffn, const int32_t* assist_info,

@@ -101,6 +101,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(CombineArgs a, int nc
   const Dims& d = a.d;
   const int64_t tok = blockIdx.x / nchunk;
   const int chunk = blockIdx.x - (int)(tok * nchunk);
+  griddep_wait();  // the inverse map comes from the permute kernel
   if (threadIdx.x < d.NS) {
     const int k = threadIdx.x;
     int code = a.inv[tok * d.NS + k];
@@ -166,9 +167,9 @@ cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) {
   const int units = a.d.H >> 3;
   const int nchunk = (units + kThreads - 1) / kThreads;
   const int64_t grid = (int64_t)a.d.W * a.d.BS * nchunk;
-  if (a.out_f32) combine_kernel<true><<<(unsigned)grid, kThreads, 0, s>>>(a, nchunk);
-  else combine_kernel<false><<<(unsigned)grid, kThreads, 0, s>>>(a, nchunk);
-  return cudaGetLastError();
+  if (a.out_f32)
+    return launch_pdl(combine_kernel<true>, dim3((unsigned)grid), dim3(kThreads), 0, s, a, nchunk);
+  return launch_pdl(combine_kernel<false>, dim3((unsigned)grid), dim3(kThreads), 0, s, a, nchunk);
 }
 
 }  // namespace cq

@@ -18,17 +18,22 @@ struct Dims {
 };
 
 // Workspace layout (byte offsets, each segment 256-byte aligned).
-//   hdr      : uint32 status, uint32 done counter, int32 total rows, pad
-//   counts_t : int32 [G][W]  per (global expert slot, source rank) row counts
-//   blockoff : int32 [G][W]  first global row of each (slot, source) block
-//   eidx     : int32 [W*BS*NS] arrival ordinal of each slot, or a CQ_INV code
+//   hdr       : uint32 status, uint32 done counter, int32 total rows, pad
+//   counts_t  : int32 [G][W]  rows per (global expert slot, source rank)
+//   local_off : int32 [G][W]  first row of each (slot, source) block, counted
+//                             from the start of its destination rank
+//   eidx      : int32 [W*BS*NS] arrival ordinal of each slot, or a CQ_INV code
+//   rank_tot  : int32 [W]     rows received by each destination rank
+//   rank_base : int32 [W+1]   first global row of each destination rank
 struct Workspace {
   uint32_t* status;
   uint32_t* done;
   int32_t* total;
   int32_t* counts_t;
-  int32_t* blockoff;
+  int32_t* local_off;
   int32_t* eidx;
+  int32_t* rank_tot;
+  int32_t* rank_base;
 };
 
 constexpr size_t kHdrBytes = 256;
@@ -39,6 +44,8 @@ inline size_t workspace_bytes(const Dims& d) {
   b += align256(sizeof(int32_t) * (size_t)d.G * d.W);
   b += align256(sizeof(int32_t) * (size_t)d.G * d.W);
   b += align256(sizeof(int32_t) * (size_t)d.W * d.BS * d.NS);
+  b += align256(sizeof(int32_t) * (size_t)d.W);
+  b += align256(sizeof(int32_t) * (size_t)(d.W + 1));
   return b;
 }
 
@@ -51,9 +58,13 @@ inline Workspace carve(void* base, const Dims& d) {
   p += kHdrBytes;
   w.counts_t = reinterpret_cast<int32_t*>(p);
   p += align256(sizeof(int32_t) * (size_t)d.G * d.W);
-  w.blockoff = reinterpret_cast<int32_t*>(p);
+  w.local_off = reinterpret_cast<int32_t*>(p);
   p += align256(sizeof(int32_t) * (size_t)d.G * d.W);
   w.eidx = reinterpret_cast<int32_t*>(p);
+  p += align256(sizeof(int32_t) * (size_t)d.W * d.BS * d.NS);
+  w.rank_tot = reinterpret_cast<int32_t*>(p);
+  p += align256(sizeof(int32_t) * (size_t)d.W);
+  w.rank_base = reinterpret_cast<int32_t*>(p);
   return w;
 }
 
@@ -78,6 +89,8 @@ struct PermuteArgs {
   Dims d;
   const uint16_t* x;
   const int32_t* expert_ids;
+  const uint8_t* mask;          // only to skip prefetching rows of inactive tokens
+  const int32_t* bs_per_rank;   // idem
   const float* smooth;
   const float* expert_scales;
   void* expand_x;
@@ -100,6 +113,31 @@ struct CombineArgs {
   void* y;
   int32_t out_f32;
 };
+
+// Launch with programmatic stream serialisation: the kernel may start while
+// the previous kernel in the stream is still running. Every kernel launched
+// this way executes griddep_wait() before it reads anything an earlier kernel
+// wrote, which waits for that kernel to complete and its writes to be visible.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
+}
+
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 // Launchers (each returns the cudaError_t of its launch).
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);

@@ -158,6 +158,39 @@ __global__ void __launch_bounds__(256) permute_kernel(PermuteArgs a) {
   const int64_t tok = blockIdx.x;
   const int r = (int)(tok / d.BS), i = (int)(tok - (int64_t)r * d.BS);
   const int lane = threadIdx.x & 31;
+  const int H = d.H;
+  const int units = H >> 4;
+  const uint16_t* xrow = a.x + tok * H;
+
+  // Thread t owns the 16-element units t and t + blockDim of the token row.
+  Units U;
+  auto load_row = [&]() {
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int u = threadIdx.x + q * blockDim.x;
+      U.ok[q] = u < units;
+      if (U.ok[q]) {
+        U.v[q][0] = ld_nc_v4(xrow + 16 * u);
+        U.v[q][1] = ld_nc_v4(xrow + 16 * u + 8);
+      } else {
+        U.v[q][0] = U.v[q][1] = make_uint4(0, 0, 0, 0);
+      }
+    }
+  };
+  // From the inputs alone, could this token be active? If so, start loading
+  // its row now: this kernel may be running while the routing kernel ends.
+  bool prefetched = !a.bs_per_rank || i < a.bs_per_rank[r];
+  if (prefetched && a.mask) {
+    if (d.mask_ndim == 1) {
+      prefetched = a.mask[tok] != 0;
+    } else {
+      bool any = false;
+      for (int j = 0; j < d.K; ++j) any |= a.mask[tok * d.K + j] != 0;
+      prefetched = any;
+    }
+  }
+  if (prefetched) load_row();
+  griddep_wait();  // routing outputs (ordinals, block offsets) are read from here on
 
   if (threadIdx.x < 32) {
     const int k = lane;
@@ -166,17 +199,18 @@ __global__ void __launch_bounds__(256) permute_kernel(PermuteArgs a) {
       const int e = a.ws.eidx[tok * d.NS + k];
       int code = e;
       if (e >= 0) {
-        int g, id = 0;
+        int g, dst;  // global expert slot, destination rank
         if (k < d.K) {
-          id = a.expert_ids[tok * d.K + k];
+          const int id = a.expert_ids[tok * d.K + k];
           g = d.S_r + id;
+          dst = d.S_r + id / d.L;
           srow = d.S_eff + id;
         } else {
           const int s = k - d.K;
-          g = s * d.R_rep + r % d.R_rep;
+          g = dst = s * d.R_rep + r % d.R_rep;  // a shared-expert rank hosts one slot
           srow = s;
         }
-        row = a.ws.blockoff[(int64_t)g * d.W + r] + e;
+        row = a.ws.rank_base[dst] + a.ws.local_off[(int64_t)g * d.W + r] + e;
         if (row < 0 || (int64_t)row >= d.R_max) {  // consistency guard: never write outside
           atomicOr(a.ws.status, (uint32_t)CQ_ST_INTERNAL);
           row = -1;
@@ -202,23 +236,7 @@ __global__ void __launch_bounds__(256) permute_kernel(PermuteArgs a) {
   __syncthreads();
   const int nrows = s_nrows;
   if (nrows == 0) return;
-
-  // Load the token row: thread t owns 16-element units t and t + blockDim.
-  const int H = d.H;
-  const int units = H >> 4;
-  const uint16_t* xrow = a.x + tok * H;
-  Units U;
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const int u = threadIdx.x + q * blockDim.x;
-    U.ok[q] = u < units;
-    if (U.ok[q]) {
-      U.v[q][0] = ld_nc_v4(xrow + 16 * u);
-      U.v[q][1] = ld_nc_v4(xrow + 16 * u + 8);
-    } else {
-      U.v[q][0] = U.v[q][1] = make_uint4(0, 0, 0, 0);
-    }
-  }
+  if (!prefetched) load_row();  // routing found rows the inputs did not predict
 
   if (MODE == 0) {
     for (int n = 0; n < nrows; ++n) {
@@ -305,6 +323,8 @@ __global__ void __launch_bounds__(256) permute_kernel(PermuteArgs a) {
       if (threadIdx.x == 0 && d.SC > nblk) sc[nblk] = 0;  // Align2 padding column
     }
   }
+  // This CTA's stores are issued: the combine kernel may start launching.
+  griddep_launch_dependents();
 }
 
 template <int MODE, bool SMOOTH>
@@ -313,8 +333,7 @@ cudaError_t launch_mode(const PermuteArgs& a, cudaStream_t s) {
   int threads = ((units + 1) / 2 + 31) / 32 * 32;
   if (threads < 32) threads = 32;
   const int64_t grid = (int64_t)a.d.W * a.d.BS;
-  permute_kernel<MODE, SMOOTH><<<(unsigned)grid, threads, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(permute_kernel<MODE, SMOOTH>, dim3((unsigned)grid), dim3(threads), 0, s, a);
 }
 
 }  // namespace

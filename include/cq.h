@@ -148,13 +148,17 @@ int cq_dispatch(const cq_config* cfg, const void* x, const int32_t* expert_ids,
  * route: scan, counts, prefix sums (writes ep_recv_count, expert_token_nums,
  *        the rank_row_base part of assist_info, and the workspace);
  * permute: row placement and quantisation (writes expand_x, dynamic_scales,
- *        the rows and inv parts of assist_info, expand_scales). */
+ *        the rows and inv parts of assist_info, expand_scales). It may start
+ *        while the route kernel still runs and prefetch token rows; the mask
+ *        and bs_per_rank (nullable, as given to route) only stop it from
+ *        prefetching rows of inactive tokens. */
 int cq_dispatch_route(const cq_config* cfg, const int32_t* expert_ids,
                       const uint8_t* x_active_mask, const int32_t* bs_per_rank,
                       int32_t* assist_info, int32_t* ep_recv_count, int64_t* expert_token_nums,
                       void* workspace, size_t workspace_bytes, void* stream);
 int cq_dispatch_permute(const cq_config* cfg, const void* x, const int32_t* expert_ids,
-                        const float* smooth_scales, const float* expert_scales,
+                        const float* smooth_scales, const uint8_t* x_active_mask,
+                        const int32_t* bs_per_rank, const float* expert_scales,
                         void* expand_x, void* dynamic_scales, int32_t* assist_info,
                         float* expand_scales, void* workspace, size_t workspace_bytes,
                         void* stream);
