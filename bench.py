@@ -42,7 +42,14 @@ L2_FLUSH_BYTES = 256 << 20
 # DRAM bytes per launch read from an ncu capture of the named kernel, keyed by
 # the SHA-256 of the kernel's source file when it was captured; reported only
 # while the source is unchanged.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # profiles/dsv3_kernels_ncu_full.md: read 470.065408 MB + write 50.161408 MB
+    "combine": {"bytes_per_launch": 520226816,
+                "src_sha": "6ec55b69f2c4b6bc4e4f93ae7ab286b905c8ca541fc5cd584011ccc04221c83f"},
+    # read 59.2512 MB + write 175.902976 MB
+    "permute": {"bytes_per_launch": 235154176,
+                "src_sha": "4f67ff779144f681463b901fb709516e62474b245cc0c351d6eda7b58c130758"},
+}
 
 
 def parse_args(argv=None):
@@ -216,6 +223,19 @@ def oracle_sample(wl, budget_s: float, max_tokens: int | None = None):
 
 
 # ------------------------------------------------------------- distributed ----
+
+def job_throughput(local_ms: float, units_per_rank: int, steps: int, dist=None, device=None):
+    """Whole-job throughput: the units every rank processed over the slowest
+    rank's time (a max over ranks). Returns (units/s, slowest ms)."""
+    slowest, world = float(local_ms), 1
+    if dist is not None and dist.is_initialized():
+        import torch
+
+        t = torch.tensor([slowest], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        slowest, world = float(t.item()), dist.get_world_size()
+    return world * units_per_rank * steps / (slowest / 1e3), slowest
+
 
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -409,13 +429,8 @@ def run_cq(args):
     t_wall = time.perf_counter() - t_wall
     clk = clocks.stop()
     t_step = [e[0].elapsed_time(e[1]) for e in ev]
-    total_ms = sum(t_step)
-    if dist is not None:
-        tt = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    value, total_ms = job_throughput(sum(t_step), tokens, args.steps, dist, dev)
     ms_per_step = total_ms / args.steps
-    value = world * tokens * args.steps / (total_ms / 1e3)
 
     # End to end through cq_dispatch / cq_combine with host buffers: each step
     # copies x, expert_ids and expert_scales from pinned memory and reads y back.
@@ -424,37 +439,57 @@ def run_cq(args):
         hx = torch.from_numpy(np.ascontiguousarray(wl.x)).view(torch.bfloat16).pin_memory()
         hids = torch.from_numpy(np.ascontiguousarray(wl.expert_ids)).pin_memory()
         hw = torch.from_numpy(np.ascontiguousarray(wl.expert_scales)).pin_memory()
-        hy = torch.empty(y.shape, dtype=torch.bfloat16).pin_memory()
-        dx, dids, dw = torch.empty_like(x), torch.empty_like(ids), torch.empty_like(w)
         n_e2e = max(10, min(args.steps, 500))
+        # Two buffer sets: step k uploads into set k % 2 on the upload stream,
+        # computes on the main stream, downloads y on the download stream; the
+        # events keep each set's reuse ordered, so copies of neighbouring
+        # steps overlap the compute of this one.
+        s_up, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        sets = [dict(x=torch.empty_like(x), ids=torch.empty_like(ids), w=torch.empty_like(w),
+                     y=torch.empty_like(y),
+                     hy=torch.empty(y.shape, dtype=torch.bfloat16).pin_memory(),
+                     up=torch.cuda.Event(), done=torch.cuda.Event(), down=torch.cuda.Event())
+                for _ in range(2)]
+        for b in sets:
+            b["done"].record(stream)
+            b["down"].record(stream)
 
-        def e2e_step():
-            dx.copy_(hx, non_blocking=True)
-            dids.copy_(hids, non_blocking=True)
-            dw.copy_(hw, non_blocking=True)
-            o = cq.dispatch(cfg, dx, dids, smooth_scales=sm, x_active_mask=mask, bs_per_rank=bpr,
-                            expert_scales=dw, workspace=ws, out=out)
-            cq.combine(cfg, ffn, o.assist_info, dw, o.ep_recv_count, ori_x=dx, y=y)
-            hy.copy_(y, non_blocking=True)
+        def e2e_step(k):
+            b = sets[k % 2]
+            with torch.cuda.stream(s_up):
+                s_up.wait_event(b["done"])  # the set's inputs are free once its last compute ended
+                b["x"].copy_(hx, non_blocking=True)
+                b["ids"].copy_(hids, non_blocking=True)
+                b["w"].copy_(hw, non_blocking=True)
+                b["up"].record(s_up)
+            stream.wait_event(b["up"])
+            stream.wait_event(b["down"])  # y of this set has been read back
+            o = cq.dispatch(cfg, b["x"], b["ids"], smooth_scales=sm, x_active_mask=mask,
+                            bs_per_rank=bpr, expert_scales=b["w"], workspace=ws, out=out)
+            cq.combine(cfg, ffn, o.assist_info, b["w"], o.ep_recv_count, ori_x=b["x"], y=b["y"])
+            b["done"].record(stream)
+            with torch.cuda.stream(s_down):
+                s_down.wait_event(b["done"])
+                b["hy"].copy_(b["y"], non_blocking=True)
+                b["down"].record(s_down)
 
-        for _ in range(3):
-            e2e_step()
+        for k in range(3):
+            e2e_step(k)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier()
-        e0.record(stream)
-        for _ in range(n_e2e):
-            e2e_step()
-        e1.record(stream)
+        e0.record(s_up)
+        for k in range(n_e2e):
+            e2e_step(k)
+        s_down.wait_event(sets[(n_e2e - 1) % 2]["down"])
+        e1.record(s_down)
         barrier()
-        e_ms = e0.elapsed_time(e1)
-        if dist is not None:
-            tt = torch.tensor([e_ms], device=dev, dtype=torch.float64)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e_ms = float(tt.item())
-        e2e = {"value": world * tokens * n_e2e / (e_ms / 1e3), "unit": UNIT,
+        e_value, _ = job_throughput(e0.elapsed_time(e1), tokens, n_e2e, dist, dev)
+        e2e = {"value": e_value, "unit": UNIT,
                "h2d_bytes_per_step": hx.nbytes + hids.nbytes + hw.nbytes,
-               "d2h_bytes_per_step": hy.nbytes, "steps": n_e2e,
-               "api": "cq_dispatch + cq_combine (libcq C ABI via ctypes)"}
+               "d2h_bytes_per_step": sets[0]["hy"].nbytes, "steps": n_e2e,
+               "api": "cq_dispatch + cq_combine (libcq C ABI via ctypes)",
+               "pipelining": "two buffer sets; upload, compute and download on three "
+                             "streams, so neighbouring steps' copies overlap"}
 
     if rank != 0:
         if dist is not None:
