@@ -62,6 +62,11 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--quant-mode", type=int, default=None,
+                    help="override the workload's quant_mode (0, 2, 5)")
+    ap.add_argument("--combine", choices=["bf16", "int8"], default="bf16",
+                    help="combine from bf16 expert outputs, or from int8 ones quantised on the "
+                         "expert side (the quantiser is timed separately, outside the step)")
     ap.add_argument("--flush", choices=["write+read", "write"], default="write+read",
                     help="L2 flush between steps (outside the timed events)")
     ap.add_argument("--no-graph", action="store_true",
@@ -134,7 +139,8 @@ class ClockSampler:
 
 # -------------------------------------------------------- byte accounting ----
 
-def algorithmic_bytes(cfg, rows: int, tokens_active: int, with_scales: bool) -> dict:
+def algorithmic_bytes(cfg, rows: int, tokens_active: int, with_scales: bool,
+                      combine_int8: bool = False) -> dict:
     """Bytes each kernel must move per launch (reads + writes of HBM), given
     the routed row count P and the active token count."""
     W, BS, K, H = cfg.ep_world_size, cfg.max_bs, cfg.topk, cfg.hidden
@@ -149,8 +155,12 @@ def algorithmic_bytes(cfg, rows: int, tokens_active: int, with_scales: bool) -> 
                + rows * (H * b_code + b_scale + 16)  # codes, scale, (src, token, slot) record
                + 4 * T * NS * 2 + 4 * T * K     # eidx read, inv write, ids read
                + (8 * rows if with_scales else 0))  # routing weight read + carried copy
-    combine = 2 * H * rows + 2 * H * T + 4 * T * NS + 4 * T * K
-    return {"route": route, "permute": permute, "combine": combine}
+    ffn_row = (H + 4 * (H // 8)) if combine_int8 else 2 * H  # int8 codes + block scales
+    combine = ffn_row * rows + 2 * H * T + 4 * T * NS + 4 * T * K
+    out = {"route": route, "permute": permute, "combine": combine}
+    if combine_int8:
+        out["combine_quant"] = rows * (2 * H + H + 4 * (H // 8))  # bf16 in, codes + scales out
+    return out
 
 
 def measured_peaks() -> tuple[float, str]:
@@ -307,6 +317,8 @@ def run_cq(args):
         torch.cuda.synchronize()
 
     wl = workloads.WORKLOADS[args.workload]()
+    if args.quant_mode is not None:
+        wl = wl.with_mode(args.quant_mode)
     cfg = cq.Config.from_dict(wl.cfg)
     tdev = lambda a, dt: None if a is None else torch.from_numpy(  # noqa: E731
         np.ascontiguousarray(a)).to(dev).view(dt)
@@ -322,6 +334,23 @@ def run_cq(args):
     ridx = (torch.arange(cfg.max_rows, device=dev, dtype=torch.int64) * 7919) % 4096
     ffn = pool.index_select(0, ridx).contiguous()
     y = torch.empty(cfg.ep_world_size, cfg.max_bs, cfg.hidden, dtype=torch.bfloat16, device=dev)
+    ffn_q = ffn_s = None
+    if args.combine == "int8":
+        # The expert side's int8 outputs, made once before timing (a producer
+        # would emit them from its own epilogue); the quantiser is timed apart.
+        cq.dispatch(cfg, x, ids, smooth_scales=sm, x_active_mask=mask, bs_per_rank=bpr,
+                    expert_scales=w, workspace=ws, out=out)
+        ffn_q, ffn_s = cq.combine_quant(cfg, ffn, out.assist_info)
+
+    consts = dict(const_alpha1=tdev(wl.const_alpha1, torch.float32),
+                  const_alpha2=tdev(wl.const_alpha2, torch.float32),
+                  const_v=tdev(wl.const_v, torch.bfloat16))
+
+    def combine_call(assist_info, erc, w_, x_, y_):
+        if args.combine == "int8":
+            return cq.combine_q8(cfg, ffn_q, ffn_s, assist_info, w_, erc, ori_x=x_, y=y_,
+                                 **consts)
+        return cq.combine(cfg, ffn, assist_info, w_, erc, ori_x=x_, y=y_, **consts)
     flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -351,7 +380,7 @@ def run_cq(args):
         cq.dispatch_permute(cfg, x, ids, sm, w, mask, bpr, workspace=ws, out=out)
         if evs and len(evs) == 4:
             evs[2].record(stream)
-        cq.combine(cfg, ffn, out.assist_info, w, out.ep_recv_count, ori_x=x, y=y)
+        combine_call(out.assist_info, out.ep_recv_count, w, x, y)
         if evs:
             evs[-1].record(stream)
 
@@ -381,8 +410,8 @@ def run_cq(args):
                                                         out=out)),
                     ("permute", lambda: cq.dispatch_permute(cfg, x, ids, sm, w, mask, bpr,
                                                             workspace=ws, out=out)),
-                    ("combine", lambda: cq.combine(cfg, ffn, out.assist_info, w,
-                                                   out.ep_recv_count, ori_x=x, y=y))):
+                    ("combine", lambda: combine_call(out.assist_info, out.ep_recv_count, w, x,
+                                                     y))):
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g, stream=side):
                     fn()
@@ -396,8 +425,7 @@ def run_cq(args):
         parts = [lambda: cq.dispatch_route(cfg, ids, mask, bpr, workspace=ws, out=out),
                  lambda: cq.dispatch_permute(cfg, x, ids, sm, w, mask, bpr, workspace=ws,
                                              out=out),
-                 lambda: cq.combine(cfg, ffn, out.assist_info, w, out.ep_recv_count, ori_x=x,
-                                    y=y)]
+                 lambda: combine_call(out.assist_info, out.ep_recv_count, w, x, y)]
 
     # Per-kernel breakdown: events between the kernels.
     n_bd = max(3, min(args.steps, 500))
@@ -466,7 +494,7 @@ def run_cq(args):
             stream.wait_event(b["down"])  # y of this set has been read back
             o = cq.dispatch(cfg, b["x"], b["ids"], smooth_scales=sm, x_active_mask=mask,
                             bs_per_rank=bpr, expert_scales=b["w"], workspace=ws, out=out)
-            cq.combine(cfg, ffn, o.assist_info, b["w"], o.ep_recv_count, ori_x=b["x"], y=b["y"])
+            combine_call(o.assist_info, o.ep_recv_count, b["w"], b["x"], b["y"])
             b["done"].record(stream)
             with torch.cuda.stream(s_down):
                 s_down.wait_event(b["done"])
@@ -496,16 +524,33 @@ def run_cq(args):
             dist.destroy_process_group()
         return 0
 
-    ab = algorithmic_bytes(cfg, rows, tokens, with_scales=True)
+    ab = algorithmic_bytes(cfg, rows, tokens, with_scales=True,
+                           combine_int8=args.combine == "int8")
     means = {"route": statistics.mean(t_route), "permute": statistics.mean(t_perm),
              "combine": statistics.mean(t_comb)}
+    if args.combine == "int8":
+        # the expert-side quantiser, timed alone (not part of the step)
+        eq0, eq1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_q = max(3, min(args.steps, 200))
+        t_q = []
+        for _ in range(n_q):
+            flush.zero_()
+            eq0.record(stream)
+            cq.combine_quant(cfg, ffn, out.assist_info, ffn_q, ffn_s)
+            eq1.record(stream)
+            torch.cuda.synchronize()
+            t_q.append(eq0.elapsed_time(eq1))
+        means["combine_quant"] = statistics.mean(t_q)
     peak, peak_kind = measured_peaks()
     kernels = {k: {"us": 1e3 * means[k], "alg_bytes": ab[k],
                    "gbs": ab[k] / (means[k] * 1e-3) / 1e9,
                    "frac": ab[k] / (means[k] * 1e-3) / 1e9 / peak} for k in means}
     dom = max(("permute", "combine"), key=lambda k: means[k])
+    traffic = None
+    if args.workload == "dsv3" and args.quant_mode in (None, 2) and args.combine == "bf16":
+        traffic = ncu_traffic(dom)  # the captured configuration
     roof = {"kernel": dom, "bound": "hbm", "achieved": kernels[dom]["gbs"], "peak": peak,
-            "unit": "GB/s", "frac": kernels[dom]["frac"], "traffic": ncu_traffic(dom),
+            "unit": "GB/s", "frac": kernels[dom]["frac"], "traffic": traffic,
             "peak_source": f"hbm_gbs of {peak_kind}"}
 
     cpu = None
@@ -517,8 +562,13 @@ def run_cq(args):
           "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
           "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
           "config": {"workload": workload_desc(wl), "tokens_per_step": tokens,
-                     "rows_per_step": rows, "io": "bf16 tokens in, int8 codes + f32 scales "
-                     "on the wire, bf16 out",
+                     "rows_per_step": rows,
+                     "io": "bf16 tokens in; dispatch rows " + {
+                         0: "bf16", 2: "int8 + f32 per-row scale",
+                         5: "e4m3 + e8m0 per-32 scales"}[cfg.quant_mode]
+                     + "; combine from " + ("int8 expert outputs + f32 per-8 scales"
+                                            if args.combine == "int8" else "bf16 expert outputs")
+                     + "; bf16 out",
                      "l2": "flushed between steps: 256 MiB write" + (
                          " then 256 MiB read (no dirty lines left)"
                          if args.flush == "write+read" else ""),

@@ -7,6 +7,6 @@ C ABI declared in include/cq.h). This package is its thin Python binding:
 synthetic inputs; ``build`` compiles the library in-tree.
 """
 from .api import (Config, DispatchResult, alloc_dispatch_outputs, alloc_workspace,  # noqa: F401
-                  assist_views, combine, dispatch, dispatch_permute, dispatch_route,
-                  read_status)
+                  assist_views, combine, combine_q8, combine_quant, dispatch, dispatch_permute,
+                  dispatch_route, read_status)
 from ._lib import CqError  # noqa: F401

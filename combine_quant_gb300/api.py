@@ -244,6 +244,61 @@ def combine(cfg: Config, expand_x_ffn: torch.Tensor, assist_info: torch.Tensor,
     return y
 
 
+def combine_quant(cfg: Config, expand_x_ffn: torch.Tensor, assist_info: torch.Tensor,
+                  codes: Optional[torch.Tensor] = None, scales: Optional[torch.Tensor] = None):
+    """Expert-side int8 block quantisation of the FFN outputs (cq_combine_quant).
+    Returns (codes int8 [R_max, H], scales f32 [R_max, H/8])."""
+    R, H = cfg.max_rows, cfg.hidden
+    dev = assist_info.device
+    _need(expand_x_ffn, "expand_x_ffn", torch.bfloat16, (R, H), dev)
+    _need(assist_info, "assist_info", torch.int32, (cfg.assist_info_size,), dev)
+    if codes is None:
+        codes = torch.empty(R, H, dtype=torch.int8, device=dev)
+    if scales is None:
+        scales = torch.empty(R, H // 8, dtype=torch.float32, device=dev)
+    _need(codes, "codes", torch.int8, (R, H), dev)
+    _need(scales, "scales", torch.float32, (R, H // 8), dev)
+    c = cfg.as_c()
+    rc = _lib.load().cq_combine_quant(ctypes.byref(c), _ptr(expand_x_ffn), _ptr(assist_info),
+                                      _ptr(codes), _ptr(scales), _stream(dev))
+    _lib.check(rc, "cq_combine_quant")
+    return codes, scales
+
+
+def combine_q8(cfg: Config, codes: torch.Tensor, scales: torch.Tensor, assist_info: torch.Tensor,
+               expert_scales: torch.Tensor, ep_recv_count: Optional[torch.Tensor] = None,
+               ori_x: Optional[torch.Tensor] = None,
+               const_alpha1: Optional[torch.Tensor] = None,
+               const_alpha2: Optional[torch.Tensor] = None,
+               const_v: Optional[torch.Tensor] = None,
+               out_dtype: torch.dtype = torch.bfloat16,
+               y: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """MoE combine from int8 expert outputs (cq_combine_q8)."""
+    W, BS, K, H = cfg.ep_world_size, cfg.max_bs, cfg.topk, cfg.hidden
+    dev = assist_info.device
+    _need(codes, "codes", torch.int8, (cfg.max_rows, H), dev)
+    _need(scales, "scales", torch.float32, (cfg.max_rows, H // 8), dev)
+    _need(assist_info, "assist_info", torch.int32, (cfg.assist_info_size,), dev)
+    _need(expert_scales, "expert_scales", torch.float32, (W, BS, K), dev)
+    _need(ori_x, "ori_x", torch.bfloat16, (W, BS, H), dev)
+    Q = cfg.const_expert_num
+    _need(const_alpha1, "const_alpha1", torch.float32, (Q,), dev)
+    _need(const_alpha2, "const_alpha2", torch.float32, (Q,), dev)
+    _need(const_v, "const_v", torch.bfloat16, (Q, H), dev)
+    if out_dtype not in (torch.bfloat16, torch.float32):
+        raise ValueError("out_dtype must be bfloat16 or float32")
+    if y is None:
+        y = torch.empty(W, BS, H, dtype=out_dtype, device=dev)
+    _need(y, "y", out_dtype, (W, BS, H), dev)
+    c = cfg.as_c()
+    rc = _lib.load().cq_combine_q8(
+        ctypes.byref(c), _ptr(codes), _ptr(scales), _ptr(assist_info), _ptr(ep_recv_count),
+        _ptr(expert_scales), _ptr(ori_x), _ptr(const_alpha1), _ptr(const_alpha2), _ptr(const_v),
+        0 if out_dtype == torch.bfloat16 else 1, _ptr(y), _stream(dev))
+    _lib.check(rc, "cq_combine_q8")
+    return y
+
+
 def read_status(workspace: torch.Tensor) -> int:
     """Synchronise the current stream, return and clear the sticky status bits."""
     st = ctypes.c_uint32(0)

@@ -127,6 +127,7 @@ int permute_impl(const cq_config* cfg, const void* x, const int32_t* expert_ids,
   a.assist_rows = assist_info + cq::assist_rows_off(d);
   a.inv = assist_info + cq::assist_inv_off(d);
   a.expand_scales = expand_scales;
+  a.scale_rows_bulk = d.SC % 16 == 0 && aligned(dynamic_scales, 16);
   a.ws = cq::carve(workspace, d);
   return cq::launch_permute(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? CQ_OK
                                                                                    : CQ_ERR_CUDA;
@@ -214,35 +215,91 @@ int cq_dispatch(const cq_config* cfg, const void* x, const int32_t* expert_ids,
                       workspace, workspace_bytes, stream);
 }
 
+}  // extern "C"
+
+namespace {
+
+// Checks and argument block shared by the two combine entry points.
+int combine_args(const cq_config* cfg, const int32_t* assist_info, const float* expert_scales,
+                 const void* ori_x, const float* const_alpha1, const float* const_alpha2,
+                 const void* const_v, int32_t out_dtype, void* y, cq::CombineArgs* a) {
+  int rc = validate(cfg);
+  if (rc != CQ_OK) return rc;
+  const Dims d = dims_of(cfg);
+  if (!assist_info || !expert_scales || !y) return CQ_ERR_ARG;
+  if ((d.C + d.Q) > 0 && !ori_x) return CQ_ERR_ARG;
+  if (d.Q > 0 && (!const_alpha1 || !const_alpha2 || !const_v)) return CQ_ERR_ARG;
+  if (out_dtype != 0 && out_dtype != 1) return CQ_ERR_ARG;
+  if (!aligned(y, 16) || (ori_x && !aligned(ori_x, 16)) || (const_v && !aligned(const_v, 16)))
+    return CQ_ERR_ARG;
+  *a = cq::CombineArgs{};
+  a->d = d;
+  a->inv = assist_info + cq::assist_inv_off(d);
+  a->expert_scales = expert_scales;
+  a->ori_x = static_cast<const uint16_t*>(ori_x);
+  a->alpha1 = const_alpha1;
+  a->alpha2 = const_alpha2;
+  a->const_v = static_cast<const uint16_t*>(const_v);
+  a->y = y;
+  a->out_f32 = out_dtype;
+  return CQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 int cq_combine(const cq_config* cfg, const void* expand_x_ffn, const int32_t* assist_info,
                const int32_t* ep_recv_count, const float* expert_scales, const void* ori_x,
                const float* const_alpha1, const float* const_alpha2, const void* const_v,
                int32_t out_dtype, void* y, void* stream) {
   (void)ep_recv_count;  // the inverse map inside assist_info locates every row
+  cq::CombineArgs a;
+  int rc = combine_args(cfg, assist_info, expert_scales, ori_x, const_alpha1, const_alpha2,
+                        const_v, out_dtype, y, &a);
+  if (rc != CQ_OK) return rc;
+  if (!expand_x_ffn || !aligned(expand_x_ffn, 16)) return CQ_ERR_ARG;
+  a.ffn = static_cast<const uint16_t*>(expand_x_ffn);
+  return cq::launch_combine(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? CQ_OK
+                                                                                   : CQ_ERR_CUDA;
+}
+
+int cq_combine_quant(const cq_config* cfg, const void* expand_x_ffn, const int32_t* assist_info,
+                     int8_t* ffn_codes, float* ffn_scales, void* stream) {
   int rc = validate(cfg);
   if (rc != CQ_OK) return rc;
   const Dims d = dims_of(cfg);
-  if (!assist_info || !expert_scales || !y) return CQ_ERR_ARG;
-  if (!expand_x_ffn && d.R_max > 0) return CQ_ERR_ARG;
-  if ((d.C + d.Q) > 0 && !ori_x) return CQ_ERR_ARG;
-  if (d.Q > 0 && (!const_alpha1 || !const_alpha2 || !const_v)) return CQ_ERR_ARG;
-  if (out_dtype != 0 && out_dtype != 1) return CQ_ERR_ARG;
-  if (!aligned(expand_x_ffn, 16) || !aligned(y, 16) || (ori_x && !aligned(ori_x, 16)) ||
-      (const_v && !aligned(const_v, 16)))
+  if (!expand_x_ffn || !assist_info || !ffn_codes || !ffn_scales) return CQ_ERR_ARG;
+  if (!aligned(expand_x_ffn, 16) || !aligned(ffn_codes, 16) || !aligned(ffn_scales, 4))
     return CQ_ERR_ARG;
-  cq::CombineArgs a;
+  cq::CombineArgs a{};
   a.d = d;
   a.ffn = static_cast<const uint16_t*>(expand_x_ffn);
-  a.inv = assist_info + cq::assist_inv_off(d);
-  a.expert_scales = expert_scales;
-  a.ori_x = static_cast<const uint16_t*>(ori_x);
-  a.alpha1 = const_alpha1;
-  a.alpha2 = const_alpha2;
-  a.const_v = static_cast<const uint16_t*>(const_v);
-  a.y = y;
-  a.out_f32 = out_dtype;
-  return cq::launch_combine(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? CQ_OK
-                                                                                   : CQ_ERR_CUDA;
+  a.ffn_q = ffn_codes;
+  a.ffn_scales = ffn_scales;
+  a.total_rows = assist_info + cq::assist_base_off(d) + d.W;
+  return cq::launch_combine_quant(a, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? CQ_OK
+             : CQ_ERR_CUDA;
+}
+
+int cq_combine_q8(const cq_config* cfg, const int8_t* ffn_codes, const float* ffn_scales,
+                  const int32_t* assist_info, const int32_t* ep_recv_count,
+                  const float* expert_scales, const void* ori_x, const float* const_alpha1,
+                  const float* const_alpha2, const void* const_v, int32_t out_dtype, void* y,
+                  void* stream) {
+  (void)ep_recv_count;
+  cq::CombineArgs a;
+  int rc = combine_args(cfg, assist_info, expert_scales, ori_x, const_alpha1, const_alpha2,
+                        const_v, out_dtype, y, &a);
+  if (rc != CQ_OK) return rc;
+  if (!ffn_codes || !ffn_scales || !aligned(ffn_codes, 16) || !aligned(ffn_scales, 4))
+    return CQ_ERR_ARG;
+  a.ffn_q = const_cast<int8_t*>(ffn_codes);
+  a.ffn_scales = const_cast<float*>(ffn_scales);
+  return cq::launch_combine_q8(a, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? CQ_OK
+             : CQ_ERR_CUDA;
 }
 
 int moe_dispatch(const cq_config* cfg, const void* x, const int32_t* expert_ids,

@@ -48,15 +48,6 @@ __device__ __forceinline__ void fma8(float (&acc)[8], float w, const uint4& v) {
   }
 }
 
-__device__ __forceinline__ void add8(float (&acc)[8], const uint4& v) {
-  const uint32_t* p = reinterpret_cast<const uint32_t*>(&v);
-#pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    acc[2 * t] = __fadd_rn(acc[2 * t], bf_lo(p[t]));
-    acc[2 * t + 1] = __fadd_rn(acc[2 * t + 1], bf_hi(p[t]));
-  }
-}
-
 // const expert: acc += w * (a1 * x + a2 * v), each product and the sum rounded.
 __device__ __forceinline__ void fma8_const(float (&acc)[8], float w, float a1, float a2,
                                            const uint4& x, const uint4& v) {
@@ -90,11 +81,75 @@ __device__ __forceinline__ void store8(void* y, int64_t elem, const float (&acc)
   }
 }
 
+__device__ __forceinline__ uint2 ld_nc_v2(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ float ld_nc_f32(const float* p) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void fma8f(float (&acc)[8], float w, const float (&v)[8]) {
+#pragma unroll
+  for (int t = 0; t < 8; ++t) acc[t] = __fmaf_rn(w, v[t], acc[t]);
+}
+
+__device__ __forceinline__ void add8f(float (&acc)[8], const float (&v)[8]) {
+#pragma unroll
+  for (int t = 0; t < 8; ++t) acc[t] = __fadd_rn(acc[t], v[t]);
+}
+
+// Expert-output rows as bf16: 8 values per 16-byte load.
+struct SrcBf16 {
+  const uint16_t* ffn;
+  struct Item {
+    uint4 v;
+  };
+  __device__ Item load(int64_t row, int H, int u) const {
+    return {ld_nc_v4(ffn + row * H + 8 * (int64_t)u)};
+  }
+  __device__ void floats(const Item& it, float (&f)[8]) const {
+    const uint32_t* p = reinterpret_cast<const uint32_t*>(&it.v);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      f[2 * t] = bf_lo(p[t]);
+      f[2 * t + 1] = bf_hi(p[t]);
+    }
+  }
+};
+
+// Expert-output rows as int8 with one scale per 8 values ("CANN MoE
+// Dispatch/Combine 通信算子性能优化实践", Int8DequantProcess): each value is
+// dequantised (code times block scale, one rounding) before it is summed.
+struct SrcQ8 {
+  const int8_t* codes;
+  const float* scales;
+  struct Item {
+    uint2 q;
+    float s;
+  };
+  __device__ Item load(int64_t row, int H, int u) const {
+    return {ld_nc_v2(codes + row * H + 8 * (int64_t)u), ld_nc_f32(scales + row * (H >> 3) + u)};
+  }
+  __device__ void floats(const Item& it, float (&f)[8]) const {
+#pragma unroll
+    for (int t = 0; t < 8; ++t) {
+      const uint32_t word = t < 4 ? it.q.x : it.q.y;
+      const int c = (int)(int8_t)(word >> (8 * (t & 3)));
+      f[t] = __fmul_rn((float)c, it.s);
+    }
+  }
+};
+
 // One CTA per (token, chunk of kThreads 8-element units); one unit per thread.
 constexpr int kThreads = 128;
 
-template <bool OUT_F32>
-__global__ void __launch_bounds__(kThreads) combine_kernel(CombineArgs a, int nchunk) {
+template <bool OUT_F32, class Src>
+__global__ void __launch_bounds__(kThreads) combine_kernel(CombineArgs a, Src src, int nchunk) {
   __shared__ int s_code[kMaxSlots];
   __shared__ float s_w[kMaxSlots];
 
@@ -128,15 +183,13 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(CombineArgs a, int nc
   const uint16_t* xrow = a.ori_x ? a.ori_x + tok * H : nullptr;
 
   for (int k0 = 0; k0 < d.K; k0 += kBatch) {
-    uint4 v[kBatch];
+    // Issue the loads of a batch of routed rows before the first multiply.
+    typename Src::Item v[kBatch];
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
       const int k = k0 + b;
       const int code = k < d.K ? s_code[k] : CQ_INV_NONE;
-      const uint16_t* src = nullptr;
-      if (code >= 0) src = a.ffn + (int64_t)code * H;
-      else if (code == CQ_INV_COPY) src = xrow;
-      v[b] = src ? ld_nc_v4(src + col) : make_uint4(0, 0, 0, 0);
+      if (code >= 0) v[b] = src.load(code, H, u);
     }
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
@@ -144,8 +197,12 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(CombineArgs a, int nc
       if (k >= d.K) break;
       const int code = s_code[k];
       const float w = s_w[k];
-      if (code >= 0 || code == CQ_INV_COPY) {
-        fma8(acc, w, v[b]);
+      if (code >= 0) {
+        float f[8];
+        src.floats(v[b], f);
+        fma8f(acc, w, f);
+      } else if (code == CQ_INV_COPY) {
+        fma8(acc, w, ld_nc_v4(xrow + col));  // Moe(ori_x) = ori_x
       } else if (code <= CQ_INV_CONST_BASE) {
         const int c = CQ_INV_CONST_BASE - code;
         fma8_const(acc, w, a.alpha1[c], a.alpha2[c], ld_nc_v4(xrow + col),
@@ -156,9 +213,44 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(CombineArgs a, int nc
   }
   for (int k = d.K; k < d.NS; ++k) {
     const int code = s_code[k];
-    if (code >= 0) add8(acc, ld_nc_v4(a.ffn + (int64_t)code * H + col));
+    if (code >= 0) {
+      float f[8];
+      src.floats(src.load(code, H, u), f);
+      add8f(acc, f);
+    }
   }
   store8<OUT_F32>(a.y, tok * H + col, acc);
+}
+
+// Combine-side int8 quantisation of the expert outputs before they are sent
+// back ("CANN MoE Dispatch/Combine 通信算子性能优化实践", Int8QuantProcess):
+// per block of 8 values, scale = max|v| * fl(1/127), code = RNE(v / scale).
+// One CTA per (row, chunk); rows past the dispatched total are skipped.
+__global__ void __launch_bounds__(kThreads) combine_quant_kernel(CombineArgs a, int nchunk) {
+  griddep_wait();  // the rows may come from the preceding kernel
+  const Dims& d = a.d;
+  const int64_t row = blockIdx.x / nchunk;
+  const int chunk = blockIdx.x - (int)(row * nchunk);
+  if (row >= (int64_t)*a.total_rows) return;
+  const int H = d.H;
+  const int u = chunk * kThreads + threadIdx.x;
+  if (u >= (H >> 3)) return;
+  float f[8];
+  SrcBf16{a.ffn}.floats(SrcBf16{a.ffn}.load(row, H, u), f);
+  float m = 0.f;
+#pragma unroll
+  for (int t = 0; t < 8; ++t) m = fmaxf(m, fabsf(f[t]));
+  const float s = __fmul_rn(m, __fdiv_rn(1.f, 127.f));
+  uint32_t w[2] = {0u, 0u};
+#pragma unroll
+  for (int t = 0; t < 8; ++t) {
+    int c = __float2int_rn(__fdiv_rn(f[t], s));  // 0/0 is NaN, which converts to 0
+    c = max(-128, min(127, c));
+    w[t >> 2] |= ((uint32_t)c & 0xffu) << (8 * (t & 3));
+  }
+  int8_t* dst = a.ffn_q + row * H + 8 * (int64_t)u;
+  asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(dst), "r"(w[0]), "r"(w[1]) : "memory");
+  a.ffn_scales[row * (H >> 3) + u] = s;
 }
 
 }  // namespace
@@ -166,10 +258,28 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(CombineArgs a, int nc
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) {
   const int units = a.d.H >> 3;
   const int nchunk = (units + kThreads - 1) / kThreads;
-  const int64_t grid = (int64_t)a.d.W * a.d.BS * nchunk;
+  const dim3 grid((unsigned)((int64_t)a.d.W * a.d.BS * nchunk));
+  const SrcBf16 src{a.ffn};
   if (a.out_f32)
-    return launch_pdl(combine_kernel<true>, dim3((unsigned)grid), dim3(kThreads), 0, s, a, nchunk);
-  return launch_pdl(combine_kernel<false>, dim3((unsigned)grid), dim3(kThreads), 0, s, a, nchunk);
+    return launch_pdl(combine_kernel<true, SrcBf16>, grid, dim3(kThreads), 0, s, a, src, nchunk);
+  return launch_pdl(combine_kernel<false, SrcBf16>, grid, dim3(kThreads), 0, s, a, src, nchunk);
+}
+
+cudaError_t launch_combine_q8(const CombineArgs& a, cudaStream_t s) {
+  const int units = a.d.H >> 3;
+  const int nchunk = (units + kThreads - 1) / kThreads;
+  const dim3 grid((unsigned)((int64_t)a.d.W * a.d.BS * nchunk));
+  const SrcQ8 src{a.ffn_q, a.ffn_scales};
+  if (a.out_f32)
+    return launch_pdl(combine_kernel<true, SrcQ8>, grid, dim3(kThreads), 0, s, a, src, nchunk);
+  return launch_pdl(combine_kernel<false, SrcQ8>, grid, dim3(kThreads), 0, s, a, src, nchunk);
+}
+
+cudaError_t launch_combine_quant(const CombineArgs& a, cudaStream_t s) {
+  const int units = a.d.H >> 3;
+  const int nchunk = (units + kThreads - 1) / kThreads;
+  const dim3 grid((unsigned)(a.d.R_max * nchunk));
+  return launch_pdl(combine_quant_kernel, grid, dim3(kThreads), 0, s, a, nchunk);
 }
 
 }  // namespace cq

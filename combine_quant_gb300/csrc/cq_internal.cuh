@@ -98,12 +98,16 @@ struct PermuteArgs {
   int32_t* assist_rows;  // [R_max][4]
   int32_t* inv;          // [W*BS*NS]
   float* expand_scales;
+  int32_t scale_rows_bulk;  // mode 5: scale rows are 16-byte sized and aligned (bulk stores)
   Workspace ws;
 };
 
 struct CombineArgs {
   Dims d;
-  const uint16_t* ffn;
+  const uint16_t* ffn;         // bf16 expert outputs [R_max, H] (bf16 combine, quantiser input)
+  int8_t* ffn_q;               // int8 expert outputs [R_max, H] (int8 combine input, quantiser output)
+  float* ffn_scales;           // their block scales [R_max, H/8]
+  const int32_t* total_rows;   // rank_row_base[W] inside assist_info (quantiser)
   const int32_t* inv;
   const float* expert_scales;
   const uint16_t* ori_x;
@@ -142,6 +146,8 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 // Launchers (each returns the cudaError_t of its launch).
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
 cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t s);
-cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);     // from bf16 rows
+cudaError_t launch_combine_q8(const CombineArgs& a, cudaStream_t s);  // from int8 rows
+cudaError_t launch_combine_quant(const CombineArgs& a, cudaStream_t s);
 
 }  // namespace cq

@@ -5,11 +5,12 @@
 // ordinal, the address rule of "MoeDistributeDispatch和MoeDistributeCombine
 // 算子设计介绍" §3.4.2 with the source block folded into the expert offset),
 // writes the inverse map, the (src, token, slot) row record and the carried
-// weight. All threads then load the token row once with 128-bit loads,
-// quantise it in registers and store the codes to every routed row with
-// 128-bit stores: quant_mode 0 copies the bf16 row, quant_mode 2 is per-token
-// dynamic int8 (optionally per-expert smoothed, then quantised once per
-// slot), quant_mode 5 is mx-clip e4m3 with one power-of-two scale per 32
+// weight. All threads load the token row once with 128-bit loads (started
+// before the routing kernels finish), quantise it in registers and stage the
+// code row in shared memory; one thread then writes it to every routed row
+// with bulk (TMA) stores. quant_mode 0 copies the bf16 row, quant_mode 2 is
+// per-token dynamic int8 (optionally per-expert smoothed, then quantised once
+// per slot), quant_mode 5 is mx-clip e4m3 with one power-of-two scale per 32
 // elements ("low_latency_dispatch" 计算公式).
 //
 // Arithmetic is fixed to single IEEE binary32 operations (explicit _rn
@@ -30,10 +31,31 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
   return v;
 }
 
-__device__ __forceinline__ void st_v4(void* p, uint4 v) {
-  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
-               "r"(v.w)
+__device__ __forceinline__ void st_shared_v4(void* p, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
+                   (uint32_t)__cvta_generic_to_shared(p)),
+               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
+}
+
+// Bulk (TMA) stores of staged rows: shared memory -> global, issued by one
+// thread, completion tracked in bulk groups. Both addresses 16-byte aligned,
+// size a multiple of 16.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> bulk reads
+}
+__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+               "r"((uint32_t)__cvta_generic_to_shared(ssrc)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -153,6 +175,7 @@ __global__ void __launch_bounds__(256) permute_kernel(PermuteArgs a) {
   __shared__ int s_srow[kMaxSlots];  // their smooth-table rows
   __shared__ int s_nrows;
   __shared__ float s_red[2][32];
+  extern __shared__ __align__(128) uint8_t s_stage[];  // staged code row(s) + mx scale row
 
   const Dims& d = a.d;
   const int64_t tok = blockIdx.x;
@@ -238,37 +261,50 @@ __global__ void __launch_bounds__(256) permute_kernel(PermuteArgs a) {
   if (nrows == 0) return;
   if (!prefetched) load_row();  // routing found rows the inputs did not predict
 
+  // Every mode stages its code row once in shared memory; thread 0 then
+  // writes it to each routed row with one bulk (TMA) store per row, so the
+  // K-fold store traffic costs no per-thread store instructions.
+  uint8_t* const stage = s_stage;
   if (MODE == 0) {
-    for (int n = 0; n < nrows; ++n) {
-      uint16_t* dst = static_cast<uint16_t*>(a.expand_x) + (int64_t)s_row[n] * H;
+    // quant_mode 0: the bf16 row itself travels ([DV3] 情形 1).
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int u = threadIdx.x + q * blockDim.x;
-        if (U.ok[q]) {
-          st_v4(dst + 16 * u, U.v[q][0]);
-          st_v4(dst + 16 * u + 8, U.v[q][1]);
-        }
+    for (int q = 0; q < 2; ++q) {
+      const int u = threadIdx.x + q * blockDim.x;
+      if (U.ok[q]) {
+        st_shared_v4(stage + 32 * u, U.v[q][0]);
+        st_shared_v4(stage + 32 * u + 16, U.v[q][1]);
       }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int n = 0; n < nrows; ++n)
+        bulk_store(static_cast<uint16_t*>(a.expand_x) + (int64_t)s_row[n] * H, stage, 2u * H);
+      bulk_commit();
+      bulk_wait_read<0>();
     }
   } else if (MODE == 2 && !SMOOTH) {
     // One quantisation per token: every routed row gets the same codes.
     const float amax = block_max(fmaxf(unit_amax(U.v[0]), unit_amax(U.v[1])), s_red[0]);
     const float s = __fdiv_rn(127.f, amax);
     const float deq = __fdiv_rn(1.f, s);
-    uint4 c[2];
 #pragma unroll
-    for (int q = 0; q < 2; ++q) c[q] = unit_q8(U.v[q], s);
-    for (int n = 0; n < nrows; ++n) {
-      int8_t* dst = static_cast<int8_t*>(a.expand_x) + (int64_t)s_row[n] * H;
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int u = threadIdx.x + q * blockDim.x;
-        if (U.ok[q]) st_v4(dst + 16 * u, c[q]);
-      }
-      if (threadIdx.x == 0) static_cast<float*>(a.dynamic_scales)[s_row[n]] = deq;
+    for (int q = 0; q < 2; ++q) {
+      const int u = threadIdx.x + q * blockDim.x;
+      if (U.ok[q]) st_shared_v4(stage + 16 * u, unit_q8(U.v[q], s));
     }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int n = 0; n < nrows; ++n)
+        bulk_store(static_cast<int8_t*>(a.expand_x) + (int64_t)s_row[n] * H, stage, (uint32_t)H);
+      bulk_commit();
+      bulk_wait_read<0>();
+    }
+    if (threadIdx.x < nrows) static_cast<float*>(a.dynamic_scales)[s_row[threadIdx.x]] = deq;
   } else if (MODE == 2 && SMOOTH) {
     // x_fp32 = x * smooth[expert]: one amax and one scale per routed row.
+    // Two staging buffers: row n is built while row n-1's bulk store reads.
     for (int n = 0; n < nrows; ++n) {
       const float* sm = a.smooth + (int64_t)s_srow[n] * H;
       float xf[2][16];
@@ -285,42 +321,62 @@ __global__ void __launch_bounds__(256) permute_kernel(PermuteArgs a) {
 #pragma unroll
         for (int t = 0; t < 16; ++t) m = fmaxf(m, fabsf(xf[q][t]));
       }
+      // block_max starts with a barrier: thread 0's wait below for the
+      // store of row n-2 (same buffer) is complete before anyone writes it.
       const float amax = block_max(m, s_red[n & 1]);
       const float s = __fdiv_rn(127.f, amax);
-      int8_t* dst = static_cast<int8_t*>(a.expand_x) + (int64_t)s_row[n] * H;
+      uint8_t* buf = stage + (n & 1) * H;
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         const int u = threadIdx.x + q * blockDim.x;
-        if (U.ok[q]) st_v4(dst + 16 * u, floats_q8(xf[q], s));
+        if (U.ok[q]) st_shared_v4(buf + 16 * u, floats_q8(xf[q], s));
       }
-      if (threadIdx.x == 0) static_cast<float*>(a.dynamic_scales)[s_row[n]] = __fdiv_rn(1.f, s);
+      fence_proxy_async_smem();
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        bulk_store(static_cast<int8_t*>(a.expand_x) + (int64_t)s_row[n] * H, buf, (uint32_t)H);
+        bulk_commit();
+        bulk_wait_read<1>();
+        static_cast<float*>(a.dynamic_scales)[s_row[n]] = __fdiv_rn(1.f, s);
+      }
     }
+    if (threadIdx.x == 0) bulk_wait_read<0>();
   } else if (MODE == 5) {
-    // Lanes 2m and 2m+1 hold the two halves of one 32-element block.
-    uint4 c[2];
-    int e[2];
+    // Lanes 2m and 2m+1 hold the two halves of one 32-element block. The
+    // e8m0 scale row is staged after the code row.
+    uint8_t* srow_stage = stage + H;
+    const int nblk = units >> 1;
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
       float m = unit_amax(U.v[q]);
       m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
       m = fmaxf(m, 1e-4f);
-      e[q] = ceil_log2_bits(__fdiv_rn(m, 448.f));
-      c[q] = unit_e4m3(U.v[q], e[q]);
-    }
-    const int nblk = units >> 1;
-    for (int n = 0; n < nrows; ++n) {
-      const int64_t row = s_row[n];
-      uint8_t* dst = static_cast<uint8_t*>(a.expand_x) + row * H;
-      uint8_t* sc = static_cast<uint8_t*>(a.dynamic_scales) + row * d.SC;
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int u = threadIdx.x + q * blockDim.x;
-        if (U.ok[q]) {
-          st_v4(dst + 16 * u, c[q]);
-          if ((u & 1) == 0) sc[u >> 1] = (uint8_t)(e[q] + 127);
-        }
+      const int e = ceil_log2_bits(__fdiv_rn(m, 448.f));
+      const int u = threadIdx.x + q * blockDim.x;
+      if (U.ok[q]) {
+        st_shared_v4(stage + 16 * u, unit_e4m3(U.v[q], e));
+        if ((u & 1) == 0) srow_stage[u >> 1] = (uint8_t)(e + 127);
       }
-      if (threadIdx.x == 0 && d.SC > nblk) sc[nblk] = 0;  // Align2 padding column
+    }
+    if (threadIdx.x == 0 && d.SC > nblk) srow_stage[nblk] = 0;  // Align2 padding column
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int n = 0; n < nrows; ++n) {
+        const int64_t row = s_row[n];
+        bulk_store(static_cast<uint8_t*>(a.expand_x) + row * H, stage, (uint32_t)H);
+        if (a.scale_rows_bulk)
+          bulk_store(static_cast<uint8_t*>(a.dynamic_scales) + row * d.SC, srow_stage,
+                     (uint32_t)d.SC);
+      }
+      bulk_commit();
+      bulk_wait_read<0>();
+    }
+    if (!a.scale_rows_bulk) {  // scale rows not 16-byte sized / aligned: plain stores
+      for (int n = 0; n < nrows; ++n) {
+        uint8_t* sc = static_cast<uint8_t*>(a.dynamic_scales) + (int64_t)s_row[n] * d.SC;
+        for (int b = threadIdx.x; b < d.SC; b += blockDim.x) sc[b] = srow_stage[b];
+      }
     }
   }
   // This CTA's stores are issued: the combine kernel may start launching.
@@ -333,7 +389,11 @@ cudaError_t launch_mode(const PermuteArgs& a, cudaStream_t s) {
   int threads = ((units + 1) / 2 + 31) / 32 * 32;
   if (threads < 32) threads = 32;
   const int64_t grid = (int64_t)a.d.W * a.d.BS;
-  return launch_pdl(permute_kernel<MODE, SMOOTH>, dim3((unsigned)grid), dim3(threads), 0, s, a);
+  // Staging: one bf16 row (mode 0), one or two int8 rows (mode 2, two when
+  // smoothed per slot), or an e4m3 row plus its scale row (mode 5).
+  size_t smem = MODE == 0 ? 2 * (size_t)a.d.H : (size_t)a.d.H * (SMOOTH ? 2 : 1);
+  if (MODE == 5) smem += ((size_t)a.d.SC + 15) & ~size_t(15);
+  return launch_pdl(permute_kernel<MODE, SMOOTH>, dim3((unsigned)grid), dim3(threads), smem, s, a);
 }
 
 }  // namespace

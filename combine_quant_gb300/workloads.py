@@ -185,7 +185,23 @@ def skew(seed: int = 4, W: int = 16, BS: int = 512, M: int = 128, K: int = 16,
     return Workload("skew", cfg, x, ids, w, smooth, None, bs, seed=seed)
 
 
-WORKLOADS = {"tiny": tiny, "dsv3": dsv3, "mxfp8": mxfp8, "special": special, "skew": skew}
+def perf_table(bs: int, seed: int = 5, quant_mode: int = 0) -> Workload:
+    """The shape of the performance table of "CANN MoE Dispatch/Combine 通信
+    算子性能优化实践" (性能数据): 8 ranks, 4 experts per rank, K=8, H=7168,
+    BS 8 or 256 per rank. Routing: top-8 of N(0,1) logits; x ~ N(0,1)."""
+    W, L, K, H = 8, 4, 8, 7168
+    M = W * L
+    rng = np.random.Generator(np.random.PCG64(seed + bs))
+    cfg = make_config(ep_world_size=W, moe_expert_num=M, max_bs=bs, topk=K, hidden=H,
+                      quant_mode=quant_mode, expert_token_nums_type=1)
+    x = _normal_bf16(rng, (W, bs, H))
+    ids, w = _router_topk(rng, W * bs, M, K, bias_sd=0.0)
+    return Workload(f"perf_table_bs{bs}", cfg, x, ids.reshape(W, bs, K), w.reshape(W, bs, K),
+                    seed=seed)
+
+
+WORKLOADS = {"tiny": tiny, "dsv3": dsv3, "mxfp8": mxfp8, "special": special, "skew": skew,
+             "perf8": lambda: perf_table(8), "perf256": lambda: perf_table(256)}
 
 
 def ffn_standin(seed: int, rows: int, H: int, chunk: int = 1 << 24) -> np.ndarray:

@@ -190,6 +190,31 @@ int cq_combine(const cq_config* cfg, const void* expand_x_ffn, const int32_t* as
                const float* const_alpha1, const float* const_alpha2, const void* const_v,
                int32_t out_dtype, void* y, void* stream);
 
+/*
+ * Combine with int8 expert outputs ("CANN MoE Dispatch/Combine 通信算子性能
+ * 优化实践", 通信前量化: Combine 发送前按 block 量化为 int8, Int8QuantProcess /
+ * Int8DequantProcess). The expert side quantises each output row before it is
+ * sent back, in blocks of 8 values (32 bytes of fp32): scale = max|v| times
+ * fl(1/127), code = round-to-nearest-even(v / scale) saturated to int8 (an
+ * all-zero block has scale 0 and codes 0). The receiving side dequantises
+ * each value (code * scale, one binary32 rounding) and then forms exactly the
+ * sum of cq_combine.
+ *
+ * cq_combine_quant: expand_x_ffn bf16 [R_max, H] -> ffn_codes int8 [R_max, H]
+ *   and ffn_scales f32 [R_max, H/8]; only the dispatched rows (the total in
+ *   assist_info) are written. A producer that fuses this quantisation into
+ *   its own epilogue can skip this call.
+ * cq_combine_q8: as cq_combine, reading ffn_codes / ffn_scales instead of
+ *   bf16 rows (0.5 fewer bytes per value).
+ */
+int cq_combine_quant(const cq_config* cfg, const void* expand_x_ffn, const int32_t* assist_info,
+                     int8_t* ffn_codes, float* ffn_scales, void* stream);
+int cq_combine_q8(const cq_config* cfg, const int8_t* ffn_codes, const float* ffn_scales,
+                  const int32_t* assist_info, const int32_t* ep_recv_count,
+                  const float* expert_scales, const void* ori_x, const float* const_alpha1,
+                  const float* const_alpha2, const void* const_v, int32_t out_dtype, void* y,
+                  void* stream);
+
 /* The spec names of the two operators: identical to cq_dispatch / cq_combine. */
 int moe_dispatch(const cq_config* cfg, const void* x, const int32_t* expert_ids,
                  const float* smooth_scales, const uint8_t* x_active_mask,

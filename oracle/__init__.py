@@ -99,6 +99,11 @@ def lib() -> ctypes.CDLL:
         for name in ("cqo_e4m3_encode_n", "cqo_bf16_from_f32_n", "cqo_ceil_log2_n"):
             getattr(L, name).argtypes = [P, P, ctypes.c_int64]
             getattr(L, name).restype = None
+        L.cqo_combine_quant_row.argtypes = [ctypes.c_int32, P, P, P]
+        L.cqo_combine_quant_row.restype = ctypes.c_int
+        L.cqo_combine_token_q8.argtypes = [cfgp, ctypes.c_int32, ctypes.c_int32] + [P] * 8 + [
+            ctypes.c_int32, P]
+        L.cqo_combine_token_q8.restype = ctypes.c_int
         _LIB = L
     return _LIB
 
@@ -310,3 +315,41 @@ def ceil_log2_array(v) -> np.ndarray:
     out = np.empty(a.shape, np.int32)
     lib().cqo_ceil_log2_n(_ptr(a), _ptr(out), a.size)
     return out
+
+
+def combine_quant_row(row_bits):
+    """Combine-side int8 block quantisation of one bf16 row: (codes, scales)."""
+    x = _c(row_bits, np.uint16)
+    H = x.shape[0]
+    codes, scales = np.empty(H, np.int8), np.empty(H // 8, np.float32)
+    rc = lib().cqo_combine_quant_row(H, _ptr(x), _ptr(codes), _ptr(scales))
+    if rc != OK:
+        raise ValueError(f"oracle combine_quant_row failed: {rc}")
+    return codes, scales
+
+
+def combine_quant_rows(rows_bits):
+    rows = _c(rows_bits, np.uint16)
+    codes = np.empty(rows.shape, np.int8)
+    scales = np.empty((rows.shape[0], rows.shape[1] // 8), np.float32)
+    for n in range(rows.shape[0]):
+        codes[n], scales[n] = combine_quant_row(rows[n])
+    return codes, scales
+
+
+def combine_tokens_q8(cfg: dict, tokens, codes, scales, inv, expert_scales, ori_x=None,
+                      const_alpha1=None, const_alpha2=None, const_v=None, out_f32=False):
+    """Combine the listed (r, i) tokens from int8 expert outputs."""
+    H = cfg["hidden"]
+    y = np.empty((len(tokens), H), np.float32 if out_f32 else np.uint16)
+    args = [_c(codes, np.int8), _c(scales, np.float32), _c(inv, np.int32),
+            _c(expert_scales, np.float32), _c(ori_x, np.uint16), _c(const_alpha1, np.float32),
+            _c(const_alpha2, np.float32), _c(const_v, np.uint16)]
+    ptrs = [_ptr(a) for a in args]
+    cfgc = _cfg(cfg)
+    for n, (r, i) in enumerate(tokens):
+        rc = lib().cqo_combine_token_q8(ctypes.byref(cfgc), int(r), int(i), *ptrs, int(out_f32),
+                                        _ptr(y[n]))
+        if rc != OK:
+            raise ValueError(f"oracle combine_token_q8 failed: {rc}")
+    return y

@@ -498,3 +498,74 @@ int cqo_combine(const cqo_config* c, const uint16_t* ffn, const int32_t* inv,
   }
   return CQO_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Combine-side int8 quantisation, [PERF] 通信前量化 / Int8QuantProcess and   */
+/* Int8DequantProcess: before an expert output row is sent back it is cut     */
+/* into 32-byte blocks of 8 float values; per block the scale is the largest  */
+/* magnitude times 1/SCALE_PARAM (SCALE_PARAM = 127), each value is divided by */
+/* the scale and cast to int8; the receiver multiplies back by the scale.     */
+/* ------------------------------------------------------------------------ */
+
+int cqo_combine_quant_row(int32_t H, const uint16_t* row, int8_t* codes, float* scales) {
+  if (H % 8 != 0) return CQO_ERR_ARG;
+  const float inv_param = 1.0f / 127.0f; /* the constant 1/SCALE_PARAM, rounded once */
+  for (int32_t b = 0; b < H / 8; ++b) {
+    float m = 0.0f;
+    for (int32_t t = 0; t < 8; ++t) {
+      float a = fabsf(cqo_bf16_to_f32(row[b * 8 + t]));
+      if (a > m) m = a;
+    }
+    const float scale = m * inv_param; /* Muls(1/SCALE_PARAM) */
+    for (int32_t t = 0; t < 8; ++t) {
+      /* Div, then one round-to-nearest-even cast (0/0 = NaN gives 0) */
+      codes[b * 8 + t] = sat_rne_int8(cqo_bf16_to_f32(row[b * 8 + t]) / scale);
+    }
+    scales[b] = scale;
+  }
+  return CQO_OK;
+}
+
+int cqo_combine_token_q8(const cqo_config* c, int32_t r, int32_t i, const int8_t* ffn_codes,
+                         const float* ffn_scales, const int32_t* inv, const float* expert_scales,
+                         const uint16_t* ori_x, const float* const_alpha1,
+                         const float* const_alpha2, const uint16_t* const_v, int32_t out_f32,
+                         void* y_row) {
+  const int32_t H = c->hidden, K = c->topk, BS = c->max_bs;
+  if (H % 8 != 0) return CQO_ERR_ARG;
+  const int32_t Seff = (c->shared_expert_rank_num > 0) ? c->shared_expert_num : 0;
+  const int32_t NS = K + Seff;
+  const int64_t tok = (int64_t)r * BS + i;
+  const int32_t* slots = inv + tok * NS;
+  for (int32_t h = 0; h < H; ++h) {
+    float acc = 0.0f;
+    for (int32_t j = 0; j < K; ++j) {
+      const int32_t code = slots[j];
+      const float w = expert_scales[tok * K + j];
+      float v;
+      if (code >= 0) {
+        /* received row: dequantise first (int8 value times its block scale) */
+        v = (float)ffn_codes[(int64_t)code * H + h] * ffn_scales[(int64_t)code * (H / 8) + h / 8];
+      } else if (code == CQO_INV_COPY) {
+        v = cqo_bf16_to_f32(ori_x[tok * H + h]);
+      } else if (code <= CQO_INV_CONST_BASE) {
+        const int32_t q = CQO_INV_CONST_BASE - code;
+        const float p1 = const_alpha1[q] * cqo_bf16_to_f32(ori_x[tok * H + h]);
+        const float p2 = const_alpha2[q] * cqo_bf16_to_f32(const_v[(int64_t)q * H + h]);
+        v = p1 + p2;
+      } else {
+        continue;
+      }
+      acc = fmaf(w, v, acc);
+    }
+    for (int32_t s = 0; s < Seff; ++s) {
+      const int32_t code = slots[K + s];
+      if (code >= 0)
+        acc = acc + (float)ffn_codes[(int64_t)code * H + h] *
+                        ffn_scales[(int64_t)code * (H / 8) + h / 8];
+    }
+    if (out_f32) ((float*)y_row)[h] = acc;
+    else ((uint16_t*)y_row)[h] = cqo_bf16_from_f32(acc);
+  }
+  return CQO_OK;
+}

@@ -110,6 +110,20 @@ int cqo_combine(const cqo_config* c, const uint16_t* ffn, const int32_t* inv,
                 const float* expert_scales, const uint16_t* ori_x, const float* const_alpha1,
                 const float* const_alpha2, const uint16_t* const_v, int32_t out_f32, void* y);
 
+/* Combine-side int8 block quantisation of one expert-output row of H bf16
+ * values: blocks of 8 elements, scale = max|v| * fl(1/127), codes =
+ * RNE(v / scale) saturated to int8. codes [H], scales [H/8] (H % 8 == 0). */
+int cqo_combine_quant_row(int32_t hidden, const uint16_t* row, int8_t* codes, float* scales);
+
+/* Combine one token from int8 expert outputs: each routed / shared row is
+ * dequantised (code * block scale) before the weighted sum. ffn_codes is
+ * [rows, H] int8, ffn_scales [rows, H/8]. Otherwise as cqo_combine_token. */
+int cqo_combine_token_q8(const cqo_config* c, int32_t r, int32_t i, const int8_t* ffn_codes,
+                         const float* ffn_scales, const int32_t* inv, const float* expert_scales,
+                         const uint16_t* ori_x, const float* const_alpha1,
+                         const float* const_alpha2, const uint16_t* const_v, int32_t out_f32,
+                         void* y_row);
+
 /* Format helpers, exposed so the tests can pin them on their own. */
 uint8_t cqo_e4m3_encode(float v);  /* round to nearest even, saturate to +-448 */
 float cqo_e4m3_decode(uint8_t b);

@@ -1,0 +1,86 @@
+"""GPU parity of the combine-side int8 path against the oracle: the expert-side
+block quantiser (codes and scales bit-exact) and the dequantising combine
+(fp32 within 1e-5 and bf16 within 1 ulp; exact agreement is also asserted,
+both sides use the same operation order)."""
+import numpy as np
+import pytest
+import torch
+
+import gpu_harness as gh
+import oracle
+from combine_quant_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+def _case(name):
+    return {
+        "tiny": lambda: workloads.tiny(0, 2),
+        "special_small": lambda: workloads.special(seed=23, W=8, BS=20, H=1024, M=48),
+        "skew_small": lambda: workloads.skew(seed=24, W=4, BS=64, M=32, K=16, H=2048),
+        "dsv3": lambda: workloads.dsv3(),
+    }[name]()
+
+
+@pytest.mark.parametrize("name", ["tiny", "special_small", "skew_small", "dsv3"])
+def test_combine_q8_parity(name):
+    import combine_quant_gb300 as cq
+    wl = _case(name)
+    cfg, out, status, _ = gh.gpu_dispatch(wl)
+    ref = oracle.route(wl.cfg, wl.expert_ids, wl.mask, wl.bs_per_rank)
+    ffn = gh.FfnStandin(wl, cfg.max_rows)
+    codes, scales = cq.combine_quant(cfg, ffn.device_rows, out.assist_info)
+    # quantiser: every dispatched row against the oracle's quantisation of its pool row
+    pc, ps = oracle.combine_quant_rows(ffn.pool)
+    R = ref.rows
+    idx = np.arange(R, dtype=np.int64)
+    if R > 4096:
+        idx = np.unique(np.concatenate([idx[:512], idx[-512:], np.random.default_rng(3).integers(
+            0, R, 2048)]))
+    ti = torch.from_numpy(idx).to(gh.DEV)
+    gc = gh.host(codes.index_select(0, ti))
+    gs = gh.host(scales.index_select(0, ti))
+    src = (idx * 7919) % ffn.P
+    assert np.array_equal(gc, pc[src]), "int8 codes differ"
+    assert np.array_equal(gs.view(np.uint32), ps[src].view(np.uint32)), "block scales differ"
+    # dequantising combine
+    W, BS = wl.cfg["ep_world_size"], wl.cfg["max_bs"]
+    w = gh.dev(wl.expert_scales, torch.float32)
+    kw = dict(ori_x=gh.dev(wl.x, torch.bfloat16), const_alpha1=gh.dev(wl.const_alpha1, torch.float32),
+              const_alpha2=gh.dev(wl.const_alpha2, torch.float32),
+              const_v=gh.dev(wl.const_v, torch.bfloat16))
+    y32 = cq.combine_q8(cfg, codes, scales, out.assist_info, w, out.ep_recv_count,
+                        out_dtype=torch.float32, **kw)
+    yb = cq.combine_q8(cfg, codes, scales, out.assist_info, w, out.ep_recv_count, **kw)
+    if W * BS <= 2048:
+        toks = [(r, i) for r in range(W) for i in range(BS)]
+    else:
+        rng = np.random.default_rng(5)
+        toks = [(r, 0) for r in range(W)] + [(r, BS - 1) for r in range(W)] + [
+            (int(a), int(b)) for a, b in zip(rng.integers(0, W, 96), rng.integers(0, BS, 96))]
+    tt = torch.tensor([r * BS + i for r, i in toks], device=gh.DEV)
+    g32 = gh.host(y32.view(W * BS, -1).index_select(0, tt))
+    gb = gh.host(yb.view(W * BS, -1).index_select(0, tt))
+    inv = ffn.remap_inv(ref.inv)
+    r32 = oracle.combine_tokens_q8(wl.cfg, toks, pc, ps, inv, wl.expert_scales, wl.x,
+                                   wl.const_alpha1, wl.const_alpha2, wl.const_v, out_f32=True)
+    rb = oracle.combine_tokens_q8(wl.cfg, toks, pc, ps, inv, wl.expert_scales, wl.x,
+                                  wl.const_alpha1, wl.const_alpha2, wl.const_v, out_f32=False)
+    assert np.max(np.abs(g32 - r32)) <= 1e-5
+    assert np.max(gh.bf16_ulp_diff(gb, rb)) <= 1
+    assert np.array_equal(g32.view(np.uint32), r32.view(np.uint32))
+    assert np.array_equal(gb, rb)
+
+
+def test_combine_quant_zero_rows():
+    """All-zero expert rows: scale 0, codes 0, and a zero contribution."""
+    import combine_quant_gb300 as cq
+    wl = workloads.tiny(1, 2)
+    cfg, out, _, _ = gh.gpu_dispatch(wl)
+    zeros = torch.zeros(cfg.max_rows, cfg.hidden, dtype=torch.bfloat16, device=gh.DEV)
+    codes, scales = cq.combine_quant(cfg, zeros, out.assist_info)
+    R = int(gh.host(cq.assist_views(cfg, out.assist_info)[2])[-1])
+    assert torch.count_nonzero(codes[:R]) == 0 and torch.count_nonzero(scales[:R]) == 0
+    y = cq.combine_q8(cfg, codes, scales, out.assist_info, gh.dev(wl.expert_scales, torch.float32),
+                      out_dtype=torch.float32)
+    assert torch.count_nonzero(y) == 0
