@@ -33,6 +33,8 @@ class Config:
     quant_mode: int = 0
     expert_token_nums_type: int = 1
     mask_ndim: int = 0
+    x_dtype: int = 0       # 0 bf16, 1 fp16
+    smooth_kind: int = 0   # 0 per-expert rows, 1 one row for all experts, 2 one scalar
 
     @classmethod
     def from_dict(cls, d: dict) -> "Config":
@@ -73,8 +75,17 @@ class Config:
     def workspace_size(self) -> int:
         return self._q("cq_workspace_size")
 
+    @property
+    def token_dtype(self) -> torch.dtype:
+        return torch.float16 if self.x_dtype == 1 else torch.bfloat16
+
+    @property
+    def group_cols(self) -> int:
+        return (self.hidden + 127) // 128
+
     def code_dtype(self) -> torch.dtype:
-        return {0: torch.bfloat16, 2: torch.int8, 5: torch.uint8}[self.quant_mode]
+        return {0: self.token_dtype, 1: torch.int8, 2: torch.int8, 3: torch.uint8,
+                4: torch.uint8, 5: torch.uint8}[self.quant_mode]
 
 
 @functools.lru_cache(maxsize=256)
@@ -128,7 +139,9 @@ def alloc_dispatch_outputs(cfg: Config, device, with_expand_scales: bool = True)
     L = cfg.local_expert_num
     if cfg.quant_mode == 2:
         dyn = torch.empty(R, dtype=torch.float32, device=device)
-    elif cfg.quant_mode == 5:
+    elif cfg.quant_mode == 3:
+        dyn = torch.empty(R, cfg.group_cols, dtype=torch.float32, device=device)
+    elif cfg.quant_mode in (4, 5):
         dyn = torch.empty(R, cfg.scale_cols, dtype=torch.uint8, device=device)
     else:
         dyn = None
@@ -145,10 +158,11 @@ def _check_inputs(cfg, x, expert_ids, smooth_scales, x_active_mask, bs_per_rank,
     dev = expert_ids.device
     _need(expert_ids, "expert_ids", torch.int32, (W, BS, K))
     if x is not None:
-        _need(x, "x", torch.bfloat16, (W, BS, H), dev)
+        _need(x, "x", cfg.token_dtype, (W, BS, H), dev)
     if smooth_scales is not None:
         s_eff = cfg.shared_expert_num if cfg.shared_expert_rank_num > 0 else 0
-        _need(smooth_scales, "smooth_scales", torch.float32, (s_eff + cfg.moe_expert_num, H), dev)
+        shape = {0: (s_eff + cfg.moe_expert_num, H), 1: (H,), 2: (1,)}[cfg.smooth_kind]
+        _need(smooth_scales, "smooth_scales", torch.float32, shape, dev)
     if cfg.mask_ndim == 1:
         _need(x_active_mask, "x_active_mask", torch.uint8, (W, BS), dev)
     elif cfg.mask_ndim == 2:
@@ -217,21 +231,23 @@ def combine(cfg: Config, expand_x_ffn: torch.Tensor, assist_info: torch.Tensor,
             const_alpha1: Optional[torch.Tensor] = None,
             const_alpha2: Optional[torch.Tensor] = None,
             const_v: Optional[torch.Tensor] = None,
-            out_dtype: torch.dtype = torch.bfloat16,
+            out_dtype: Optional[torch.dtype] = None,
             y: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """MoE combine (cq_combine): y [W, BS, H] in bf16 or float32."""
+    """MoE combine (cq_combine): y [W, BS, H] in the token dtype (default) or float32."""
     W, BS, K, H = cfg.ep_world_size, cfg.max_bs, cfg.topk, cfg.hidden
     dev = assist_info.device
-    _need(expand_x_ffn, "expand_x_ffn", torch.bfloat16, (cfg.max_rows, H), dev)
+    _need(expand_x_ffn, "expand_x_ffn", cfg.token_dtype, (cfg.max_rows, H), dev)
     _need(assist_info, "assist_info", torch.int32, (cfg.assist_info_size,), dev)
     _need(expert_scales, "expert_scales", torch.float32, (W, BS, K), dev)
-    _need(ori_x, "ori_x", torch.bfloat16, (W, BS, H), dev)
+    _need(ori_x, "ori_x", cfg.token_dtype, (W, BS, H), dev)
     Q = cfg.const_expert_num
     _need(const_alpha1, "const_alpha1", torch.float32, (Q,), dev)
     _need(const_alpha2, "const_alpha2", torch.float32, (Q,), dev)
-    _need(const_v, "const_v", torch.bfloat16, (Q, H), dev)
-    if out_dtype not in (torch.bfloat16, torch.float32):
-        raise ValueError("out_dtype must be bfloat16 or float32")
+    _need(const_v, "const_v", cfg.token_dtype, (Q, H), dev)
+    if out_dtype is None:
+        out_dtype = cfg.token_dtype
+    if out_dtype not in (cfg.token_dtype, torch.float32):
+        raise ValueError("out_dtype must be the token dtype or float32")
     if y is None:
         y = torch.empty(W, BS, H, dtype=out_dtype, device=dev)
     _need(y, "y", out_dtype, (W, BS, H), dev)
@@ -239,7 +255,7 @@ def combine(cfg: Config, expand_x_ffn: torch.Tensor, assist_info: torch.Tensor,
     rc = _lib.load().cq_combine(
         ctypes.byref(c), _ptr(expand_x_ffn), _ptr(assist_info), _ptr(ep_recv_count),
         _ptr(expert_scales), _ptr(ori_x), _ptr(const_alpha1), _ptr(const_alpha2), _ptr(const_v),
-        0 if out_dtype == torch.bfloat16 else 1, _ptr(y), _stream(dev))
+        0 if out_dtype != torch.float32 else 1, _ptr(y), _stream(dev))
     _lib.check(rc, "cq_combine")
     return y
 
@@ -250,7 +266,7 @@ def combine_quant(cfg: Config, expand_x_ffn: torch.Tensor, assist_info: torch.Te
     Returns (codes int8 [R_max, H], scales f32 [R_max, H/8])."""
     R, H = cfg.max_rows, cfg.hidden
     dev = assist_info.device
-    _need(expand_x_ffn, "expand_x_ffn", torch.bfloat16, (R, H), dev)
+    _need(expand_x_ffn, "expand_x_ffn", cfg.token_dtype, (R, H), dev)
     _need(assist_info, "assist_info", torch.int32, (cfg.assist_info_size,), dev)
     if codes is None:
         codes = torch.empty(R, H, dtype=torch.int8, device=dev)
@@ -271,7 +287,7 @@ def combine_q8(cfg: Config, codes: torch.Tensor, scales: torch.Tensor, assist_in
                const_alpha1: Optional[torch.Tensor] = None,
                const_alpha2: Optional[torch.Tensor] = None,
                const_v: Optional[torch.Tensor] = None,
-               out_dtype: torch.dtype = torch.bfloat16,
+               out_dtype: Optional[torch.dtype] = None,
                y: Optional[torch.Tensor] = None) -> torch.Tensor:
     """MoE combine from int8 expert outputs (cq_combine_q8)."""
     W, BS, K, H = cfg.ep_world_size, cfg.max_bs, cfg.topk, cfg.hidden
@@ -280,13 +296,15 @@ def combine_q8(cfg: Config, codes: torch.Tensor, scales: torch.Tensor, assist_in
     _need(scales, "scales", torch.float32, (cfg.max_rows, H // 8), dev)
     _need(assist_info, "assist_info", torch.int32, (cfg.assist_info_size,), dev)
     _need(expert_scales, "expert_scales", torch.float32, (W, BS, K), dev)
-    _need(ori_x, "ori_x", torch.bfloat16, (W, BS, H), dev)
+    _need(ori_x, "ori_x", cfg.token_dtype, (W, BS, H), dev)
     Q = cfg.const_expert_num
     _need(const_alpha1, "const_alpha1", torch.float32, (Q,), dev)
     _need(const_alpha2, "const_alpha2", torch.float32, (Q,), dev)
-    _need(const_v, "const_v", torch.bfloat16, (Q, H), dev)
-    if out_dtype not in (torch.bfloat16, torch.float32):
-        raise ValueError("out_dtype must be bfloat16 or float32")
+    _need(const_v, "const_v", cfg.token_dtype, (Q, H), dev)
+    if out_dtype is None:
+        out_dtype = cfg.token_dtype
+    if out_dtype not in (cfg.token_dtype, torch.float32):
+        raise ValueError("out_dtype must be the token dtype or float32")
     if y is None:
         y = torch.empty(W, BS, H, dtype=out_dtype, device=dev)
     _need(y, "y", out_dtype, (W, BS, H), dev)
@@ -294,7 +312,7 @@ def combine_q8(cfg: Config, codes: torch.Tensor, scales: torch.Tensor, assist_in
     rc = _lib.load().cq_combine_q8(
         ctypes.byref(c), _ptr(codes), _ptr(scales), _ptr(assist_info), _ptr(ep_recv_count),
         _ptr(expert_scales), _ptr(ori_x), _ptr(const_alpha1), _ptr(const_alpha2), _ptr(const_v),
-        0 if out_dtype == torch.bfloat16 else 1, _ptr(y), _stream(dev))
+        0 if out_dtype != torch.float32 else 1, _ptr(y), _stream(dev))
     _lib.check(rc, "cq_combine_q8")
     return y
 

@@ -35,12 +35,14 @@ int validate(const cq_config* c) {
   if (c->global_bs != 0 && c->global_bs != c->max_bs * W) return CQ_ERR_ARG;
   if (c->expert_token_nums_type != 0 && c->expert_token_nums_type != 1) return CQ_ERR_ARG;
   if (c->mask_ndim < 0 || c->mask_ndim > 2) return CQ_ERR_ARG;
-  if (c->quant_mode == 1 || c->quant_mode == 3 || c->quant_mode == 4) return CQ_ERR_UNSUPPORTED;
-  if (c->quant_mode != 0 && c->quant_mode != 2 && c->quant_mode != 5) return CQ_ERR_ARG;
+  if (c->quant_mode < 0 || c->quant_mode > 5) return CQ_ERR_ARG;
+  if (c->x_dtype != 0 && c->x_dtype != 1) return CQ_ERR_ARG;
+  if (c->smooth_kind < 0 || c->smooth_kind > 2) return CQ_ERR_ARG;
   // Vector paths: 16-element units (16-byte stores of int8 / e4m3 rows); mx
   // blocks of 32 never straddle two threads' units.
   if (c->hidden % 16 != 0) return CQ_ERR_UNSUPPORTED;
-  if (c->quant_mode == 5 && c->hidden % 32 != 0) return CQ_ERR_UNSUPPORTED;
+  if ((c->quant_mode == 4 || c->quant_mode == 5) && c->hidden % 32 != 0)
+    return CQ_ERR_UNSUPPORTED;
   return CQ_OK;
 }
 
@@ -63,8 +65,10 @@ Dims dims_of(const cq_config* c) {
   d.mode = c->quant_mode;
   d.etn_type = c->expert_token_nums_type;
   d.mask_ndim = c->mask_ndim;
+  d.x_dtype = c->x_dtype;
   const int32_t blocks = (d.H + 31) / 32;
   d.SC = (blocks + 1) / 2 * 2;
+  d.G3 = (d.H + 127) / 128;
   d.R_max = (int64_t)d.W * d.BS * d.NS;
   return d;
 }
@@ -108,10 +112,12 @@ int permute_impl(const cq_config* cfg, const void* x, const int32_t* expert_ids,
   if (rc != CQ_OK) return rc;
   const Dims d = dims_of(cfg);
   if (!x || !expert_ids || !expand_x || !assist_info) return CQ_ERR_ARG;
-  if (d.mode != 0 && !dynamic_scales) return CQ_ERR_ARG;
-  if (smooth && d.mode != 2) return CQ_ERR_ARG;  // mx modes take no smooth scales
-  if (!aligned(x, 16) || !aligned(expand_x, 16) || (smooth && !aligned(smooth, 16)) ||
-      !aligned(assist_info, 16))
+  if (d.mode >= 2 && !dynamic_scales) return CQ_ERR_ARG;
+  // [LLD] quant_mode 相关约束: mx modes take no scales; static quantisation needs them.
+  if (smooth && (d.mode == 0 || d.mode == 4 || d.mode == 5)) return CQ_ERR_ARG;
+  if (!smooth && d.mode == 1) return CQ_ERR_ARG;
+  if (!aligned(x, 16) || !aligned(expand_x, 16) ||
+      (smooth && cfg->smooth_kind != 2 && !aligned(smooth, 16)) || !aligned(assist_info, 16))
     return CQ_ERR_ARG;
   if ((rc = check_ws(d, workspace, workspace_bytes)) != CQ_OK) return rc;
   cq::PermuteArgs a;
@@ -121,13 +127,15 @@ int permute_impl(const cq_config* cfg, const void* x, const int32_t* expert_ids,
   a.mask = d.mask_ndim ? mask : nullptr;
   a.bs_per_rank = bs_per_rank;
   a.smooth = smooth;
+  a.smooth_kind = cfg->smooth_kind;
   a.expert_scales = expert_scales;
   a.expand_x = expand_x;
   a.dynamic_scales = dynamic_scales;
   a.assist_rows = assist_info + cq::assist_rows_off(d);
   a.inv = assist_info + cq::assist_inv_off(d);
   a.expand_scales = expand_scales;
-  a.scale_rows_bulk = d.SC % 16 == 0 && aligned(dynamic_scales, 16);
+  const int scale_row_bytes = d.mode == 3 ? 4 * d.G3 : d.SC;
+  a.scale_rows_bulk = scale_row_bytes % 16 == 0 && aligned(dynamic_scales, 16);
   a.ws = cq::carve(workspace, d);
   return cq::launch_permute(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? CQ_OK
                                                                                    : CQ_ERR_CUDA;
@@ -205,8 +213,10 @@ int cq_dispatch(const cq_config* cfg, const void* x, const int32_t* expert_ids,
   // Check the permute half's arguments too before enqueueing the route half.
   int rc = validate(cfg);
   if (rc != CQ_OK) return rc;
-  if (!x || !expand_x || (cfg->quant_mode != 0 && !dynamic_scales)) return CQ_ERR_ARG;
-  if (smooth_scales && cfg->quant_mode != 2) return CQ_ERR_ARG;
+  const int m = cfg->quant_mode;
+  if (!x || !expand_x || (m >= 2 && !dynamic_scales)) return CQ_ERR_ARG;
+  if (smooth_scales && (m == 0 || m == 4 || m == 5)) return CQ_ERR_ARG;
+  if (!smooth_scales && m == 1) return CQ_ERR_ARG;
   rc = route_impl(cfg, expert_ids, x_active_mask, bs_per_rank, assist_info, ep_recv_count,
                   expert_token_nums, workspace, workspace_bytes, stream);
   if (rc != CQ_OK) return rc;
@@ -337,7 +347,7 @@ const char* cq_strerror(int code) {
   switch (code) {
     case CQ_OK: return "ok";
     case CQ_ERR_ARG: return "invalid argument (range, divisibility, null or misaligned pointer)";
-    case CQ_ERR_UNSUPPORTED: return "unsupported configuration (quant_mode 1/3/4, or hidden size)";
+    case CQ_ERR_UNSUPPORTED: return "unsupported hidden size (needs H % 16 == 0, H % 32 for mx modes)";
     case CQ_ERR_CUDA: return "CUDA launch or query failed";
     case CQ_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case CQ_ERR_TOO_LARGE: return "problem needs more scratch than the built-in no-alloc buffer";

@@ -1,19 +1,18 @@
-// cq_combine.cu -- inverse permute + top-K weighted sum.
+// cq_combine.cu -- inverse permute + top-K weighted sum, and the combine-side
+// int8 quantisation of the expert outputs.
 //
 // One CTA per (token, 1024-element chunk). The slot table of the token (row
 // of each expert output, or a zero / copy / const code) is read into shared
 // memory; every thread then owns one 8-element unit of the chunk, gathers the
-// expert rows with 128-bit loads (a batch of 8 routed slots issued before the
-// first multiply, so 8 loads are in flight per thread), and sums
-// in binary32: one fused multiply-add per routed slot in slot order, then the
-// shared-expert rows added unweighted, then one rounding to the output type.
-// This is the weighted sum of "MoeDistributeDispatch和MoeDistributeCombine
-// 算子设计介绍" §3.4.2 and of the combine steps of "CANN MoE Dispatch/Combine
-// 通信算子性能优化实践" (multiply by expert scale, sum in float, add the shared
-// expert output, cast back), with the special experts of "low_latency_dispatch"
-// 特殊专家场景.
-#include <cuda_bf16.h>
-
+// expert rows with vector loads (a batch of 8 routed slots issued before the
+// first multiply), and sums in binary32: one fused multiply-add per routed
+// slot in slot order, then the shared-expert rows added unweighted, then one
+// rounding to the output type. This is the weighted sum of
+// "MoeDistributeDispatch和MoeDistributeCombine算子设计介绍" §3.4.2 and of the
+// combine steps of "CANN MoE Dispatch/Combine 通信算子性能优化实践" (multiply by
+// expert scale, sum in float, add the shared expert output, cast back), with
+// the special experts of "low_latency_dispatch" 特殊专家场景. Token, expert
+// output and result rows are bf16 or fp16 (the T template parameter).
 #include "cq_internal.cuh"
 
 namespace cq {
@@ -30,57 +29,6 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
   return v;
 }
 
-__device__ __forceinline__ void st_v4(void* p, uint4 v) {
-  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
-               "r"(v.w)
-               : "memory");
-}
-
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-__device__ __forceinline__ void fma8(float (&acc)[8], float w, const uint4& v) {
-  const uint32_t* p = reinterpret_cast<const uint32_t*>(&v);
-#pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    acc[2 * t] = __fmaf_rn(w, bf_lo(p[t]), acc[2 * t]);
-    acc[2 * t + 1] = __fmaf_rn(w, bf_hi(p[t]), acc[2 * t + 1]);
-  }
-}
-
-// const expert: acc += w * (a1 * x + a2 * v), each product and the sum rounded.
-__device__ __forceinline__ void fma8_const(float (&acc)[8], float w, float a1, float a2,
-                                           const uint4& x, const uint4& v) {
-  const uint32_t* px = reinterpret_cast<const uint32_t*>(&x);
-  const uint32_t* pv = reinterpret_cast<const uint32_t*>(&v);
-#pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    const float t0 = __fadd_rn(__fmul_rn(a1, bf_lo(px[t])), __fmul_rn(a2, bf_lo(pv[t])));
-    const float t1 = __fadd_rn(__fmul_rn(a1, bf_hi(px[t])), __fmul_rn(a2, bf_hi(pv[t])));
-    acc[2 * t] = __fmaf_rn(w, t0, acc[2 * t]);
-    acc[2 * t + 1] = __fmaf_rn(w, t1, acc[2 * t + 1]);
-  }
-}
-
-template <bool OUT_F32>
-__device__ __forceinline__ void store8(void* y, int64_t elem, const float (&acc)[8]) {
-  if (OUT_F32) {
-    float* p = static_cast<float*>(y) + elem;
-    st_v4(p, make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]),
-                        __float_as_uint(acc[2]), __float_as_uint(acc[3])));
-    st_v4(p + 4, make_uint4(__float_as_uint(acc[4]), __float_as_uint(acc[5]),
-                            __float_as_uint(acc[6]), __float_as_uint(acc[7])));
-  } else {
-    uint32_t o[4];
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * t], acc[2 * t + 1]);
-      o[t] = *reinterpret_cast<const uint32_t*>(&b);
-    }
-    st_v4(static_cast<uint16_t*>(y) + elem, make_uint4(o[0], o[1], o[2], o[3]));
-  }
-}
-
 __device__ __forceinline__ uint2 ld_nc_v2(const void* p) {
   uint2 v;
   asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
@@ -93,6 +41,23 @@ __device__ __forceinline__ float ld_nc_f32(const float* p) {
   return v;
 }
 
+__device__ __forceinline__ void st_v4(void* p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// 8 fp32 values of an 8-element unit of 16-bit values.
+template <class T>
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+  const uint32_t* p = reinterpret_cast<const uint32_t*>(&v);
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    f[2 * t] = T::lo(p[t]);
+    f[2 * t + 1] = T::hi(p[t]);
+  }
+}
+
 __device__ __forceinline__ void fma8f(float (&acc)[8], float w, const float (&v)[8]) {
 #pragma unroll
   for (int t = 0; t < 8; ++t) acc[t] = __fmaf_rn(w, v[t], acc[t]);
@@ -103,8 +68,36 @@ __device__ __forceinline__ void add8f(float (&acc)[8], const float (&v)[8]) {
   for (int t = 0; t < 8; ++t) acc[t] = __fadd_rn(acc[t], v[t]);
 }
 
-// Expert-output rows as bf16: 8 values per 16-byte load.
-struct SrcBf16 {
+// const expert: acc += w * (a1 * x + a2 * v), each product and the sum rounded.
+template <class T>
+__device__ __forceinline__ void fma8_const(float (&acc)[8], float w, float a1, float a2,
+                                           const uint4& x, const uint4& v) {
+  float fx[8], fv[8];
+  unpack8<T>(x, fx);
+  unpack8<T>(v, fv);
+#pragma unroll
+  for (int t = 0; t < 8; ++t)
+    acc[t] = __fmaf_rn(w, __fadd_rn(__fmul_rn(a1, fx[t]), __fmul_rn(a2, fv[t])), acc[t]);
+}
+
+template <class T, bool OUT_F32>
+__device__ __forceinline__ void store8(void* y, int64_t elem, const float (&acc)[8]) {
+  if (OUT_F32) {
+    float* p = static_cast<float*>(y) + elem;
+    st_v4(p, make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]),
+                        __float_as_uint(acc[2]), __float_as_uint(acc[3])));
+    st_v4(p + 4, make_uint4(__float_as_uint(acc[4]), __float_as_uint(acc[5]),
+                            __float_as_uint(acc[6]), __float_as_uint(acc[7])));
+  } else {
+    st_v4(static_cast<uint16_t*>(y) + elem,
+          make_uint4(T::pack2(acc[0], acc[1]), T::pack2(acc[2], acc[3]),
+                     T::pack2(acc[4], acc[5]), T::pack2(acc[6], acc[7])));
+  }
+}
+
+// Expert-output rows as 16-bit values: 8 per 16-byte load.
+template <class T>
+struct Src16 {
   const uint16_t* ffn;
   struct Item {
     uint4 v;
@@ -112,14 +105,7 @@ struct SrcBf16 {
   __device__ Item load(int64_t row, int H, int u) const {
     return {ld_nc_v4(ffn + row * H + 8 * (int64_t)u)};
   }
-  __device__ void floats(const Item& it, float (&f)[8]) const {
-    const uint32_t* p = reinterpret_cast<const uint32_t*>(&it.v);
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      f[2 * t] = bf_lo(p[t]);
-      f[2 * t + 1] = bf_hi(p[t]);
-    }
-  }
+  __device__ void floats(const Item& it, float (&f)[8]) const { unpack8<T>(it.v, f); }
 };
 
 // Expert-output rows as int8 with one scale per 8 values ("CANN MoE
@@ -148,7 +134,7 @@ struct SrcQ8 {
 // One CTA per (token, chunk of kThreads 8-element units); one unit per thread.
 constexpr int kThreads = 128;
 
-template <bool OUT_F32, class Src>
+template <class T, bool OUT_F32, class Src>
 __global__ void __launch_bounds__(kThreads) combine_kernel(CombineArgs a, Src src, int nchunk) {
   __shared__ int s_code[kMaxSlots];
   __shared__ float s_w[kMaxSlots];
@@ -202,11 +188,13 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(CombineArgs a, Src sr
         src.floats(v[b], f);
         fma8f(acc, w, f);
       } else if (code == CQ_INV_COPY) {
-        fma8(acc, w, ld_nc_v4(xrow + col));  // Moe(ori_x) = ori_x
+        float f[8];
+        unpack8<T>(ld_nc_v4(xrow + col), f);  // Moe(ori_x) = ori_x
+        fma8f(acc, w, f);
       } else if (code <= CQ_INV_CONST_BASE) {
         const int c = CQ_INV_CONST_BASE - code;
-        fma8_const(acc, w, a.alpha1[c], a.alpha2[c], ld_nc_v4(xrow + col),
-                   ld_nc_v4(a.const_v + (int64_t)c * H + col));
+        fma8_const<T>(acc, w, a.alpha1[c], a.alpha2[c], ld_nc_v4(xrow + col),
+                      ld_nc_v4(a.const_v + (int64_t)c * H + col));
       }
       // CQ_INV_NONE: zero expert, masked pair or inactive token adds nothing.
     }
@@ -219,13 +207,14 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(CombineArgs a, Src sr
       add8f(acc, f);
     }
   }
-  store8<OUT_F32>(a.y, tok * H + col, acc);
+  store8<T, OUT_F32>(a.y, tok * H + col, acc);
 }
 
 // Combine-side int8 quantisation of the expert outputs before they are sent
 // back ("CANN MoE Dispatch/Combine 通信算子性能优化实践", Int8QuantProcess):
 // per block of 8 values, scale = max|v| * fl(1/127), code = RNE(v / scale).
 // One CTA per (row, chunk); rows past the dispatched total are skipped.
+template <class T>
 __global__ void __launch_bounds__(kThreads) combine_quant_kernel(CombineArgs a, int nchunk) {
   griddep_wait();  // the rows may come from the preceding kernel
   const Dims& d = a.d;
@@ -236,7 +225,7 @@ __global__ void __launch_bounds__(kThreads) combine_quant_kernel(CombineArgs a, 
   const int u = chunk * kThreads + threadIdx.x;
   if (u >= (H >> 3)) return;
   float f[8];
-  SrcBf16{a.ffn}.floats(SrcBf16{a.ffn}.load(row, H, u), f);
+  unpack8<T>(ld_nc_v4(a.ffn + row * H + 8 * (int64_t)u), f);
   float m = 0.f;
 #pragma unroll
   for (int t = 0; t < 8; ++t) m = fmaxf(m, fabsf(f[t]));
@@ -253,33 +242,36 @@ __global__ void __launch_bounds__(kThreads) combine_quant_kernel(CombineArgs a, 
   a.ffn_scales[row * (H >> 3) + u] = s;
 }
 
+template <class T, class Src>
+cudaError_t launch_combine_t(const CombineArgs& a, const Src& src, cudaStream_t s) {
+  const int units = a.d.H >> 3;
+  const int nchunk = (units + kThreads - 1) / kThreads;
+  const dim3 grid((unsigned)((int64_t)a.d.W * a.d.BS * nchunk));
+  if (a.out_f32)
+    return launch_pdl(combine_kernel<T, true, Src>, grid, dim3(kThreads), 0, s, a, src, nchunk);
+  return launch_pdl(combine_kernel<T, false, Src>, grid, dim3(kThreads), 0, s, a, src, nchunk);
+}
+
 }  // namespace
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) {
-  const int units = a.d.H >> 3;
-  const int nchunk = (units + kThreads - 1) / kThreads;
-  const dim3 grid((unsigned)((int64_t)a.d.W * a.d.BS * nchunk));
-  const SrcBf16 src{a.ffn};
-  if (a.out_f32)
-    return launch_pdl(combine_kernel<true, SrcBf16>, grid, dim3(kThreads), 0, s, a, src, nchunk);
-  return launch_pdl(combine_kernel<false, SrcBf16>, grid, dim3(kThreads), 0, s, a, src, nchunk);
+  if (a.d.x_dtype == 1) return launch_combine_t<F16>(a, Src16<F16>{a.ffn}, s);
+  return launch_combine_t<BF16>(a, Src16<BF16>{a.ffn}, s);
 }
 
 cudaError_t launch_combine_q8(const CombineArgs& a, cudaStream_t s) {
-  const int units = a.d.H >> 3;
-  const int nchunk = (units + kThreads - 1) / kThreads;
-  const dim3 grid((unsigned)((int64_t)a.d.W * a.d.BS * nchunk));
   const SrcQ8 src{a.ffn_q, a.ffn_scales};
-  if (a.out_f32)
-    return launch_pdl(combine_kernel<true, SrcQ8>, grid, dim3(kThreads), 0, s, a, src, nchunk);
-  return launch_pdl(combine_kernel<false, SrcQ8>, grid, dim3(kThreads), 0, s, a, src, nchunk);
+  if (a.d.x_dtype == 1) return launch_combine_t<F16>(a, src, s);
+  return launch_combine_t<BF16>(a, src, s);
 }
 
 cudaError_t launch_combine_quant(const CombineArgs& a, cudaStream_t s) {
   const int units = a.d.H >> 3;
   const int nchunk = (units + kThreads - 1) / kThreads;
   const dim3 grid((unsigned)(a.d.R_max * nchunk));
-  return launch_pdl(combine_quant_kernel, grid, dim3(kThreads), 0, s, a, nchunk);
+  if (a.d.x_dtype == 1)
+    return launch_pdl(combine_quant_kernel<F16>, grid, dim3(kThreads), 0, s, a, nchunk);
+  return launch_pdl(combine_quant_kernel<BF16>, grid, dim3(kThreads), 0, s, a, nchunk);
 }
 
 }  // namespace cq

@@ -1,6 +1,8 @@
 // cq_internal.cuh -- internal definitions shared by the libcq translation units.
 #pragma once
 
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -13,7 +15,9 @@ struct Dims {
   int32_t W, M, S_eff, S_r, R_rep;  // R_rep: replicas per shared expert (S_r / S)
   int32_t Z, C, Q, BS, K, H, L, NS, G;  // G = S_r + M global expert slots
   int32_t mode, etn_type, mask_ndim;
-  int32_t SC;                     // mx scale columns
+  int32_t x_dtype;                // 0 bf16, 1 fp16
+  int32_t SC;                     // mx scale columns: Align2(Ceil(H, 32))
+  int32_t G3;                     // mode-3 groups per row: Ceil(H, 128)
   int64_t R_max;
 };
 
@@ -92,13 +96,14 @@ struct PermuteArgs {
   const uint8_t* mask;          // only to skip prefetching rows of inactive tokens
   const int32_t* bs_per_rank;   // idem
   const float* smooth;
+  int32_t smooth_kind;          // 0 per-expert rows, 1 one row for all, 2 one scalar
   const float* expert_scales;
   void* expand_x;
   void* dynamic_scales;
   int32_t* assist_rows;  // [R_max][4]
   int32_t* inv;          // [W*BS*NS]
   float* expand_scales;
-  int32_t scale_rows_bulk;  // mode 5: scale rows are 16-byte sized and aligned (bulk stores)
+  int32_t scale_rows_bulk;  // modes 3-5: scale rows are 16-byte sized and aligned (bulk stores)
   Workspace ws;
 };
 
@@ -116,6 +121,31 @@ struct CombineArgs {
   const uint16_t* const_v;
   void* y;
   int32_t out_f32;
+};
+
+// The two 16-bit token types. In a packed 32-bit word element 2t is the low
+// half. Conversions to fp32 are exact; pack2 rounds to nearest even.
+struct BF16 {
+  static __device__ __forceinline__ float lo(uint32_t w) { return __uint_as_float(w << 16); }
+  static __device__ __forceinline__ float hi(uint32_t w) {
+    return __uint_as_float(w & 0xffff0000u);
+  }
+  static __device__ __forceinline__ uint32_t pack2(float a, float b) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&v);
+  }
+};
+struct F16 {
+  static __device__ __forceinline__ float lo(uint32_t w) {
+    return __half2float(__ushort_as_half((unsigned short)(w & 0xffffu)));
+  }
+  static __device__ __forceinline__ float hi(uint32_t w) {
+    return __half2float(__ushort_as_half((unsigned short)(w >> 16)));
+  }
+  static __device__ __forceinline__ uint32_t pack2(float a, float b) {
+    const __half2 v = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t*>(&v);
+  }
 };
 
 // Launch with programmatic stream serialisation: the kernel may start while

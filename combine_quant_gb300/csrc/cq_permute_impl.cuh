@@ -1,0 +1,488 @@
+// cq_permute_impl.cuh -- fused gather-quantise-scatter (MoePermute + pre-send
+// quantisation), templated on the 16-bit token type; instantiated for bf16
+// and fp16 by cq_permute_bf16.cu / cq_permute_f16.cu.
+//
+// One CTA per source token (r, i). Warp 0 turns each slot's arrival ordinal
+// into its global row (rank base + first row of the (expert slot, source)
+// block within the rank + ordinal: the address rule of "MoeDistributeDispatch
+// 和MoeDistributeCombine算子设计介绍" §3.4.2 with the source block folded into the
+// expert offset), writes the inverse map, the (src, token, slot) row record and
+// the carried weight. All threads load the token row once with 128-bit loads
+// (started before the routing kernels finish), quantise it in registers and
+// stage the code row in shared memory; one thread then writes it to every
+// routed row with bulk (TMA) stores.
+//
+// Quantisation ("low_latency_dispatch" 计算公式, [DV3] 功能说明 情形 1 / 情形 2):
+//   mode 0  the 16-bit row travels unchanged
+//   mode 1  static: int8 = RNE(x * scales)
+//   mode 2  per token: s = 127 / max|x*scales|, int8 = RNE(x*scales * s), carry 1/s
+//   mode 3  per 128-group: s = 448 / max|x*scales|, e4m3 = RNE(x*scales * s), carry 1/s
+//   mode 4  mx: per 32-block, e = floor(log2 max|x|) - 8, e4m3 of x / 2^e, e8m0 e+127
+//   mode 5  mx clip: per 32-block, e = ceil(log2(max(max|x|, 1e-4) / 448)), idem
+// "scales" (smooth) is one row per expert, one row for all, or one scalar.
+// Arithmetic is single IEEE binary32 operations (explicit _rn intrinsics, no
+// contraction), so codes and scales are reproducible bit for bit.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "cq_internal.cuh"
+
+namespace cq {
+namespace permute_detail {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kMaxSlots = 32;  // NS <= 16 + 4
+
+using BF16 = cq::BF16;
+using F16 = cq::F16;
+
+// Smooth-scale shapes ([LLD] quant_mode 相关约束).
+enum SmoothKind { kNoSmooth = 0, kRowPerSlot = 1, kSharedRow = 2, kScalar = 3 };
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void st_shared_v4(void* p, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(
+                   (uint32_t)__cvta_generic_to_shared(p)),
+               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// Bulk (TMA) stores of staged rows: shared memory -> global, issued by one
+// thread, completion tracked in bulk groups. Both addresses 16-byte aligned,
+// size a multiple of 16.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> bulk reads
+}
+__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+               "r"((uint32_t)__cvta_generic_to_shared(ssrc)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Round to nearest even, saturate to int8 (a NaN product gives 0).
+__device__ __forceinline__ uint32_t q8(float v) {
+  int c = __float2int_rn(v);
+  c = max(-128, min(127, c));
+  return (uint32_t)c & 0xffu;
+}
+
+// Two binary32 values to two e4m3 bytes (lo in the low byte), round to
+// nearest even, saturating to +-448.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Exact ceil(log2(q)) for a positive normal binary32 q.
+__device__ __forceinline__ int ceil_log2_bits(float q) {
+  const uint32_t b = __float_as_uint(q);
+  return (int)((b >> 23) & 0xffu) - 127 + ((b & 0x7fffffu) != 0u ? 1 : 0);
+}
+
+// Exact floor(log2(a)) for a positive finite binary32 a (also subnormal).
+__device__ __forceinline__ int floor_log2_bits(float a) {
+  const uint32_t b = __float_as_uint(a);
+  const int ex = (int)((b >> 23) & 0xffu);
+  if (ex != 0) return ex - 127;
+  const uint32_t m = b & 0x7fffffu;  // a = m * 2^-149
+  return (31 - __clz((int)m)) - 149;
+}
+
+// 2^k as a binary32, for k in [-126, 127].
+__device__ __forceinline__ float pow2(int k) { return __uint_as_float((uint32_t)(k + 127) << 23); }
+
+__device__ __forceinline__ float max16(const float (&v)[16]) {
+  float m = 0.f;
+#pragma unroll
+  for (int t = 0; t < 16; ++t) m = fmaxf(m, fabsf(v[t]));
+  return m;
+}
+
+__device__ __forceinline__ uint4 q8_16(const float (&v)[16], float s) {
+  uint32_t o[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t)
+    o[t] = q8(__fmul_rn(v[4 * t], s)) | (q8(__fmul_rn(v[4 * t + 1], s)) << 8) |
+           (q8(__fmul_rn(v[4 * t + 2], s)) << 16) | (q8(__fmul_rn(v[4 * t + 3], s)) << 24);
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ uint4 q8_16_direct(const float (&v)[16]) {
+  uint32_t o[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t)
+    o[t] = q8(v[4 * t]) | (q8(v[4 * t + 1]) << 8) | (q8(v[4 * t + 2]) << 16) |
+           (q8(v[4 * t + 3]) << 24);
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ uint4 e4m3_16(const float (&v)[16], float mult) {
+  uint32_t o[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t)
+    o[t] = e4m3x2(__fmul_rn(v[4 * t], mult), __fmul_rn(v[4 * t + 1], mult)) |
+           (e4m3x2(__fmul_rn(v[4 * t + 2], mult), __fmul_rn(v[4 * t + 3], mult)) << 16);
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Block-wide max of one float per thread; `buf` holds >= 32 floats and must
+// not be reused by another block_max until the next __syncthreads.
+__device__ __forceinline__ float block_max(float v, float* buf) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+  if ((threadIdx.x & 31) == 0) buf[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float m = 0.f;
+  const int nw = blockDim.x >> 5;
+  for (int w = 0; w < nw; ++w) m = fmaxf(m, buf[w]);
+  return m;
+}
+
+// Thread-owned part of the token row: two 16-element units (32 bytes each).
+struct Units {
+  uint4 v[2][2];
+  bool ok[2];
+};
+
+// fp32 values of one unit, times the smooth scales when given.
+template <class T, int SM>
+__device__ __forceinline__ void unit_values(const uint4 (&u)[2], const float* srow, float scalar,
+                                            int unit, float (&f)[16]) {
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(&u[0]);
+#pragma unroll
+  for (int t = 0; t < 8; ++t) {
+    f[2 * t] = T::lo(w[t]);
+    f[2 * t + 1] = T::hi(w[t]);
+  }
+  if (SM == kScalar) {
+#pragma unroll
+    for (int t = 0; t < 16; ++t) f[t] = __fmul_rn(f[t], scalar);
+  } else if (SM == kRowPerSlot || SM == kSharedRow) {
+    const float* sm = srow + 16 * unit;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const uint4 q = ld_nc_v4(sm + 4 * t);
+      f[4 * t] = __fmul_rn(f[4 * t], __uint_as_float(q.x));
+      f[4 * t + 1] = __fmul_rn(f[4 * t + 1], __uint_as_float(q.y));
+      f[4 * t + 2] = __fmul_rn(f[4 * t + 2], __uint_as_float(q.z));
+      f[4 * t + 3] = __fmul_rn(f[4 * t + 3], __uint_as_float(q.w));
+    }
+  }
+}
+
+// Quantise this thread's two units of one row into the staging buffer: codes
+// at 16 bytes per unit in `codes`, the per-group (mode 3, floats) or
+// per-block (modes 4/5, e8m0 bytes) scales in `scales`. Mode 2 returns the
+// row's carried scale. `red` is a block_max buffer (mode 2 only).
+template <int MODE>
+__device__ __forceinline__ float quantise(const float (&f)[2][16], const Units& U,
+                                          uint8_t* codes, uint8_t* scales, float* red) {
+  float carried = 0.f;
+  if (MODE == 1) {
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+      if (U.ok[q]) st_shared_v4(codes + 16 * (threadIdx.x + q * blockDim.x), q8_16_direct(f[q]));
+  } else if (MODE == 2) {
+    const float amax = block_max(fmaxf(max16(f[0]), max16(f[1])), red);
+    const float s = __fdiv_rn(127.f, amax);  // +inf for an all-zero row: codes 0, carried 0
+    carried = __fdiv_rn(1.f, s);
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+      if (U.ok[q]) st_shared_v4(codes + 16 * (threadIdx.x + q * blockDim.x), q8_16(f[q], s));
+  } else if (MODE == 3) {
+    // A 128-group is 8 units held by 8 consecutive lanes.
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      float m = max16(f[q]);
+      m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
+      m = fmaxf(m, __shfl_xor_sync(kFull, m, 2));
+      m = fmaxf(m, __shfl_xor_sync(kFull, m, 4));
+      const float s = __fdiv_rn(448.f, m);
+      const float mult = m == 0.f ? 0.f : s;  // an all-zero group: codes 0, scale 0
+      const int u = threadIdx.x + q * blockDim.x;
+      if (U.ok[q]) {
+        st_shared_v4(codes + 16 * u, e4m3_16(f[q], mult));
+        if ((u & 7) == 0) reinterpret_cast<float*>(scales)[u >> 3] = __fdiv_rn(1.f, s);
+      }
+    }
+  } else {
+    // mx: a 32-block is 2 units held by lanes 2m, 2m+1.
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      float m = max16(f[q]);
+      m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
+      int e;
+      if (MODE == 4) {
+        e = m == 0.f ? -127 : max(floor_log2_bits(m) - 8, -127);  // emax(e4m3) = 8
+      } else {
+        e = ceil_log2_bits(__fdiv_rn(fmaxf(m, 1e-4f), 448.f));
+      }
+      const int u = threadIdx.x + q * blockDim.x;
+      if (U.ok[q]) {
+        st_shared_v4(codes + 16 * u, e4m3_16(f[q], pow2(-e)));  // x / 2^e, exact scaling
+        if ((u & 1) == 0) scales[u >> 1] = (uint8_t)(e + 127);
+      }
+    }
+  }
+  return carried;
+}
+
+// T: token type; MODE: quant_mode; SM: SmoothKind.
+template <class T, int MODE, int SM>
+__global__ void __launch_bounds__(256) permute_kernel(PermuteArgs a) {
+  __shared__ int s_row[kMaxSlots];   // compact list of routed rows
+  __shared__ int s_srow[kMaxSlots];  // their smooth-table rows
+  __shared__ int s_nrows;
+  __shared__ float s_red[2][32];
+  extern __shared__ __align__(128) uint8_t s_stage[];  // staged code row(s) + scale row(s)
+
+  const Dims& d = a.d;
+  const int64_t tok = blockIdx.x;
+  const int r = (int)(tok / d.BS), i = (int)(tok - (int64_t)r * d.BS);
+  const int lane = threadIdx.x & 31;
+  const int H = d.H;
+  const int units = H >> 4;
+  const uint16_t* xrow = a.x + tok * H;
+
+  Units U;
+  auto load_row = [&]() {
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int u = threadIdx.x + q * blockDim.x;
+      U.ok[q] = u < units;
+      if (U.ok[q]) {
+        U.v[q][0] = ld_nc_v4(xrow + 16 * u);
+        U.v[q][1] = ld_nc_v4(xrow + 16 * u + 8);
+      } else {
+        U.v[q][0] = U.v[q][1] = make_uint4(0, 0, 0, 0);
+      }
+    }
+  };
+  // From the inputs alone, could this token be active? If so, start loading
+  // its row now: this kernel may be running while the routing kernels end.
+  bool prefetched = !a.bs_per_rank || i < a.bs_per_rank[r];
+  if (prefetched && a.mask) {
+    if (d.mask_ndim == 1) {
+      prefetched = a.mask[tok] != 0;
+    } else {
+      bool any = false;
+      for (int j = 0; j < d.K; ++j) any |= a.mask[tok * d.K + j] != 0;
+      prefetched = any;
+    }
+  }
+  if (prefetched) load_row();
+  griddep_wait();  // routing outputs (ordinals, offsets) are read from here on
+
+  if (threadIdx.x < 32) {
+    const int k = lane;
+    int row = -1, srow = 0;
+    if (k < d.NS) {
+      const int e = a.ws.eidx[tok * d.NS + k];
+      int code = e;
+      if (e >= 0) {
+        int g, dst;  // global expert slot, destination rank
+        if (k < d.K) {
+          const int id = a.expert_ids[tok * d.K + k];
+          g = d.S_r + id;
+          dst = d.S_r + id / d.L;
+          srow = d.S_eff + id;
+        } else {
+          const int s = k - d.K;
+          g = dst = s * d.R_rep + r % d.R_rep;  // a shared-expert rank hosts one slot
+          srow = s;
+        }
+        row = a.ws.rank_base[dst] + a.ws.local_off[(int64_t)g * d.W + r] + e;
+        if (row < 0 || (int64_t)row >= d.R_max) {  // consistency guard: never write outside
+          atomicOr(a.ws.status, (uint32_t)CQ_ST_INTERNAL);
+          row = -1;
+          code = CQ_INV_NONE;
+        } else {
+          code = row;
+          reinterpret_cast<int4*>(a.assist_rows)[row] = make_int4(r, i, k, 0);
+          if (a.expand_scales)
+            a.expand_scales[row] =
+                k < d.K ? (a.expert_scales ? a.expert_scales[tok * d.K + k] : 0.f) : 1.f;
+        }
+      }
+      a.inv[tok * d.NS + k] = code;
+    }
+    const unsigned bal = __ballot_sync(kFull, row >= 0);
+    if (row >= 0) {
+      const int pos = __popc(bal & ((1u << lane) - 1u));
+      s_row[pos] = row;
+      s_srow[pos] = srow;
+    }
+    if (lane == 0) s_nrows = __popc(bal);
+  }
+  __syncthreads();
+  const int nrows = s_nrows;
+  if (nrows == 0) return;
+  if (!prefetched) load_row();  // routing found rows the inputs did not predict
+
+  // Staged row layout: code row (2H bytes in mode 0, else H), then the scale
+  // row padded to 16 bytes; two such buffers when each slot is quantised alone.
+  const int code_bytes = MODE == 0 ? 2 * H : H;
+  const int scale_bytes = MODE == 3 ? 4 * d.G3 : ((MODE == 4 || MODE == 5) ? d.SC : 0);
+  const int stride = code_bytes + ((scale_bytes + 15) & ~15);
+  char* const dyn = static_cast<char*>(a.dynamic_scales);
+  char* const out = static_cast<char*>(a.expand_x);
+
+  if (MODE == 0) {
+    // The 16-bit row itself travels ([DV3] 情形 1): stage it once.
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int u = threadIdx.x + q * blockDim.x;
+      if (U.ok[q]) {
+        st_shared_v4(s_stage + 32 * u, U.v[q][0]);
+        st_shared_v4(s_stage + 32 * u + 16, U.v[q][1]);
+      }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int n = 0; n < nrows; ++n)
+        bulk_store(out + (int64_t)s_row[n] * code_bytes, s_stage, (uint32_t)code_bytes);
+      bulk_commit();
+      bulk_wait_read<0>();
+    }
+  } else if (SM == kRowPerSlot) {
+    // x * smooth[expert]: one quantisation per routed row. Two staging
+    // buffers: row n is built while row n-1's bulk store still reads.
+    for (int n = 0; n < nrows; ++n) {
+      // Thread 0 waited (below) for the store that last read this buffer
+      // (row n-2); the barrier makes every thread see that.
+      if (n > 0) __syncthreads();
+      const float* sm = a.smooth + (int64_t)s_srow[n] * H;
+      float f[2][16];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int u = threadIdx.x + q * blockDim.x;
+        if (U.ok[q]) {
+          unit_values<T, SM>(U.v[q], sm, 0.f, u, f[q]);
+        } else {
+#pragma unroll
+          for (int t = 0; t < 16; ++t) f[q][t] = 0.f;
+        }
+      }
+      uint8_t* buf = s_stage + (n & 1) * stride;
+      const float carried = quantise<MODE>(f, U, buf, buf + code_bytes, s_red[n & 1]);
+      fence_proxy_async_smem();
+      __syncthreads();
+      const int64_t row = s_row[n];
+      if (threadIdx.x == 0) {
+        bulk_store(out + row * code_bytes, buf, (uint32_t)code_bytes);
+        if (scale_bytes && a.scale_rows_bulk)
+          bulk_store(dyn + row * scale_bytes, buf + code_bytes, (uint32_t)scale_bytes);
+        bulk_commit();
+        bulk_wait_read<1>();
+        if (MODE == 2) reinterpret_cast<float*>(dyn)[row] = carried;
+      }
+      if (scale_bytes && !a.scale_rows_bulk)
+        for (int b = threadIdx.x; b < scale_bytes; b += blockDim.x)
+          dyn[row * scale_bytes + b] = buf[code_bytes + b];
+    }
+    if (threadIdx.x == 0) bulk_wait_read<0>();
+  } else {
+    // One quantisation per token: every routed row gets the same codes.
+    const float* srow = SM == kSharedRow ? a.smooth : nullptr;
+    const float scalar = SM == kScalar ? a.smooth[0] : 0.f;
+    float f[2][16];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int u = threadIdx.x + q * blockDim.x;
+      if (U.ok[q]) {
+        unit_values<T, SM>(U.v[q], srow, scalar, u, f[q]);
+      } else {
+#pragma unroll
+        for (int t = 0; t < 16; ++t) f[q][t] = 0.f;
+      }
+    }
+    const float carried = quantise<MODE>(f, U, s_stage, s_stage + code_bytes, s_red[0]);
+    if (MODE == 5 || MODE == 4) {
+      if (threadIdx.x == 0 && d.SC > (units >> 1)) s_stage[code_bytes + (units >> 1)] = 0;
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int n = 0; n < nrows; ++n) {
+        const int64_t row = s_row[n];
+        bulk_store(out + row * code_bytes, s_stage, (uint32_t)code_bytes);
+        if (scale_bytes && a.scale_rows_bulk)
+          bulk_store(dyn + row * scale_bytes, s_stage + code_bytes, (uint32_t)scale_bytes);
+      }
+      bulk_commit();
+      bulk_wait_read<0>();
+    }
+    if (MODE == 2 && threadIdx.x < nrows)
+      reinterpret_cast<float*>(dyn)[s_row[threadIdx.x]] = carried;
+    if (scale_bytes && !a.scale_rows_bulk) {  // scale rows not 16-byte sized / aligned
+      for (int n = 0; n < nrows; ++n)
+        for (int b = threadIdx.x; b < scale_bytes; b += blockDim.x)
+          dyn[(int64_t)s_row[n] * scale_bytes + b] = s_stage[code_bytes + b];
+    }
+  }
+  // This CTA's stores are issued: the combine kernel may start launching.
+  griddep_launch_dependents();
+}
+
+template <class T, int MODE, int SM>
+cudaError_t launch_one(const PermuteArgs& a, cudaStream_t s) {
+  const int units = a.d.H >> 4;
+  int threads = ((units + 1) / 2 + 31) / 32 * 32;
+  if (threads < 32) threads = 32;
+  const int64_t grid = (int64_t)a.d.W * a.d.BS;
+  const size_t code_bytes = MODE == 0 ? 2 * (size_t)a.d.H : (size_t)a.d.H;
+  const size_t scale_bytes =
+      MODE == 3 ? 4 * (size_t)a.d.G3 : ((MODE == 4 || MODE == 5) ? (size_t)a.d.SC : 0);
+  const size_t smem = (code_bytes + ((scale_bytes + 15) & ~size_t(15))) * (SM == kRowPerSlot ? 2 : 1);
+  return launch_pdl(permute_kernel<T, MODE, SM>, dim3((unsigned)grid), dim3(threads), smem, s, a);
+}
+
+// Choose the instantiation for the call's mode and smooth shape.
+template <class T>
+cudaError_t launch_typed(const PermuteArgs& a, cudaStream_t s) {
+  int sm = kNoSmooth;
+  if (a.smooth) sm = a.smooth_kind == 0 ? kRowPerSlot : (a.smooth_kind == 1 ? kSharedRow : kScalar);
+  switch (a.d.mode) {
+    case 0: return launch_one<T, 0, kNoSmooth>(a, s);
+    case 1:
+      if (sm == kRowPerSlot) return launch_one<T, 1, kRowPerSlot>(a, s);
+      if (sm == kSharedRow) return launch_one<T, 1, kSharedRow>(a, s);
+      if (sm == kScalar) return launch_one<T, 1, kScalar>(a, s);
+      return cudaErrorInvalidValue;  // static quantisation needs scales
+    case 2:
+      if (sm == kRowPerSlot) return launch_one<T, 2, kRowPerSlot>(a, s);
+      if (sm == kSharedRow) return launch_one<T, 2, kSharedRow>(a, s);
+      if (sm == kScalar) return launch_one<T, 2, kScalar>(a, s);
+      return launch_one<T, 2, kNoSmooth>(a, s);
+    case 3:
+      if (sm == kRowPerSlot) return launch_one<T, 3, kRowPerSlot>(a, s);
+      if (sm == kSharedRow) return launch_one<T, 3, kSharedRow>(a, s);
+      if (sm == kScalar) return launch_one<T, 3, kScalar>(a, s);
+      return launch_one<T, 3, kNoSmooth>(a, s);
+    case 4: return launch_one<T, 4, kNoSmooth>(a, s);
+    case 5: return launch_one<T, 5, kNoSmooth>(a, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace permute_detail
+}  // namespace cq

@@ -30,7 +30,7 @@ import torch
 CONFIG_FIELDS = (
     "ep_world_size", "moe_expert_num", "shared_expert_num", "shared_expert_rank_num",
     "zero_expert_num", "copy_expert_num", "const_expert_num", "max_bs", "topk", "hidden",
-    "global_bs", "quant_mode", "expert_token_nums_type", "mask_ndim",
+    "global_bs", "quant_mode", "expert_token_nums_type", "mask_ndim", "x_dtype", "smooth_kind",
 )
 
 
@@ -81,6 +81,20 @@ class Workload:
 def to_bf16_bits(a: np.ndarray) -> np.ndarray:
     t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16)
     return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def to_f16_bits(a: np.ndarray) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def as_fp16(wl: "Workload") -> "Workload":
+    """The same workload with fp16 tokens: x and const_v re-rounded from
+    their bf16 values to fp16 (round to nearest even), x_dtype = 1."""
+    cfg = dict(wl.cfg, x_dtype=1)
+    f16 = lambda b: None if b is None else to_f16_bits(bf16_bits_to_f32(b))  # noqa: E731
+    return Workload(wl.name + "_f16", cfg, f16(wl.x), wl.expert_ids, wl.expert_scales,
+                    wl.smooth, wl.mask, wl.bs_per_rank, wl.const_alpha1, wl.const_alpha2,
+                    f16(wl.const_v), wl.seed, dict(wl.notes))
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
@@ -204,13 +218,16 @@ WORKLOADS = {"tiny": tiny, "dsv3": dsv3, "mxfp8": mxfp8, "special": special, "sk
              "perf8": lambda: perf_table(8), "perf256": lambda: perf_table(256)}
 
 
-def ffn_standin(seed: int, rows: int, H: int, chunk: int = 1 << 24) -> np.ndarray:
-    """Stand-in for the experts' FFN output, bf16 bits [rows, H]: values
-    N(0,1) rounded to bf16. Drawn in chunks to bound host memory spikes."""
+def ffn_standin(seed: int, rows: int, H: int, chunk: int = 1 << 24,
+                x_dtype: int = 0) -> np.ndarray:
+    """Stand-in for the experts' FFN output, 16-bit bits [rows, H] (bf16, or
+    fp16 when x_dtype == 1): values N(0,1) rounded to nearest even. Drawn in
+    chunks to bound host memory spikes."""
     rng = np.random.Generator(np.random.PCG64(1000 + seed))
+    conv = to_f16_bits if x_dtype == 1 else to_bf16_bits
     out = np.empty((rows, H), np.uint16)
     flat = out.reshape(-1)
     for s in range(0, flat.size, chunk):
         n = min(chunk, flat.size - s)
-        flat[s:s + n] = to_bf16_bits(rng.standard_normal(n, dtype=np.float32))
+        flat[s:s + n] = conv(rng.standard_normal(n, dtype=np.float32))
     return out

@@ -57,15 +57,20 @@ typedef struct cq_config {
   int32_t hidden;                 /* H in [1024, 8192]; this build needs H % 16 == 0
                                      (H % 32 == 0 for quant_mode 5) */
   int32_t global_bs;              /* 0 or BS * W ([DV3] global_bs) */
-  int32_t quant_mode;             /* 0 none, 2 per-token int8, 5 mx-clip e4m3 */
+  int32_t quant_mode;             /* 0 none, 1 static int8, 2 per-token int8, 3 per-128-group
+                                     e4m3, 4 mx e4m3, 5 mx-clip e4m3 ([LLD] 计算公式) */
   int32_t expert_token_nums_type; /* 0 cumulative sums, 1 counts */
   int32_t mask_ndim;              /* 0 none, 1 per token [W,BS], 2 per pair [W,BS,K] */
+  int32_t x_dtype;                /* 0 bf16, 1 fp16: x, ori_x, const_v, expert outputs, y */
+  int32_t smooth_kind;            /* shape of smooth_scales ("scales"): 0 one row per expert
+                                     [(S_r>0 ? S : 0) + M, H], 1 one row [H] for every
+                                     expert, 2 one scalar [1] */
 } cq_config;
 
 enum {
   CQ_OK = 0,
   CQ_ERR_ARG = -1,         /* a range or divisibility rule broken, or a required pointer NULL */
-  CQ_ERR_UNSUPPORTED = -2, /* quant_mode 1/3/4, or H not a multiple of 16 (32 for mode 5) */
+  CQ_ERR_UNSUPPORTED = -2, /* H not a multiple of 16 (32 for quant_mode 4 and 5) */
   CQ_ERR_CUDA = -3,        /* a CUDA launch or query failed */
   CQ_ERR_WORKSPACE = -4,   /* workspace smaller than cq_workspace_size() or misaligned */
   CQ_ERR_TOO_LARGE = -5    /* cq_dispatch_noalloc: the problem needs more scratch than
@@ -109,19 +114,24 @@ int cq_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
  * Inputs:
  *   x              bf16 [W, BS, H]  tokens of every logical rank
  *   expert_ids     int32 [W, BS, K] routed expert ids (MoE, zero, copy, const ranges)
- *   smooth_scales  f32 [(S_r>0 ? S : 0) + M, H] or NULL; mode 2 only. Shared
- *                  expert s uses row s, MoE expert e row (S_r>0 ? S : 0) + e.
+ *   smooth_scales  the "scales" of [LLD]: required in mode 1, optional in
+ *                  modes 2 and 3, NULL in modes 0, 4, 5. Shape by
+ *                  smooth_kind: 0 f32 [(S_r>0 ? S : 0) + M, H] (shared expert s
+ *                  uses row s, MoE expert e row (S_r>0 ? S : 0) + e), 1 f32 [H]
+ *                  for every expert, 2 f32 [1].
  *   x_active_mask  uint8 [W, BS] (mask_ndim 1) or [W, BS, K] (2), or NULL
  *   bs_per_rank    int32 [W] tokens of each rank (<= BS), or NULL for all BS
  *   expert_scales  f32 [W, BS, K] routing weights, or NULL (expand_scales
  *                  then unused)
  * Outputs (rows past the true total are left untouched):
- *   expand_x       [R_max, H]: bf16 (mode 0), int8 (mode 2), e4m3 bytes (mode 5).
- *                  Rank d's rows, expert-contiguous (local expert ascending,
- *                  then source rank ascending, then arrival order).
- *   dynamic_scales f32 [R_max] dequantisation multipliers (mode 2), or
- *                  uint8 e8m0 [R_max, SC] block scales 2^e stored as e+127
- *                  (mode 5, pad column 0); ignored in mode 0 (may be NULL).
+ *   expand_x       [R_max, H]: the token type (mode 0), int8 (modes 1, 2),
+ *                  e4m3 bytes (modes 3, 4, 5). Rank d's rows, expert-contiguous
+ *                  (local expert ascending, then source rank ascending, then
+ *                  arrival order).
+ *   dynamic_scales dequantisation multipliers: f32 [R_max] (mode 2), f32
+ *                  [R_max, Ceil(H,128)] one per 128-group (mode 3), uint8 e8m0
+ *                  [R_max, SC] block scales 2^e stored as e+127 (modes 4, 5,
+ *                  pad column 0); not used in modes 0 and 1 (may be NULL).
  *   assist_info    int32 [cq_assist_info_size()]: pass unchanged to cq_combine.
  *                  Layout: [R_max][4] rows (src_rank, src_token, slot, 0);
  *                  then inv [W, BS, NS] (row of each slot or a CQ_INV_* code);

@@ -36,7 +36,7 @@ INV_CONST_BASE = -3
 _FIELDS = (
     "ep_world_size", "moe_expert_num", "shared_expert_num", "shared_expert_rank_num",
     "zero_expert_num", "copy_expert_num", "const_expert_num", "max_bs", "topk", "hidden",
-    "global_bs", "quant_mode", "expert_token_nums_type", "mask_ndim",
+    "global_bs", "quant_mode", "expert_token_nums_type", "mask_ndim", "x_dtype", "smooth_kind",
 )
 
 
@@ -79,6 +79,16 @@ def lib() -> ctypes.CDLL:
         L.cqo_route.restype = ctypes.c_int64
         L.cqo_quant_row.argtypes = [ctypes.c_int32, ctypes.c_int32, P, P, P, P]
         L.cqo_quant_row.restype = ctypes.c_int
+        L.cqo_quant_row2.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P, P, P, P, P]
+        L.cqo_quant_row2.restype = ctypes.c_int
+        L.cqo_group_cols.argtypes = [cfgp]
+        L.cqo_group_cols.restype = ctypes.c_int32
+        L.cqo_f16_to_f32.argtypes = [ctypes.c_uint16]
+        L.cqo_f16_to_f32.restype = ctypes.c_float
+        L.cqo_f16_from_f32.argtypes = [ctypes.c_float]
+        L.cqo_f16_from_f32.restype = ctypes.c_uint16
+        L.cqo_floor_log2.argtypes = [ctypes.c_float]
+        L.cqo_floor_log2.restype = ctypes.c_int32
         L.cqo_dispatch.argtypes = [cfgp] + [P] * 16
         L.cqo_dispatch.restype = ctypes.c_int64
         L.cqo_combine_token.argtypes = [cfgp, ctypes.c_int32, ctypes.c_int32] + [P] * 7 + [
@@ -99,7 +109,7 @@ def lib() -> ctypes.CDLL:
         for name in ("cqo_e4m3_encode_n", "cqo_bf16_from_f32_n", "cqo_ceil_log2_n"):
             getattr(L, name).argtypes = [P, P, ctypes.c_int64]
             getattr(L, name).restype = None
-        L.cqo_combine_quant_row.argtypes = [ctypes.c_int32, P, P, P]
+        L.cqo_combine_quant_row.argtypes = [ctypes.c_int32, ctypes.c_int32, P, P, P]
         L.cqo_combine_quant_row.restype = ctypes.c_int
         L.cqo_combine_token_q8.argtypes = [cfgp, ctypes.c_int32, ctypes.c_int32] + [P] * 8 + [
             ctypes.c_int32, P]
@@ -186,28 +196,39 @@ def route(cfg: dict, expert_ids, mask=None, bs_per_rank=None) -> Route:
     return Route(rows=int(rows), status=int(st.value), **b)
 
 
-def quant_row(mode: int, x_row_bits, smooth_row=None):
-    """Quantise one bf16 row (uint16 bit patterns). Returns (codes, scale)."""
+def _scale_buffer(mode: int, H: int):
+    if mode == 2:
+        return np.empty(1, np.float32)
+    if mode == 3:
+        return np.empty((H + 127) // 128, np.float32)
+    if mode in (4, 5):
+        return np.empty(((H + 31) // 32 + 1) // 2 * 2, np.uint8)
+    return None
+
+
+def quant_row(mode: int, x_row_bits, smooth_row=None, x_dtype: int = 0, smooth_scalar=None):
+    """Quantise one 16-bit row (uint16 bit patterns of bf16, or fp16 when
+    x_dtype == 1). Returns (codes, scale): scale is a float (mode 2), a
+    per-group float row (mode 3), an e8m0 byte row (modes 4, 5) or None."""
     x = _c(x_row_bits, np.uint16)
     H = x.shape[0]
     sm = _c(smooth_row, np.float32)
-    if mode == 0:
-        codes, scale = np.empty(H, np.uint16), None
-    elif mode == 2:
-        codes, scale = np.empty(H, np.int8), np.empty(1, np.float32)
-    elif mode == 5:
-        blocks = (H + 31) // 32
-        codes, scale = np.empty(H, np.uint8), np.empty((blocks + 1) // 2 * 2, np.uint8)
-    else:
-        raise ValueError(mode)
-    rc = lib().cqo_quant_row(mode, H, _ptr(x), _ptr(sm), _ptr(codes), _ptr(scale))
+    sc = None if smooth_scalar is None else np.asarray([smooth_scalar], np.float32)
+    codes = np.empty(H, code_dtype(mode))
+    scale = _scale_buffer(mode, H)
+    rc = lib().cqo_quant_row2(mode, x_dtype, H, _ptr(x), _ptr(sm), _ptr(sc), _ptr(codes),
+                              _ptr(scale))
     if rc != OK:
         raise ValueError(f"oracle quant_row failed: {rc}")
     return codes, (None if scale is None else (scale[0] if mode == 2 else scale))
 
 
 def code_dtype(mode: int):
-    return {0: np.uint16, 2: np.int8, 5: np.uint8}[mode]
+    return {0: np.uint16, 1: np.int8, 2: np.int8, 3: np.uint8, 4: np.uint8, 5: np.uint8}[mode]
+
+
+def group_cols(cfg: dict) -> int:
+    return lib().cqo_group_cols(ctypes.byref(_cfg(cfg)))
 
 
 def dispatch(cfg: dict, x_bits, expert_ids, smooth=None, mask=None, bs_per_rank=None,
@@ -222,7 +243,9 @@ def dispatch(cfg: dict, x_bits, expert_ids, smooth=None, mask=None, bs_per_rank=
     expand_x = np.zeros((R, H), code_dtype(mode))
     if mode == 2:
         dyn = np.zeros((R,), np.float32)
-    elif mode == 5:
+    elif mode == 3:
+        dyn = np.zeros((R, group_cols(cfg)), np.float32)
+    elif mode in (4, 5):
         dyn = np.zeros((R, scale_cols(cfg)), np.uint8)
     else:
         dyn = None
@@ -296,6 +319,18 @@ def ceil_log2(q: float) -> int:
     return int(lib().cqo_ceil_log2(float(q)))
 
 
+def floor_log2(a: float) -> int:
+    return int(lib().cqo_floor_log2(float(a)))
+
+
+def f16_from_f32(f: float) -> int:
+    return int(lib().cqo_f16_from_f32(float(f)))
+
+
+def f16_to_f32(h: int) -> float:
+    return float(lib().cqo_f16_to_f32(int(h)))
+
+
 def e4m3_encode_array(v) -> np.ndarray:
     a = _c(v, np.float32).reshape(-1)
     out = np.empty(a.shape, np.uint8)
@@ -317,23 +352,23 @@ def ceil_log2_array(v) -> np.ndarray:
     return out
 
 
-def combine_quant_row(row_bits):
-    """Combine-side int8 block quantisation of one bf16 row: (codes, scales)."""
+def combine_quant_row(row_bits, x_dtype: int = 0):
+    """Combine-side int8 block quantisation of one 16-bit row: (codes, scales)."""
     x = _c(row_bits, np.uint16)
     H = x.shape[0]
     codes, scales = np.empty(H, np.int8), np.empty(H // 8, np.float32)
-    rc = lib().cqo_combine_quant_row(H, _ptr(x), _ptr(codes), _ptr(scales))
+    rc = lib().cqo_combine_quant_row(H, x_dtype, _ptr(x), _ptr(codes), _ptr(scales))
     if rc != OK:
         raise ValueError(f"oracle combine_quant_row failed: {rc}")
     return codes, scales
 
 
-def combine_quant_rows(rows_bits):
+def combine_quant_rows(rows_bits, x_dtype: int = 0):
     rows = _c(rows_bits, np.uint16)
     codes = np.empty(rows.shape, np.int8)
     scales = np.empty((rows.shape[0], rows.shape[1] // 8), np.float32)
     for n in range(rows.shape[0]):
-        codes[n], scales[n] = combine_quant_row(rows[n])
+        codes[n], scales[n] = combine_quant_row(rows[n], x_dtype)
     return codes, scales
 
 

@@ -74,10 +74,10 @@ int cqo_check_config(const cqo_config* c) {
   if (c->global_bs != 0 && c->global_bs != c->max_bs * W) return CQO_ERR_ARG;
   if (c->expert_token_nums_type != 0 && c->expert_token_nums_type != 1) return CQO_ERR_ARG;
   if (c->mask_ndim < 0 || c->mask_ndim > 2) return CQO_ERR_ARG;
-  /* Argument errors outrank "not implemented": modes 1, 3, 4 are defined by
-   * [LLD] but not built here. */
-  if (c->quant_mode == 1 || c->quant_mode == 3 || c->quant_mode == 4) return CQO_ERR_UNSUPPORTED;
-  if (c->quant_mode != 0 && c->quant_mode != 2 && c->quant_mode != 5) return CQO_ERR_ARG;
+  /* [LLD] quant_mode 0..5; x as float16 or bfloat16 ([DV3] 参数说明 x). */
+  if (c->quant_mode < 0 || c->quant_mode > 5) return CQO_ERR_ARG;
+  if (c->x_dtype != 0 && c->x_dtype != 1) return CQO_ERR_ARG;
+  if (c->smooth_kind < 0 || c->smooth_kind > 2) return CQO_ERR_ARG;
   return CQO_OK;
 }
 
@@ -101,6 +101,52 @@ uint16_t cqo_bf16_from_f32(float f) {
   uint32_t keep_lsb = (u >> 16) & 1u;
   u += 0x7fffu + keep_lsb;
   return (uint16_t)(u >> 16);
+}
+
+float cqo_f16_to_f32(uint16_t h) {
+  /* IEEE binary16: 1 sign, 5 exponent bits (bias 15), 10 mantissa bits. */
+  const int sign = h >> 15, e = (h >> 10) & 0x1f, m = h & 0x3ff;
+  float mag;
+  if (e == 0) mag = ldexpf((float)m, -24);
+  else if (e == 31) mag = m ? NAN : INFINITY;
+  else mag = ldexpf(1.0f + (float)m / 1024.0f, e - 15);
+  return sign ? -mag : mag;
+}
+
+uint16_t cqo_f16_from_f32(float f) {
+  /* Round to nearest even; magnitudes from 65520 up overflow to infinity. */
+  if (isnan(f)) return 0x7e00;
+  const uint16_t sign = signbit(f) ? 0x8000 : 0;
+  const float a = fabsf(f);
+  if (a >= 65520.0f) return sign | 0x7c00;
+  if (a < 0x1p-14f) {
+    /* subnormal: value = m * 2^-24, m = 0..1023; m = 1024 is the smallest normal */
+    return sign | (uint16_t)rintf(a * 0x1p24f);
+  }
+  int e;
+  frexpf(a, &e);
+  int ex = e - 1; /* -14 .. 15 */
+  const float t = ldexpf(a, -ex);
+  float mq = rintf((t - 1.0f) * 1024.0f);
+  if (mq == 1024.0f) {
+    mq = 0.0f;
+    ex += 1;
+  }
+  if (ex > 15) return sign | 0x7c00;
+  return sign | (uint16_t)(((ex + 15) << 10) | (int)mq);
+}
+
+int32_t cqo_floor_log2(float a) {
+  /* a = m * 2^e with m in [0.5, 1)  =>  floor(log2(a)) = e - 1 (exact, also
+   * for subnormal a). */
+  int e;
+  frexpf(a, &e);
+  return e - 1;
+}
+
+int32_t cqo_group_cols(const cqo_config* c) {
+  /* [LLD] quant_mode 相关约束: pergroup scales have shape (A, Ceil(H, 128)). */
+  return (c->hidden + 127) / 128;
 }
 
 int32_t cqo_ceil_log2(float q) {
@@ -173,42 +219,75 @@ static int8_t sat_rne_int8(float v) {
 /* Quantisation of one row, [LLD] 计算公式 and [DV3] 功能说明 情形 1 / 情形 2. */
 /* ------------------------------------------------------------------------ */
 
-int cqo_quant_row(int32_t mode, int32_t H, const uint16_t* x, const float* smooth, void* codes,
-                  void* scale) {
+static float in16(int32_t dtype, uint16_t v) {
+  return dtype ? cqo_f16_to_f32(v) : cqo_bf16_to_f32(v);
+}
+
+static uint16_t out16(int32_t dtype, float f) {
+  return dtype ? cqo_f16_from_f32(f) : cqo_bf16_from_f32(f);
+}
+
+int cqo_quant_row2(int32_t mode, int32_t dt, int32_t H, const uint16_t* x, const float* smooth,
+                   const float* smooth_scalar, void* codes, void* scale) {
   if (mode == 0) {
-    /* quant_out = x: the bf16 row travels unchanged. */
+    /* quant_out = x: the 16-bit row travels unchanged. */
     memcpy(codes, x, (size_t)H * sizeof(uint16_t));
     return CQO_OK;
   }
-  if (mode == 2) {
-    /* x_fp32 = CastToFp32(x) * smooth (when given);
-     * dynamic_scales_value = 127 / max|x_fp32|;
+  /* [LLD] quant_mode 相关约束: mx modes take no smooth scales; static
+   * quantisation (mode 1) needs them. */
+  const int has_smooth = smooth != NULL || smooth_scalar != NULL;
+  if ((mode == 4 || mode == 5) && has_smooth) return CQO_ERR_ARG;
+  if (mode == 1 && !has_smooth) return CQO_ERR_ARG;
+  if (mode < 1 || mode > 5) return CQO_ERR_UNSUPPORTED;
+  /* x_fp32 = CastToFp32(x) * scales (when given). */
+  float* xf = (float*)malloc((size_t)H * sizeof(float));
+  if (!xf) return CQO_ERR_NOMEM;
+  for (int32_t h = 0; h < H; ++h) {
+    const float v = in16(dt, x[h]);
+    xf[h] = smooth_scalar ? v * *smooth_scalar : (smooth ? v * smooth[h] : v);
+  }
+  if (mode == 1) {
+    /* static: quant_out = Cast(CastToFp32(x) * scales, int8) */
+    int8_t* q = (int8_t*)codes;
+    for (int32_t h = 0; h < H; ++h) q[h] = sat_rne_int8(xf[h]);
+  } else if (mode == 2) {
+    /* dynamic_scales_value = 127 / max|x_fp32|;
      * quant_out = Cast(x_fp32 * dynamic_scales_value, int8);
      * carried scale = 1.0 / dynamic_scales_value. */
-    float* xf = (float*)malloc((size_t)H * sizeof(float));
-    if (!xf) return CQO_ERR_NOMEM;
-    for (int32_t h = 0; h < H; ++h) {
-      float v = cqo_bf16_to_f32(x[h]);
-      xf[h] = smooth ? v * smooth[h] : v;
-    }
     float amax = 0.0f;
     for (int32_t h = 0; h < H; ++h) {
-      float a = fabsf(xf[h]);
+      const float a = fabsf(xf[h]);
       if (a > amax) amax = a;
     }
-    float s = 127.0f / amax; /* +inf for an all-zero row */
+    const float s = 127.0f / amax; /* +inf for an all-zero row */
     int8_t* q = (int8_t*)codes;
     for (int32_t h = 0; h < H; ++h) q[h] = sat_rne_int8(xf[h] * s);
     *(float*)scale = 1.0f / s;
-    free(xf);
-    return CQO_OK;
-  }
-  if (mode == 5) {
-    /* mx clip quantisation, per block of 32 elements:
-     * max_abs_clamp = max(max|x|, 1e-4);
-     * shared_exp = ceil(log2(max_abs_clamp / 448));
-     * quant_out = CastToFp8E4M3(x / 2^shared_exp);
-     * the block scale 2^shared_exp is stored as e8m0 (shared_exp + 127). */
+  } else if (mode == 3) {
+    /* pergroup: the mode-2 formulas on each group of 128 values, into
+     * e4m3 (dst_type_max 448); one carried scale per group. An all-zero
+     * group gives codes 0 and scale 0. */
+    uint8_t* q = (uint8_t*)codes;
+    float* sc = (float*)scale;
+    for (int32_t g = 0; g * 128 < H; ++g) {
+      const int32_t h0 = g * 128, h1 = (h0 + 128 < H) ? h0 + 128 : H;
+      float amax = 0.0f;
+      for (int32_t h = h0; h < h1; ++h) {
+        const float a = fabsf(xf[h]);
+        if (a > amax) amax = a;
+      }
+      const float s = 448.0f / amax;
+      const float mult = amax == 0.0f ? 0.0f : s;
+      for (int32_t h = h0; h < h1; ++h) q[h] = cqo_e4m3_encode(xf[h] * mult);
+      sc[g] = 1.0f / s;
+    }
+  } else {
+    /* mode 4 (mx): shared_exp = floor(log2(max|x|)) - emax, emax = 8 for
+     *   e4m3 (448 = 1.75 * 2^8); an all-zero block uses the smallest scale;
+     * mode 5 (mx clip): shared_exp = ceil(log2(max(max|x|, 1e-4) / 448)).
+     * Both: quant_out = CastToFp8E4M3(x / 2^shared_exp), the block scale
+     * 2^shared_exp stored as e8m0 (shared_exp + 127), blocks of 32. */
     uint8_t* q = (uint8_t*)codes;
     uint8_t* sc = (uint8_t*)scale;
     const int32_t nblk = (H + 31) / 32;
@@ -217,22 +296,32 @@ int cqo_quant_row(int32_t mode, int32_t H, const uint16_t* x, const float* smoot
       const int32_t h0 = b * 32, h1 = (h0 + 32 < H) ? h0 + 32 : H;
       float amax = 0.0f;
       for (int32_t h = h0; h < h1; ++h) {
-        float a = fabsf(cqo_bf16_to_f32(x[h]));
+        const float a = fabsf(xf[h]);
         if (a > amax) amax = a;
       }
-      if (amax < 1e-4f) amax = 1e-4f;
-      int32_t e = cqo_ceil_log2(amax / 448.0f);
+      int32_t e;
+      if (mode == 4) {
+        e = amax == 0.0f ? -127 : cqo_floor_log2(amax) - 8;
+        if (e < -127) e = -127;
+      } else {
+        if (amax < 1e-4f) amax = 1e-4f;
+        e = cqo_ceil_log2(amax / 448.0f);
+      }
       for (int32_t h = h0; h < h1; ++h) {
         /* x / 2^e; 2^-e is a normal binary32 here, so ldexpf is exact. */
-        float v = ldexpf(cqo_bf16_to_f32(x[h]), -e);
-        q[h] = cqo_e4m3_encode(v);
+        q[h] = cqo_e4m3_encode(ldexpf(xf[h], -e));
       }
       sc[b] = (uint8_t)(e + 127);
     }
     for (int32_t b = nblk; b < cols; ++b) sc[b] = 0; /* Align2 padding column */
-    return CQO_OK;
   }
-  return CQO_ERR_UNSUPPORTED;
+  free(xf);
+  return CQO_OK;
+}
+
+int cqo_quant_row(int32_t mode, int32_t H, const uint16_t* x, const float* smooth, void* codes,
+                  void* scale) {
+  return cqo_quant_row2(mode, 0, H, x, smooth, NULL, codes, scale);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -394,38 +483,52 @@ int64_t cqo_dispatch(const cqo_config* c, const uint16_t* x, const int32_t* expe
                      float* expand_scales, int32_t* expand_idx, int32_t* ep_recv_count,
                      int64_t* expert_token_nums, int64_t* rank_row_base, int32_t* assist,
                      int32_t* inv, uint32_t* status) {
-  if (c->quant_mode == 5 && smooth) return CQO_ERR_ARG; /* [LLD]: mx modes take no smooth scales */
+  /* [LLD] quant_mode 相关约束: mx modes take no smooth scales; static
+   * quantisation (mode 1) needs them. */
+  if ((c->quant_mode == 4 || c->quant_mode == 5) && smooth) return CQO_ERR_ARG;
+  if (c->quant_mode == 1 && !smooth) return CQO_ERR_ARG;
   int64_t rows = cqo_route(c, expert_ids, mask, bs_per_rank, expand_idx, ep_recv_count,
                            expert_token_nums, rank_row_base, assist, inv, status);
   if (rows < 0) return rows;
   const int32_t H = c->hidden, K = c->topk, BS = c->max_bs;
   const int32_t Seff = (c->shared_expert_rank_num > 0) ? c->shared_expert_num : 0;
-  const int32_t cols = cqo_scale_cols(c);
+  const int32_t cols = cqo_scale_cols(c), gcols = cqo_group_cols(c);
   for (int64_t row = 0; row < rows; ++row) {
     const int32_t src = assist[row * 4 + 0], i = assist[row * 4 + 1], k = assist[row * 4 + 2];
     const int64_t tok = (int64_t)src * BS + i;
     const uint16_t* xr = x + tok * H;
-    /* [LLD] quant_mode 相关约束: the smooth table is (S + M, H) when shared
-     * experts exist, else (M, H); shared expert s uses row s, MoE expert e
-     * uses row S + e. */
+    /* [LLD] quant_mode 相关约束: scales are one scalar (1,), one row (H,)
+     * shared by every expert, or per expert: (S + M, H) when shared experts
+     * exist, else (M, H); shared expert s uses row s, MoE expert e row S + e. */
     const float* sm = NULL;
+    const float* sm_scalar = NULL;
     if (smooth) {
-      int64_t srow = (k < K) ? (int64_t)Seff + expert_ids[tok * K + k] : (int64_t)(k - K);
-      sm = smooth + srow * H;
+      if (c->smooth_kind == 2) {
+        sm_scalar = smooth;
+      } else if (c->smooth_kind == 1) {
+        sm = smooth;
+      } else {
+        int64_t srow = (k < K) ? (int64_t)Seff + expert_ids[tok * K + k] : (int64_t)(k - K);
+        sm = smooth + srow * H;
+      }
     }
     void* codes;
-    void* scale;
+    void* scale = NULL;
     if (c->quant_mode == 0) {
       codes = (uint16_t*)expand_x + row * H;
-      scale = NULL;
+    } else if (c->quant_mode == 1) {
+      codes = (int8_t*)expand_x + row * H;
     } else if (c->quant_mode == 2) {
       codes = (int8_t*)expand_x + row * H;
       scale = (float*)dynamic_scales + row;
+    } else if (c->quant_mode == 3) {
+      codes = (uint8_t*)expand_x + row * H;
+      scale = (float*)dynamic_scales + row * gcols;
     } else {
       codes = (uint8_t*)expand_x + row * H;
       scale = (uint8_t*)dynamic_scales + row * cols;
     }
-    int rc = cqo_quant_row(c->quant_mode, H, xr, sm, codes, scale);
+    int rc = cqo_quant_row2(c->quant_mode, c->x_dtype, H, xr, sm, sm_scalar, codes, scale);
     if (rc != CQO_OK) return rc;
     /* [DV3] expand_scales: the routing weight travels with its row; a shared
      * expert row carries weight 1 (its output is added unweighted). */
@@ -458,14 +561,14 @@ int cqo_combine_token(const cqo_config* c, int32_t r, int32_t i, const uint16_t*
       const float w = expert_scales[tok * K + j];
       float v;
       if (code >= 0) {
-        v = cqo_bf16_to_f32(ffn[(int64_t)code * H + h]);
+        v = in16(c->x_dtype, ffn[(int64_t)code * H + h]);
       } else if (code == CQO_INV_COPY) {
-        v = cqo_bf16_to_f32(ori_x[tok * H + h]); /* Moe(ori_x) = ori_x */
+        v = in16(c->x_dtype, ori_x[tok * H + h]); /* Moe(ori_x) = ori_x */
       } else if (code <= CQO_INV_CONST_BASE) {
         /* Moe(ori_x) = alpha1 * ori_x + alpha2 * v: two rounded products, one rounded sum. */
         const int32_t q = CQO_INV_CONST_BASE - code;
-        const float p1 = const_alpha1[q] * cqo_bf16_to_f32(ori_x[tok * H + h]);
-        const float p2 = const_alpha2[q] * cqo_bf16_to_f32(const_v[(int64_t)q * H + h]);
+        const float p1 = const_alpha1[q] * in16(c->x_dtype, ori_x[tok * H + h]);
+        const float p2 = const_alpha2[q] * in16(c->x_dtype, const_v[(int64_t)q * H + h]);
         v = p1 + p2;
       } else {
         continue; /* zero expert, masked pair, invalid id: Moe(ori_x) = 0 */
@@ -475,10 +578,10 @@ int cqo_combine_token(const cqo_config* c, int32_t r, int32_t i, const uint16_t*
     /* Shared experts, added unweighted after the routed ones. */
     for (int32_t s = 0; s < Seff; ++s) {
       const int32_t code = slots[K + s];
-      if (code >= 0) acc = acc + cqo_bf16_to_f32(ffn[(int64_t)code * H + h]);
+      if (code >= 0) acc = acc + in16(c->x_dtype, ffn[(int64_t)code * H + h]);
     }
     if (out_f32) ((float*)y_row)[h] = acc;
-    else ((uint16_t*)y_row)[h] = cqo_bf16_from_f32(acc);
+    else ((uint16_t*)y_row)[h] = out16(c->x_dtype, acc);
   }
   return CQO_OK;
 }
@@ -507,19 +610,20 @@ int cqo_combine(const cqo_config* c, const uint16_t* ffn, const int32_t* inv,
 /* the scale and cast to int8; the receiver multiplies back by the scale.     */
 /* ------------------------------------------------------------------------ */
 
-int cqo_combine_quant_row(int32_t H, const uint16_t* row, int8_t* codes, float* scales) {
+int cqo_combine_quant_row(int32_t H, int32_t dt, const uint16_t* row, int8_t* codes,
+                          float* scales) {
   if (H % 8 != 0) return CQO_ERR_ARG;
   const float inv_param = 1.0f / 127.0f; /* the constant 1/SCALE_PARAM, rounded once */
   for (int32_t b = 0; b < H / 8; ++b) {
     float m = 0.0f;
     for (int32_t t = 0; t < 8; ++t) {
-      float a = fabsf(cqo_bf16_to_f32(row[b * 8 + t]));
+      float a = fabsf(in16(dt, row[b * 8 + t]));
       if (a > m) m = a;
     }
     const float scale = m * inv_param; /* Muls(1/SCALE_PARAM) */
     for (int32_t t = 0; t < 8; ++t) {
       /* Div, then one round-to-nearest-even cast (0/0 = NaN gives 0) */
-      codes[b * 8 + t] = sat_rne_int8(cqo_bf16_to_f32(row[b * 8 + t]) / scale);
+      codes[b * 8 + t] = sat_rne_int8(in16(dt, row[b * 8 + t]) / scale);
     }
     scales[b] = scale;
   }
@@ -547,11 +651,11 @@ int cqo_combine_token_q8(const cqo_config* c, int32_t r, int32_t i, const int8_t
         /* received row: dequantise first (int8 value times its block scale) */
         v = (float)ffn_codes[(int64_t)code * H + h] * ffn_scales[(int64_t)code * (H / 8) + h / 8];
       } else if (code == CQO_INV_COPY) {
-        v = cqo_bf16_to_f32(ori_x[tok * H + h]);
+        v = in16(c->x_dtype, ori_x[tok * H + h]);
       } else if (code <= CQO_INV_CONST_BASE) {
         const int32_t q = CQO_INV_CONST_BASE - code;
-        const float p1 = const_alpha1[q] * cqo_bf16_to_f32(ori_x[tok * H + h]);
-        const float p2 = const_alpha2[q] * cqo_bf16_to_f32(const_v[(int64_t)q * H + h]);
+        const float p1 = const_alpha1[q] * in16(c->x_dtype, ori_x[tok * H + h]);
+        const float p2 = const_alpha2[q] * in16(c->x_dtype, const_v[(int64_t)q * H + h]);
         v = p1 + p2;
       } else {
         continue;
@@ -565,7 +669,7 @@ int cqo_combine_token_q8(const cqo_config* c, int32_t r, int32_t i, const int8_t
                         ffn_scales[(int64_t)code * (H / 8) + h / 8];
     }
     if (out_f32) ((float*)y_row)[h] = acc;
-    else ((uint16_t*)y_row)[h] = cqo_bf16_from_f32(acc);
+    else ((uint16_t*)y_row)[h] = out16(c->x_dtype, acc);
   }
   return CQO_OK;
 }

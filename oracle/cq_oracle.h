@@ -15,7 +15,8 @@
  *           ACL SHMEM 实现专家分发与聚合"
  *
  * Array conventions (all host memory, row-major, caller-owned):
- *   x, ori_x, ffn rows and const_v are bf16 stored as raw uint16 bit patterns.
+ *   x, ori_x, ffn rows, const_v and 16-bit outputs are bf16 (x_dtype 0) or fp16
+ *   (x_dtype 1), stored as raw uint16 bit patterns.
  *   NS  = K + (shared_expert_rank_num > 0 ? shared_expert_num : 0) slots per token.
  *   R_max = W * BS * NS is the bound on dispatched rows over all logical ranks.
  */
@@ -40,9 +41,12 @@ typedef struct cqo_config {
   int32_t topk;                   /* K */
   int32_t hidden;                 /* H */
   int32_t global_bs;              /* 0 or BS * W */
-  int32_t quant_mode;             /* 0, 2 or 5 */
+  int32_t quant_mode;             /* 0 .. 5 */
   int32_t expert_token_nums_type; /* 0 = cumulative sum, 1 = counts */
   int32_t mask_ndim;              /* 0 = no mask, 1 = [W,BS], 2 = [W,BS,K] */
+  int32_t x_dtype;                /* 0 = bf16, 1 = fp16 (x, ori_x, const_v, ffn rows, y) */
+  int32_t smooth_kind;            /* scales shape: 0 = per expert rows [(S)+M, H],
+                                     1 = one row [H] for every expert, 2 = one scalar */
 } cqo_config;
 
 /* Return codes. */
@@ -80,16 +84,29 @@ int64_t cqo_route(const cqo_config* c, const int32_t* expert_ids, const uint8_t*
                   int64_t* expert_token_nums, int64_t* rank_row_base, int32_t* assist,
                   int32_t* inv, uint32_t* status);
 
-/* Quantise one row of H bf16 values.
- *   mode 0: codes = the H bf16 values (uint16), no scale.
+/* Quantise one row of H bf16 values (x_dtype 0) or fp16 values (x_dtype 1).
+ * smooth_row: H floats, or NULL; smooth_scalar: used instead when not NULL.
+ *   mode 0: codes = the H 16-bit values, no scale.
+ *   mode 1: codes = H int8 (static: x * smooth), no scale.
  *   mode 2: codes = H int8; scale = one float (the dequantisation multiplier).
- *   mode 5: codes = H e4m3 bytes; scale = Align2(Ceil(H,32)) e8m0 bytes. */
+ *   mode 3: codes = H e4m3; scale = Ceil(H,128) floats (per 128-group multipliers).
+ *   mode 4: codes = H e4m3; scale = Align2(Ceil(H,32)) e8m0 bytes (floor rule).
+ *   mode 5: codes = H e4m3; scale = Align2(Ceil(H,32)) e8m0 bytes (clip rule). */
+int cqo_quant_row2(int32_t mode, int32_t x_dtype, int32_t hidden, const uint16_t* x_row,
+                   const float* smooth_row, const float* smooth_scalar, void* codes,
+                   void* scale);
+/* bf16 input, per-element smooth row or none (the original entry point). */
 int cqo_quant_row(int32_t mode, int32_t hidden, const uint16_t* x_row, const float* smooth_row,
                   void* codes, void* scale);
+int32_t cqo_group_cols(const cqo_config* c); /* mode 3: Ceil(H, 128) */
+float cqo_f16_to_f32(uint16_t h);
+uint16_t cqo_f16_from_f32(float f); /* round to nearest even */
+int32_t cqo_floor_log2(float a);    /* exact floor(log2(a)) for finite a > 0 */
 
 /* Whole dispatch: routing plus quantisation of every placed row.
  * expand_x is [R_max, H] of the mode's code type; dynamic_scales is [R_max] float
- * (mode 2) or [R_max, scale_cols] bytes (mode 5) or unused (mode 0);
+ * (mode 2), [R_max, group_cols] float (mode 3), [R_max, scale_cols] bytes
+ * (modes 4, 5) or unused (modes 0, 1); smooth follows smooth_kind;
  * expand_scales (nullable) is [R_max] float. */
 int64_t cqo_dispatch(const cqo_config* c, const uint16_t* x, const int32_t* expert_ids,
                      const float* smooth, const uint8_t* mask, const int32_t* bs_per_rank,
@@ -98,8 +115,8 @@ int64_t cqo_dispatch(const cqo_config* c, const uint16_t* x, const int32_t* expe
                      int64_t* expert_token_nums, int64_t* rank_row_base, int32_t* assist,
                      int32_t* inv, uint32_t* status);
 
-/* Combine one token (r, i) into y_row (H values; bf16 bits if out_f32 == 0,
- * else float). ffn is [rows, H] bf16. */
+/* Combine one token (r, i) into y_row (H values; 16-bit bits of x_dtype if
+ * out_f32 == 0, else float). ffn is [rows, H] of x_dtype. */
 int cqo_combine_token(const cqo_config* c, int32_t r, int32_t i, const uint16_t* ffn,
                       const int32_t* inv, const float* expert_scales, const uint16_t* ori_x,
                       const float* const_alpha1, const float* const_alpha2,
@@ -113,7 +130,8 @@ int cqo_combine(const cqo_config* c, const uint16_t* ffn, const int32_t* inv,
 /* Combine-side int8 block quantisation of one expert-output row of H bf16
  * values: blocks of 8 elements, scale = max|v| * fl(1/127), codes =
  * RNE(v / scale) saturated to int8. codes [H], scales [H/8] (H % 8 == 0). */
-int cqo_combine_quant_row(int32_t hidden, const uint16_t* row, int8_t* codes, float* scales);
+int cqo_combine_quant_row(int32_t hidden, int32_t x_dtype, const uint16_t* row, int8_t* codes,
+                          float* scales);
 
 /* Combine one token from int8 expert outputs: each routed / shared row is
  * dequantised (code * block scale) before the weighted sum. ffn_codes is

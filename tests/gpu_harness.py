@@ -21,16 +21,20 @@ def dev(a, dtype):
 
 
 def host(t: torch.Tensor) -> np.ndarray:
-    if t.dtype == torch.bfloat16:
+    if t.dtype in (torch.bfloat16, torch.float16):
         return t.view(torch.int16).cpu().numpy().view(np.uint16)
     return t.cpu().numpy()
 
 
+def uses_smooth(wl) -> bool:
+    return wl.smooth is not None and wl.cfg["quant_mode"] in (1, 2, 3)
+
+
 def gpu_dispatch(wl: workloads.Workload):
     cfg = cq.Config.from_dict(wl.cfg)
-    x = dev(wl.x, torch.bfloat16)
+    x = dev(wl.x, cfg.token_dtype)
     ids = dev(wl.expert_ids, torch.int32)
-    sm = dev(wl.smooth, torch.float32) if wl.cfg["quant_mode"] == 2 else None
+    sm = dev(wl.smooth, torch.float32) if uses_smooth(wl) else None
     mask = dev(wl.mask, torch.uint8)
     bpr = dev(wl.bs_per_rank, torch.int32)
     w = dev(wl.expert_scales, torch.float32)
@@ -53,12 +57,18 @@ def compare_route(wl, cfg, out, ref_route):
     assert np.array_equal(host(rows[:R]), ref_route.assist[:R])
 
 
-def smooth_row(wl, src, tok, k):
-    if wl.smooth is None or wl.cfg["quant_mode"] != 2:
-        return None
+def smooth_args(wl, src, tok, k):
+    """(row, scalar) smooth arguments of oracle.quant_row for one routed row."""
+    if not uses_smooth(wl):
+        return None, None
+    kind = wl.cfg.get("smooth_kind", 0)
+    if kind == 2:
+        return None, float(wl.smooth.reshape(-1)[0])
+    if kind == 1:
+        return wl.smooth.reshape(-1), None
     K = wl.cfg["topk"]
     s_eff = wl.cfg["shared_expert_num"] if wl.cfg["shared_expert_rank_num"] > 0 else 0
-    return wl.smooth[s_eff + wl.expert_ids[src, tok, k]] if k < K else wl.smooth[k - K]
+    return (wl.smooth[s_eff + wl.expert_ids[src, tok, k]] if k < K else wl.smooth[k - K]), None
 
 
 def compare_rows(wl, out, ref_route, sample):
@@ -75,11 +85,15 @@ def compare_rows(wl, out, ref_route, sample):
     es = host(out.expand_scales.index_select(0, idx)) if out.expand_scales is not None else None
     for n, row in enumerate(sample):
         src, tok, k = ref_route.assist[row, :3]
-        codes, scale = oracle.quant_row(mode, wl.x[src, tok], smooth_row(wl, src, tok, k))
+        sm_row, sm_scalar = smooth_args(wl, src, tok, k)
+        codes, scale = oracle.quant_row(mode, wl.x[src, tok], sm_row, wl.cfg.get("x_dtype", 0),
+                                        sm_scalar)
         assert np.array_equal(ex[n].view(codes.dtype), codes), f"expand_x row {row}"
         if mode == 2:
             assert dyn[n] == scale, f"dynamic_scales row {row}"
-        elif mode == 5:
+        elif mode == 3:
+            assert np.array_equal(dyn[n].view(np.uint32), scale.view(np.uint32)), f"row {row}"
+        elif mode in (4, 5):
             assert np.array_equal(dyn[n], scale), f"mx scales row {row}"
         if es is not None:
             want = wl.expert_scales[src, tok, k] if k < K else np.float32(1.0)
@@ -105,10 +119,12 @@ class FfnStandin:
     leaves its arithmetic unchanged."""
 
     def __init__(self, wl, max_rows: int, pool_rows: int = 4096):
-        self.pool = workloads.ffn_standin(wl.seed, pool_rows, wl.cfg["hidden"])
+        xd = wl.cfg.get("x_dtype", 0)
+        self.pool = workloads.ffn_standin(wl.seed, pool_rows, wl.cfg["hidden"], x_dtype=xd)
         self.P = pool_rows
         idx = (torch.arange(max_rows, dtype=torch.int64, device=DEV) * 7919) % pool_rows
-        self.device_rows = dev(self.pool, torch.bfloat16).index_select(0, idx).contiguous()
+        tdt = torch.float16 if xd == 1 else torch.bfloat16
+        self.device_rows = dev(self.pool, tdt).index_select(0, idx).contiguous()
 
     def remap_inv(self, inv: np.ndarray) -> np.ndarray:
         inv = inv.astype(np.int64)
@@ -116,12 +132,13 @@ class FfnStandin:
 
 
 def gpu_combine(wl, cfg, out, ffn: FfnStandin, out_dtype):
+    """out_dtype: torch.float32 or None (the token type)."""
     w = dev(wl.expert_scales, torch.float32)
     return cq.combine(cfg, ffn.device_rows, out.assist_info, w, out.ep_recv_count,
-                      ori_x=dev(wl.x, torch.bfloat16),
+                      ori_x=dev(wl.x, cfg.token_dtype),
                       const_alpha1=dev(wl.const_alpha1, torch.float32),
                       const_alpha2=dev(wl.const_alpha2, torch.float32),
-                      const_v=dev(wl.const_v, torch.bfloat16), out_dtype=out_dtype)
+                      const_v=dev(wl.const_v, cfg.token_dtype), out_dtype=out_dtype)
 
 
 def oracle_combine_tokens(wl, ref_route, ffn: FfnStandin, tokens, out_f32):
@@ -130,8 +147,42 @@ def oracle_combine_tokens(wl, ref_route, ffn: FfnStandin, tokens, out_f32):
                                  wl.const_v, out_f32=out_f32)
 
 
+def full_parity(wl):
+    """Whole dispatch + combine on the GPU against the oracle, every element."""
+    cfg, out, status, _ = gpu_dispatch(wl)
+    ref = oracle.dispatch(wl.cfg, wl.x, wl.expert_ids, wl.smooth if uses_smooth(wl) else None,
+                          wl.mask, wl.bs_per_rank, wl.expert_scales)
+    assert status == ref["status"]
+    route = oracle.Route(ref["rows"], ref["expand_idx"], ref["ep_recv_count"],
+                         ref["expert_token_nums"], ref["rank_row_base"], ref["assist"],
+                         ref["inv"], ref["status"])
+    compare_route(wl, cfg, out, route)
+    R = ref["rows"]
+    if R:
+        got = host(out.expand_x[:R])
+        assert np.array_equal(got.view(ref["expand_x"].dtype), ref["expand_x"][:R])
+        if ref["dynamic_scales"] is not None:
+            g, r = host(out.dynamic_scales[:R]), ref["dynamic_scales"][:R]
+            assert np.array_equal(g.view(np.uint8), r.view(np.uint8))
+        assert np.array_equal(host(out.expand_scales[:R]), ref["expand_scales"][:R])
+    ffn = FfnStandin(wl, cfg.max_rows)
+    y32 = host(gpu_combine(wl, cfg, out, ffn, torch.float32))
+    y16 = host(gpu_combine(wl, cfg, out, ffn, None))
+    inv = ffn.remap_inv(route.inv)
+    args = (wl.cfg, ffn.pool, inv, wl.expert_scales, wl.x, wl.const_alpha1, wl.const_alpha2,
+            wl.const_v)
+    r32 = oracle.combine(*args, out_f32=True)
+    r16 = oracle.combine(*args, out_f32=False)
+    assert np.max(np.abs(y32 - r32)) <= 1e-5
+    assert np.max(bf16_ulp_diff(y16, r16)) <= 1
+    assert np.array_equal(y32.view(np.uint32), r32.view(np.uint32))
+    assert np.array_equal(y16, r16)
+    return cfg, out, ref
+
+
 def bf16_ulp_diff(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:
-    """Distance in units of bf16 ordering between two bf16 bit arrays."""
+    """Distance in units of last place between two arrays of 16-bit float
+    bit patterns (bf16 or fp16: both order like sign-magnitude integers)."""
     def key(b):
         b = b.astype(np.int32)
         return np.where(b & 0x8000, -(b & 0x7fff), b & 0x7fff)

@@ -57,7 +57,8 @@ def _random_cfg(rng):
         const_expert_num=int(rng.choice([0, 1])), max_bs=int(rng.choice([1, 128, 512, 513, 0])),
         topk=int(rng.choice([1, 8, 16, 17])), hidden=int(rng.choice([1024, 7168, 8192, 1000, 8320])),
         global_bs=int(rng.choice([0, 0, 5])), quant_mode=int(rng.choice([0, 1, 2, 3, 4, 5, 6])),
-        expert_token_nums_type=int(rng.choice([0, 1, 2])), mask_ndim=int(rng.choice([0, 1, 2, 3])))
+        expert_token_nums_type=int(rng.choice([0, 1, 2])), mask_ndim=int(rng.choice([0, 1, 2, 3])),
+        x_dtype=int(rng.choice([0, 1, 2])), smooth_kind=int(rng.choice([0, 1, 2, 3])))
 
 
 def test_validation_agrees_with_oracle(lib, oracle_lib):
@@ -69,7 +70,8 @@ def test_validation_agrees_with_oracle(lib, oracle_lib):
         cfg = _random_cfg(rng)
         want = oracle.check_config(cfg)
         got = lib.cq_check_config(_c(cfg))
-        if want == 0 and (cfg["hidden"] % 16 or (cfg["quant_mode"] == 5 and cfg["hidden"] % 32)):
+        if want == 0 and (cfg["hidden"] % 16 or (cfg["quant_mode"] in (4, 5)
+                                                  and cfg["hidden"] % 32)):
             want = _lib.CQ_ERR_UNSUPPORTED
         assert got == want, cfg
         n_ok += got == 0
@@ -113,8 +115,14 @@ def test_host_errors_before_any_device_work(lib):
     args = [fake] * 13
     bad = dict(cfg, topk=0)
     assert lib.cq_dispatch(_c(bad), *args, 1 << 20, None) == _lib.CQ_ERR_ARG
-    assert lib.cq_dispatch(_c(dict(cfg, quant_mode=3)), *args, 1 << 20, None) == \
-        _lib.CQ_ERR_UNSUPPORTED
+    assert lib.cq_dispatch(_c(dict(cfg, quant_mode=5, hidden=1040)), *args, 1 << 20, None) == \
+        _lib.CQ_ERR_UNSUPPORTED  # mx blocks need H % 32 == 0 in this build
+    assert lib.cq_dispatch(_c(dict(cfg, quant_mode=6)), *args, 1 << 20, None) == _lib.CQ_ERR_ARG
+    a_nos = list(args)
+    a_nos[2] = None  # static quantisation without scales
+    assert lib.cq_dispatch(_c(dict(cfg, quant_mode=1)), *a_nos, 1 << 20, None) == _lib.CQ_ERR_ARG
+    assert lib.cq_dispatch(_c(dict(cfg, x_dtype=2)), *args, 1 << 20, None) == _lib.CQ_ERR_ARG
+    assert lib.cq_dispatch(_c(dict(cfg, smooth_kind=3)), *args, 1 << 20, None) == _lib.CQ_ERR_ARG
     # workspace too small
     assert lib.cq_dispatch(_c(cfg), *args, 16, None) == _lib.CQ_ERR_WORKSPACE
     # x missing

@@ -1,0 +1,91 @@
+"""GPU parity for quant_mode 1, 3, 4, the three smooth-scale shapes and fp16
+tokens ("low_latency_dispatch" 计算公式 / quant_mode 相关约束), element by
+element against the oracle (codes and scales bit-exact; combine exact)."""
+import numpy as np
+import pytest
+
+import gpu_harness as gh
+from combine_quant_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+def _with(wl, mode, smooth=None, kind=0):
+    cfg = dict(wl.cfg, quant_mode=mode, smooth_kind=kind)
+    return workloads.Workload(wl.name + f"_m{mode}_k{kind}", cfg, wl.x, wl.expert_ids,
+                              wl.expert_scales, smooth, wl.mask, wl.bs_per_rank,
+                              wl.const_alpha1, wl.const_alpha2, wl.const_v, wl.seed)
+
+
+def _smooth(wl, kind, seed=0):
+    rng = np.random.default_rng(100 + seed)
+    H = wl.cfg["hidden"]
+    if kind == 2:
+        return np.array([rng.uniform(0.5, 4.0)], np.float32)
+    if kind == 1:
+        return rng.uniform(0.5, 1.5, H).astype(np.float32)
+    s_eff = wl.cfg["shared_expert_num"] if wl.cfg["shared_expert_rank_num"] > 0 else 0
+    return rng.uniform(0.5, 1.5, (s_eff + wl.cfg["moe_expert_num"], H)).astype(np.float32)
+
+
+def _base(name):
+    return {
+        "tiny": lambda: workloads.tiny(3, 2),
+        "dsv3_small": lambda: workloads.dsv3(seed=21, W=8, BS=37, M=64, K=8, H=2048),
+        "special_small": lambda: workloads.special(seed=23, W=8, BS=20, H=1024, M=48),
+        "h1040": lambda: workloads.dsv3(seed=25, W=4, BS=9, M=16, K=4, H=1040),
+    }[name]()
+
+
+@pytest.mark.parametrize("base", ["tiny", "special_small"])
+@pytest.mark.parametrize("kind", [0, 1, 2])
+def test_mode1_static(base, kind):
+    wl = _base(base)
+    gh.full_parity(_with(wl, 1, _smooth(wl, kind), kind))
+
+
+@pytest.mark.parametrize("base", ["tiny", "dsv3_small", "h1040"])
+@pytest.mark.parametrize("kind", [None, 0, 1, 2])
+def test_mode3_pergroup(base, kind):
+    wl = _base(base)
+    if kind is None:
+        gh.full_parity(_with(wl, 3))
+    else:
+        gh.full_parity(_with(wl, 3, _smooth(wl, kind), kind))
+
+
+@pytest.mark.parametrize("base", ["tiny", "dsv3_small", "special_small"])
+def test_mode4_mx(base):
+    gh.full_parity(_with(_base(base), 4))
+
+
+@pytest.mark.parametrize("kind", [1, 2])
+def test_mode2_broadcast_smooth(kind):
+    wl = _base("dsv3_small")
+    gh.full_parity(_with(wl, 2, _smooth(wl, kind), kind))
+
+
+def test_mode4_extremes():
+    wl = _with(workloads.tiny(4, 2), 4)
+    x = workloads.bf16_bits_to_f32(wl.x).copy()
+    x[0, 0] = 0.0            # zero blocks -> scale byte 0
+    x[0, 1, :64] = 448.0     # exactly 2^8 * 1.75 -> scale 2^0
+    x[1, 2] *= 1e-38         # subnormal blocks -> scale clamped to 2^-127
+    x[2, 3] *= 1e30
+    wl.x = workloads.to_bf16_bits(x)
+    gh.full_parity(wl)
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2, 3, 4, 5])
+def test_fp16_tokens(mode):
+    wl = workloads.as_fp16(_base("tiny"))
+    sm = _smooth(wl, 0) if mode in (1, 2, 3) else None
+    gh.full_parity(_with(wl, mode, sm, 0))
+
+
+def test_fp16_special_experts_and_masks():
+    gh.full_parity(workloads.as_fp16(_base("special_small")))
+
+
+def test_fp16_dsv3_small():
+    gh.full_parity(workloads.as_fp16(_base("dsv3_small")))

@@ -311,8 +311,14 @@ def test_config_rejections(oracle_lib, bad):
     assert oracle.check_config(cfg) != 0
 
 
-def test_config_unsupported_modes(oracle_lib):
+def test_config_modes_and_types(oracle_lib):
+    """quant_mode 0..5 ([LLD] 计算公式), x as bf16 / fp16, three scales shapes."""
     cfg = make_config(ep_world_size=16, moe_expert_num=64, max_bs=8, topk=4, hidden=1024)
-    for m in (1, 3, 4):
-        assert oracle.check_config(dict(cfg, quant_mode=m)) == oracle.ERR_UNSUPPORTED
-    assert oracle.check_config(cfg) == 0
+    for m in range(6):
+        assert oracle.check_config(dict(cfg, quant_mode=m)) == 0
+    assert oracle.check_config(dict(cfg, quant_mode=6)) == oracle.ERR_ARG
+    assert oracle.check_config(dict(cfg, x_dtype=1)) == 0
+    assert oracle.check_config(dict(cfg, x_dtype=2)) == oracle.ERR_ARG
+    for k in range(3):
+        assert oracle.check_config(dict(cfg, smooth_kind=k)) == 0
+    assert oracle.check_config(dict(cfg, smooth_kind=3)) == oracle.ERR_ARG
