@@ -172,10 +172,19 @@ def measured_peaks() -> tuple[float, str]:
         return 6800.0, "fallback"
 
 
+KERNEL_SOURCES = {
+    "permute": ["cq_permute_impl.cuh", "cq_permute_bf16.cu", "cq_internal.cuh"],
+    "combine": ["cq_combine.cu", "cq_internal.cuh"],
+}
+
+
 def source_sha(kernel: str) -> str:
-    path = os.path.join(ROOT, "combine_quant_gb300", "csrc", f"cq_{kernel}.cu")
-    with open(path, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
+    """SHA-256 over the source files that define the kernel."""
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "combine_quant_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 def ncu_traffic(kernel: str):
