@@ -27,6 +27,7 @@ NOALLOC_SCRATCH_BYTES = 4 << 20
 CQ_ST_BAD_ID = 1
 CQ_ST_BAD_MASK = 2
 CQ_ST_INTERNAL = 4
+CQ_ST_TIMEOUT = 8
 CQ_INV_NONE = -1
 CQ_INV_COPY = -2
 CQ_INV_CONST_BASE = -3

@@ -117,7 +117,9 @@ int permute_impl(const cq_config* cfg, const void* x, const int32_t* expert_ids,
   if (smooth && (d.mode == 0 || d.mode == 4 || d.mode == 5)) return CQ_ERR_ARG;
   if (!smooth && d.mode == 1) return CQ_ERR_ARG;
   if (!aligned(x, 16) || !aligned(expand_x, 16) ||
-      (smooth && cfg->smooth_kind != 2 && !aligned(smooth, 16)) || !aligned(assist_info, 16))
+      (smooth && cfg->smooth_kind != 2 && !aligned(smooth, 16)) || !aligned(assist_info, 16) ||
+      (smooth && !aligned(smooth, 4)) ||
+      ((d.mode == 2 || d.mode == 3) && !aligned(dynamic_scales, 4)))
     return CQ_ERR_ARG;
   if ((rc = check_ws(d, workspace, workspace_bytes)) != CQ_OK) return rc;
   cq::PermuteArgs a;

@@ -29,6 +29,8 @@ struct Dims {
 //   eidx      : int32 [W*BS*NS] arrival ordinal of each slot, or a CQ_INV code
 //   rank_tot  : int32 [W]     rows received by each destination rank
 //   rank_base : int32 [W+1]   first global row of each destination rank
+//   row_src   : int2 [R_max]  (source token index r*BS+i, smooth-table row) of
+//                             each dispatched row (per-expert smooth path only)
 struct Workspace {
   uint32_t* status;
   uint32_t* done;
@@ -38,6 +40,7 @@ struct Workspace {
   int32_t* eidx;
   int32_t* rank_tot;
   int32_t* rank_base;
+  int2* row_src;
 };
 
 constexpr size_t kHdrBytes = 256;
@@ -50,6 +53,7 @@ inline size_t workspace_bytes(const Dims& d) {
   b += align256(sizeof(int32_t) * (size_t)d.W * d.BS * d.NS);
   b += align256(sizeof(int32_t) * (size_t)d.W);
   b += align256(sizeof(int32_t) * (size_t)(d.W + 1));
+  b += align256(sizeof(int2) * (size_t)d.R_max);
   return b;
 }
 
@@ -69,6 +73,8 @@ inline Workspace carve(void* base, const Dims& d) {
   w.rank_tot = reinterpret_cast<int32_t*>(p);
   p += align256(sizeof(int32_t) * (size_t)d.W);
   w.rank_base = reinterpret_cast<int32_t*>(p);
+  p += align256(sizeof(int32_t) * (size_t)(d.W + 1));
+  w.row_src = reinterpret_cast<int2*>(p);
   return w;
 }
 

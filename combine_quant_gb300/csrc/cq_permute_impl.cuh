@@ -27,6 +27,9 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "cq_internal.cuh"
 
 namespace cq {
@@ -76,6 +79,76 @@ __device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 
+// mbarrier-tracked bulk (TMA) loads: global -> shared memory.
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+// The producer's one arrival, announcing `bytes` of bulk copies.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+// Bulk copy global -> shared memory, completing `bytes` on `bar`. Both
+// addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_load(void* sdst, const void* gsrc, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(sdst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Wait for the completion of phase `parity` of `bar`, giving up after about
+// one second (false).
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait(a, parity)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_u32(p))
+               : "memory");
+  return v;
+}
+// Streaming 128-bit global store (written once, not read again here).
+__device__ __forceinline__ void st_global_cs_v4(void* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
 // Round to nearest even, saturate to int8 (a NaN product gives 0).
 __device__ __forceinline__ uint32_t q8(float v) {
   int c = __float2int_rn(v);
@@ -109,11 +182,15 @@ __device__ __forceinline__ int floor_log2_bits(float a) {
 // 2^k as a binary32, for k in [-126, 127].
 __device__ __forceinline__ float pow2(int k) { return __uint_as_float((uint32_t)(k + 127) << 23); }
 
+// max(0, |v_t|) over the 16 values, NaN ignored, as a balanced tree (max is
+// exact and associative; the final max with 0 turns an all-NaN unit into 0).
 __device__ __forceinline__ float max16(const float (&v)[16]) {
-  float m = 0.f;
+  float m[8];
 #pragma unroll
-  for (int t = 0; t < 16; ++t) m = fmaxf(m, fabsf(v[t]));
-  return m;
+  for (int t = 0; t < 8; ++t) m[t] = fmaxf(fabsf(v[t]), fabsf(v[t + 8]));
+#pragma unroll
+  for (int t = 0; t < 4; ++t) m[t] = fmaxf(m[t], m[t + 4]);
+  return fmaxf(fmaxf(fmaxf(m[0], m[2]), fmaxf(m[1], m[3])), 0.f);
 }
 
 __device__ __forceinline__ uint4 q8_16(const float (&v)[16], float s) {
@@ -134,6 +211,28 @@ __device__ __forceinline__ uint4 q8_16_direct(const float (&v)[16]) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// Four int8 codes RNE(fl(v * m)) for products that are NaN or lie in
+// [-128, 128]; a NaN product gives 0. Clamping from below at -256 maps NaN to
+// -256 (max ignores NaN) and leaves the others alone; adding 1.5 * 2^23 then
+// gives a sum whose ulp is 1, so its low mantissa bits hold the nearest-even
+// integer n, and the low byte of its bit pattern is n in two's complement
+// (-256 -> 0). Three byte permutes pack the four codes.
+__device__ __forceinline__ uint32_t q8_magic(float v, float m) {
+  constexpr float kMagic = 12582912.f;  // 1.5 * 2^23
+  return __float_as_uint(__fadd_rn(fmaxf(__fmul_rn(v, m), -256.f), kMagic));
+}
+
+__device__ __forceinline__ uint32_t q8x4_magic(float a, float b, float c, float d, float m) {
+  return __byte_perm(__byte_perm(q8_magic(a, m), q8_magic(b, m), 0x0040),
+                     __byte_perm(q8_magic(c, m), q8_magic(d, m), 0x0040), 0x5410);
+}
+
+__device__ __forceinline__ uint4 q8_16_magic(const float (&v)[16], float m) {
+  return make_uint4(q8x4_magic(v[0], v[1], v[2], v[3], m), q8x4_magic(v[4], v[5], v[6], v[7], m),
+                    q8x4_magic(v[8], v[9], v[10], v[11], m),
+                    q8x4_magic(v[12], v[13], v[14], v[15], m));
+}
+
 __device__ __forceinline__ uint4 e4m3_16(const float (&v)[16], float mult) {
   uint32_t o[4];
 #pragma unroll
@@ -143,16 +242,19 @@ __device__ __forceinline__ uint4 e4m3_16(const float (&v)[16], float mult) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// Block-wide max of one float per thread; `buf` holds >= 32 floats and must
-// not be reused by another block_max until the next __syncthreads.
+// Block-wide max of one float per thread, for blocks of at most 256 threads
+// (8 warps); `buf` holds >= 8 floats and must not be reused by another
+// block_max until the next __syncthreads.
 __device__ __forceinline__ float block_max(float v, float* buf) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
-  if ((threadIdx.x & 31) == 0) buf[threadIdx.x >> 5] = v;
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) buf[threadIdx.x >> 5] = v;
   __syncthreads();
-  float m = 0.f;
-  const int nw = blockDim.x >> 5;
-  for (int w = 0; w < nw; ++w) m = fmaxf(m, buf[w]);
+  // Every group of 8 lanes reduces the same (up to) 8 warp maxima.
+  float m = (lane & 7) < (int)(blockDim.x >> 5) ? buf[lane & 7] : 0.f;
+#pragma unroll
+  for (int o = 4; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
   return m;
 }
 
@@ -175,7 +277,7 @@ __device__ __forceinline__ void unit_values(const uint4 (&u)[2], const float* sr
   if (SM == kScalar) {
 #pragma unroll
     for (int t = 0; t < 16; ++t) f[t] = __fmul_rn(f[t], scalar);
-  } else if (SM == kRowPerSlot || SM == kSharedRow) {
+  } else if (SM == kSharedRow) {
     const float* sm = srow + 16 * unit;
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
@@ -188,25 +290,45 @@ __device__ __forceinline__ void unit_values(const uint4 (&u)[2], const float* sr
   }
 }
 
-// Quantise this thread's two units of one row into the staging buffer: codes
-// at 16 bytes per unit in `codes`, the per-group (mode 3, floats) or
+// Quantise this thread's two units of one row: codes at 16 bytes per unit in
+// `codes` (shared staging, or the global row when GLOBAL), the per-group (mode 3, floats) or
 // per-block (modes 4/5, e8m0 bytes) scales in `scales`. Mode 2 returns the
 // row's carried scale. `red` is a block_max buffer (mode 2 only).
-template <int MODE>
+// 16 code bytes to shared (staging) or, when GLOBAL, straight to global memory.
+template <bool GLOBAL>
+__device__ __forceinline__ void put16(uint8_t* p, uint4 v) {
+  if (GLOBAL) {
+    st_global_cs_v4(p, v);
+  } else {
+    st_shared_v4(p, v);
+  }
+}
+
+template <int MODE, bool GLOBAL = false>
 __device__ __forceinline__ float quantise(const float (&f)[2][16], const Units& U,
                                           uint8_t* codes, uint8_t* scales, float* red) {
   float carried = 0.f;
   if (MODE == 1) {
 #pragma unroll
     for (int q = 0; q < 2; ++q)
-      if (U.ok[q]) st_shared_v4(codes + 16 * (threadIdx.x + q * blockDim.x), q8_16_direct(f[q]));
+      if (U.ok[q]) put16<GLOBAL>(codes + 16 * (threadIdx.x + q * blockDim.x), q8_16_direct(f[q]));
   } else if (MODE == 2) {
     const float amax = block_max(fmaxf(max16(f[0]), max16(f[1])), red);
     const float s = __fdiv_rn(127.f, amax);  // +inf for an all-zero row: codes 0, carried 0
     carried = __fdiv_rn(1.f, s);
+    if (s <= 3.402823466e38f || amax == 0.f) {
+      // Every product is in [-127, 127] (|x| <= max, s rounded), or NaN (a
+      // NaN element; inf * 0 when the max is infinite): add-and-pack rounding.
+      const float mult = amax == 0.f ? 0.f : s;
 #pragma unroll
-    for (int q = 0; q < 2; ++q)
-      if (U.ok[q]) st_shared_v4(codes + 16 * (threadIdx.x + q * blockDim.x), q8_16(f[q], s));
+      for (int q = 0; q < 2; ++q)
+        if (U.ok[q]) put16<GLOBAL>(codes + 16 * (threadIdx.x + q * blockDim.x), q8_16_magic(f[q], mult));
+    } else {
+      // 127 / max overflowed (max below about 3.7e-37): saturating conversion.
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+        if (U.ok[q]) put16<GLOBAL>(codes + 16 * (threadIdx.x + q * blockDim.x), q8_16(f[q], s));
+    }
   } else if (MODE == 3) {
     // A 128-group is 8 units held by 8 consecutive lanes.
 #pragma unroll
@@ -219,7 +341,7 @@ __device__ __forceinline__ float quantise(const float (&f)[2][16], const Units& 
       const float mult = m == 0.f ? 0.f : s;  // an all-zero group: codes 0, scale 0
       const int u = threadIdx.x + q * blockDim.x;
       if (U.ok[q]) {
-        st_shared_v4(codes + 16 * u, e4m3_16(f[q], mult));
+        put16<GLOBAL>(codes + 16 * u, e4m3_16(f[q], mult));
         if ((u & 7) == 0) reinterpret_cast<float*>(scales)[u >> 3] = __fdiv_rn(1.f, s);
       }
     }
@@ -237,7 +359,7 @@ __device__ __forceinline__ float quantise(const float (&f)[2][16], const Units& 
       }
       const int u = threadIdx.x + q * blockDim.x;
       if (U.ok[q]) {
-        st_shared_v4(codes + 16 * u, e4m3_16(f[q], pow2(-e)));  // x / 2^e, exact scaling
+        put16<GLOBAL>(codes + 16 * u, e4m3_16(f[q], pow2(-e)));  // x / 2^e, exact scaling
         if ((u & 1) == 0) scales[u >> 1] = (uint8_t)(e + 127);
       }
     }
@@ -245,6 +367,49 @@ __device__ __forceinline__ float quantise(const float (&f)[2][16], const Units& 
   return carried;
 }
 
+// Slot k of token tok (source rank r): its global row = first row of the
+// destination rank + first row of the (expert slot, source) block inside the
+// rank + arrival ordinal. Writes the inverse-map entry and, for a dispatched
+// slot, the (src, token, slot) row record and the carried weight. Returns the
+// row (-1 if none) and the slot's smooth-table row in `srow`.
+__device__ __forceinline__ int map_slot(const PermuteArgs& a, int64_t tok, int r, int k,
+                                        int& srow) {
+  const Dims& d = a.d;
+  srow = 0;
+  if (k >= d.NS) return -1;
+  const int e = a.ws.eidx[tok * d.NS + k];
+  int code = e, row = -1;
+  if (e >= 0) {
+    int g, dst;  // global expert slot, destination rank
+    if (k < d.K) {
+      const int id = a.expert_ids[tok * d.K + k];
+      g = d.S_r + id;
+      dst = d.S_r + id / d.L;
+      srow = d.S_eff + id;
+    } else {
+      const int s = k - d.K;
+      g = dst = s * d.R_rep + r % d.R_rep;  // a shared-expert rank hosts one slot
+      srow = s;
+    }
+    row = a.ws.rank_base[dst] + a.ws.local_off[(int64_t)g * d.W + r] + e;
+    if (row < 0 || (int64_t)row >= d.R_max) {  // consistency guard: never write outside
+      atomicOr(a.ws.status, (uint32_t)CQ_ST_INTERNAL);
+      row = -1;
+      code = CQ_INV_NONE;
+    } else {
+      code = row;
+      const int i = (int)(tok - (int64_t)r * d.BS);
+      reinterpret_cast<int4*>(a.assist_rows)[row] = make_int4(r, i, k, 0);
+      if (a.expand_scales)
+        a.expand_scales[row] =
+            k < d.K ? (a.expert_scales ? a.expert_scales[tok * d.K + k] : 0.f) : 1.f;
+    }
+  }
+  a.inv[tok * d.NS + k] = code;
+  return row;
+}
+
+// Token-major permute for every smooth shape but per-expert rows.
 // T: token type; MODE: quant_mode; SM: SmoothKind.
 template <class T, int MODE, int SM>
 __global__ void __launch_bounds__(256) permute_kernel(PermuteArgs a) {
@@ -292,38 +457,8 @@ __global__ void __launch_bounds__(256) permute_kernel(PermuteArgs a) {
   griddep_wait();  // routing outputs (ordinals, offsets) are read from here on
 
   if (threadIdx.x < 32) {
-    const int k = lane;
-    int row = -1, srow = 0;
-    if (k < d.NS) {
-      const int e = a.ws.eidx[tok * d.NS + k];
-      int code = e;
-      if (e >= 0) {
-        int g, dst;  // global expert slot, destination rank
-        if (k < d.K) {
-          const int id = a.expert_ids[tok * d.K + k];
-          g = d.S_r + id;
-          dst = d.S_r + id / d.L;
-          srow = d.S_eff + id;
-        } else {
-          const int s = k - d.K;
-          g = dst = s * d.R_rep + r % d.R_rep;  // a shared-expert rank hosts one slot
-          srow = s;
-        }
-        row = a.ws.rank_base[dst] + a.ws.local_off[(int64_t)g * d.W + r] + e;
-        if (row < 0 || (int64_t)row >= d.R_max) {  // consistency guard: never write outside
-          atomicOr(a.ws.status, (uint32_t)CQ_ST_INTERNAL);
-          row = -1;
-          code = CQ_INV_NONE;
-        } else {
-          code = row;
-          reinterpret_cast<int4*>(a.assist_rows)[row] = make_int4(r, i, k, 0);
-          if (a.expand_scales)
-            a.expand_scales[row] =
-                k < d.K ? (a.expert_scales ? a.expert_scales[tok * d.K + k] : 0.f) : 1.f;
-        }
-      }
-      a.inv[tok * d.NS + k] = code;
-    }
+    int srow;
+    const int row = map_slot(a, tok, r, lane, srow);
     const unsigned bal = __ballot_sync(kFull, row >= 0);
     if (row >= 0) {
       const int pos = __popc(bal & ((1u << lane) - 1u));
@@ -338,7 +473,7 @@ __global__ void __launch_bounds__(256) permute_kernel(PermuteArgs a) {
   if (!prefetched) load_row();  // routing found rows the inputs did not predict
 
   // Staged row layout: code row (2H bytes in mode 0, else H), then the scale
-  // row padded to 16 bytes; two such buffers when each slot is quantised alone.
+  // row padded to 16 bytes.
   const int code_bytes = MODE == 0 ? 2 * H : H;
   const int scale_bytes = MODE == 3 ? 4 * d.G3 : ((MODE == 4 || MODE == 5) ? d.SC : 0);
   const int stride = code_bytes + ((scale_bytes + 15) & ~15);
@@ -363,43 +498,6 @@ __global__ void __launch_bounds__(256) permute_kernel(PermuteArgs a) {
       bulk_commit();
       bulk_wait_read<0>();
     }
-  } else if (SM == kRowPerSlot) {
-    // x * smooth[expert]: one quantisation per routed row. Two staging
-    // buffers: row n is built while row n-1's bulk store still reads.
-    for (int n = 0; n < nrows; ++n) {
-      // Thread 0 waited (below) for the store that last read this buffer
-      // (row n-2); the barrier makes every thread see that.
-      if (n > 0) __syncthreads();
-      const float* sm = a.smooth + (int64_t)s_srow[n] * H;
-      float f[2][16];
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int u = threadIdx.x + q * blockDim.x;
-        if (U.ok[q]) {
-          unit_values<T, SM>(U.v[q], sm, 0.f, u, f[q]);
-        } else {
-#pragma unroll
-          for (int t = 0; t < 16; ++t) f[q][t] = 0.f;
-        }
-      }
-      uint8_t* buf = s_stage + (n & 1) * stride;
-      const float carried = quantise<MODE>(f, U, buf, buf + code_bytes, s_red[n & 1]);
-      fence_proxy_async_smem();
-      __syncthreads();
-      const int64_t row = s_row[n];
-      if (threadIdx.x == 0) {
-        bulk_store(out + row * code_bytes, buf, (uint32_t)code_bytes);
-        if (scale_bytes && a.scale_rows_bulk)
-          bulk_store(dyn + row * scale_bytes, buf + code_bytes, (uint32_t)scale_bytes);
-        bulk_commit();
-        bulk_wait_read<1>();
-        if (MODE == 2) reinterpret_cast<float*>(dyn)[row] = carried;
-      }
-      if (scale_bytes && !a.scale_rows_bulk)
-        for (int b = threadIdx.x; b < scale_bytes; b += blockDim.x)
-          dyn[row * scale_bytes + b] = buf[code_bytes + b];
-    }
-    if (threadIdx.x == 0) bulk_wait_read<0>();
   } else {
     // One quantisation per token: every routed row gets the same codes.
     const float* srow = SM == kSharedRow ? a.smooth : nullptr;
@@ -443,6 +541,216 @@ __global__ void __launch_bounds__(256) permute_kernel(PermuteArgs a) {
   griddep_launch_dependents();
 }
 
+// ---------------------------------------------------------------------------
+// Per-expert smooth rows: x * smooth[expert] is quantised once per dispatched
+// row, and what the rows of one expert share is the smooth row, not the token
+// row. This path therefore runs expert-major, in two kernels:
+//
+// index_kernel: one warp per source token maps its slots to rows (map_slot)
+//   and records, for every dispatched row, its token and smooth-table row.
+//
+// smooth_rows_kernel: each CTA takes a contiguous range of dispatched rows.
+//   Rows are ordered by destination rank, then local expert, so a range spans
+//   one expert or a few: the CTA keeps the expert's smooth row in registers
+//   (reloaded only when the expert changes) and streams the token rows
+//   through a ring of kXStages shared-memory slots, filled by bulk (TMA)
+//   loads that thread 0 issues kXStages rows ahead, one mbarrier per slot.
+//   Codes go straight from registers to the row with 128-bit streaming
+//   stores; one barrier per row (the row max, or an explicit one) frees the
+//   row's ring slot for the next load.
+constexpr int kXStages = 4;
+
+template <class T>  // T only keeps one instantiation per token-type translation unit
+__global__ void __launch_bounds__(256) index_kernel(PermuteArgs a) {
+  griddep_wait();
+  const int64_t tok = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (tok < (int64_t)a.d.W * a.d.BS) {
+    const int r = (int)(tok / a.d.BS);
+    int srow;
+    const int row = map_slot(a, tok, r, threadIdx.x & 31, srow);
+    if (row >= 0) a.ws.row_src[row] = make_int2((int)tok, srow);
+  }
+  griddep_launch_dependents();
+}
+
+template <class T, int MODE>
+__global__ void __launch_bounds__(256, 2) smooth_rows_kernel(PermuteArgs a) {
+  __shared__ uint64_t s_bar[kXStages];
+  __shared__ int s_srow[kXStages];
+  __shared__ float s_red[2][32];
+  __shared__ int s_fail;
+  extern __shared__ __align__(128) uint8_t s_ring[];  // kXStages token rows
+
+  const Dims& d = a.d;
+  const int H = d.H;
+  const int units = H >> 4;
+  const uint32_t xbytes = 2u * (uint32_t)H;
+  const int scale_bytes = MODE == 3 ? 4 * d.G3 : 0;
+  uint8_t* const dyn = static_cast<uint8_t*>(a.dynamic_scales);
+  uint8_t* const out = static_cast<uint8_t*>(a.expand_x);
+
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < kXStages; ++st) mbar_init(&s_bar[st], 1);
+    mbar_fence_init();
+    s_fail = 0;
+  }
+  __syncthreads();
+  griddep_wait();  // the row table and the total come from the earlier kernels
+
+  int64_t total = *a.ws.total;
+  if (total < 0 || total > d.R_max) {  // consistency guard
+    if (threadIdx.x == 0) atomicOr(a.ws.status, (uint32_t)CQ_ST_INTERNAL);
+    total = 0;
+  }
+  const int64_t lo = total * blockIdx.x / gridDim.x;
+  const int n_rows = (int)(total * (blockIdx.x + 1) / gridDim.x - lo);
+  const int64_t n_tok = (int64_t)d.W * d.BS;
+
+  // Thread 0: start the token row of local row `issued` into its ring slot.
+  int issued = 0;
+  int2 next = make_int2(0, 0);
+  auto issue = [&](int2 p) {
+    const int st = issued % kXStages;
+    if (p.x < 0 || (int64_t)p.x >= n_tok || p.y < 0 || p.y >= d.S_eff + d.M) {
+      // consistency guard: never read outside x or the smooth table
+      atomicOr(a.ws.status, (uint32_t)CQ_ST_INTERNAL);
+      p = make_int2(0, 0);
+    }
+    s_srow[st] = p.y;
+    mbar_arrive_expect_tx(&s_bar[st], xbytes);
+    bulk_load(s_ring + (size_t)st * xbytes, a.x + (int64_t)p.x * H, xbytes, &s_bar[st]);
+    ++issued;
+  };
+  if (threadIdx.x == 0) {
+    while (issued < n_rows && issued < kXStages) issue(a.ws.row_src[lo + issued]);
+    if (issued < n_rows) next = a.ws.row_src[lo + issued];
+  }
+  __syncthreads();
+
+  Units U;
+#pragma unroll
+  for (int q = 0; q < 2; ++q) U.ok[q] = (int)threadIdx.x + q * (int)blockDim.x < units;
+  float sm[2][16];
+  int cur = -1;
+  int j = 0;
+  for (; j < n_rows; ++j) {
+    const int st = j % kXStages;
+    if (!mbar_wait(&s_bar[st], (uint32_t)(j / kXStages) & 1u)) {
+      s_fail = 1;
+      atomicOr(a.ws.status, (uint32_t)CQ_ST_TIMEOUT);
+    }
+    const int srow = s_srow[st];
+    if (srow != cur) {
+      cur = srow;
+      const float* srcs = a.smooth + (int64_t)srow * H;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int u = threadIdx.x + q * blockDim.x;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const uint4 v = U.ok[q] ? ld_nc_v4(srcs + 16 * u + 4 * t) : make_uint4(0, 0, 0, 0);
+          sm[q][4 * t] = __uint_as_float(v.x);
+          sm[q][4 * t + 1] = __uint_as_float(v.y);
+          sm[q][4 * t + 2] = __uint_as_float(v.z);
+          sm[q][4 * t + 3] = __uint_as_float(v.w);
+        }
+      }
+    }
+    float f[2][16];
+    const uint8_t* xs = s_ring + (size_t)st * xbytes;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int u = threadIdx.x + q * blockDim.x;
+      uint4 w[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+      if (U.ok[q]) {
+        w[0] = ld_shared_v4(xs + 32 * u);
+        w[1] = ld_shared_v4(xs + 32 * u + 16);
+      }
+      const uint32_t* wv = reinterpret_cast<const uint32_t*>(w);
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        f[q][2 * t] = __fmul_rn(T::lo(wv[t]), sm[q][2 * t]);
+        f[q][2 * t + 1] = __fmul_rn(T::hi(wv[t]), sm[q][2 * t + 1]);
+      }
+    }
+    const int64_t row = lo + j;
+    // Mode 2's row max holds a barrier; the other modes take one here. Past
+    // it every thread has read ring slot st.
+    if (MODE != 2) __syncthreads();
+    const float carried =
+        quantise<MODE, true>(f, U, out + row * H, dyn + row * scale_bytes, s_red[j & 1]);
+    if (s_fail) break;  // set only before the barrier above: the same in all threads
+    if (threadIdx.x == 0) {
+      if (MODE == 2) reinterpret_cast<float*>(dyn)[row] = carried;
+      if (issued < n_rows) {  // refill the slot this row used
+        issue(next);
+        if (issued < n_rows) next = a.ws.row_src[lo + issued];
+      }
+    }
+  }
+  // After a timeout, wait (bounded again) for the loads still in flight
+  // before the CTA's shared memory is released.
+  if (threadIdx.x == 0)
+    for (int jj = j; jj < issued; ++jj)
+      mbar_wait(&s_bar[jj % kXStages], (uint32_t)(jj / kXStages) & 1u);
+  griddep_launch_dependents();
+}
+
+// Number of SMs of the current device (cached per device).
+inline int sm_count() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::atomic<int>& c = cached[dev & 63];
+  int n = c.load(std::memory_order_relaxed);
+  if (n <= 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    c.store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
+// The per-expert-smooth path: index_kernel, then smooth_rows_kernel with one
+// wave of CTAs (SMs x resident CTAs per SM).
+template <class T, int MODE>
+cudaError_t launch_smooth_rows(const PermuteArgs& a, cudaStream_t s) {
+  const int64_t tokens = (int64_t)a.d.W * a.d.BS;
+  cudaError_t e =
+      launch_pdl(index_kernel<T>, dim3((unsigned)((tokens + 7) / 8)), dim3(256), 0, s, a);
+  if (e != cudaSuccess) return e;
+  const int units = a.d.H >> 4;
+  int threads = ((units + 1) / 2 + 31) / 32 * 32;
+  if (threads < 32) threads = 32;
+  const size_t smem = (size_t)kXStages * 2 * a.d.H;
+  auto* kern = smooth_rows_kernel<T, MODE>;
+  // Per instantiation: the dynamic shared memory limit set so far and the
+  // last occupancy query.
+  static std::mutex mu;
+  static size_t smem_set = 0, occ_smem = 0;
+  static int occ_threads = 0, occ_blocks = 0;
+  int blocks;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (smem > smem_set) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      smem_set = smem;
+    }
+    if (occ_threads != threads || occ_smem != smem) {
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_blocks, kern, threads, smem);
+      if (e != cudaSuccess) return e;
+      occ_threads = threads;
+      occ_smem = smem;
+    }
+    blocks = occ_blocks;
+  }
+  if (blocks < 1) return cudaErrorInvalidConfiguration;
+  int64_t grid = (int64_t)sm_count() * blocks;
+  if (grid > a.d.R_max) grid = a.d.R_max;
+  if (grid < 1) grid = 1;
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(threads), smem, s, a);
+}
+
 template <class T, int MODE, int SM>
 cudaError_t launch_one(const PermuteArgs& a, cudaStream_t s) {
   const int units = a.d.H >> 4;
@@ -452,7 +760,7 @@ cudaError_t launch_one(const PermuteArgs& a, cudaStream_t s) {
   const size_t code_bytes = MODE == 0 ? 2 * (size_t)a.d.H : (size_t)a.d.H;
   const size_t scale_bytes =
       MODE == 3 ? 4 * (size_t)a.d.G3 : ((MODE == 4 || MODE == 5) ? (size_t)a.d.SC : 0);
-  const size_t smem = (code_bytes + ((scale_bytes + 15) & ~size_t(15))) * (SM == kRowPerSlot ? 2 : 1);
+  const size_t smem = code_bytes + ((scale_bytes + 15) & ~size_t(15));
   return launch_pdl(permute_kernel<T, MODE, SM>, dim3((unsigned)grid), dim3(threads), smem, s, a);
 }
 
@@ -464,17 +772,17 @@ cudaError_t launch_typed(const PermuteArgs& a, cudaStream_t s) {
   switch (a.d.mode) {
     case 0: return launch_one<T, 0, kNoSmooth>(a, s);
     case 1:
-      if (sm == kRowPerSlot) return launch_one<T, 1, kRowPerSlot>(a, s);
+      if (sm == kRowPerSlot) return launch_smooth_rows<T, 1>(a, s);
       if (sm == kSharedRow) return launch_one<T, 1, kSharedRow>(a, s);
       if (sm == kScalar) return launch_one<T, 1, kScalar>(a, s);
       return cudaErrorInvalidValue;  // static quantisation needs scales
     case 2:
-      if (sm == kRowPerSlot) return launch_one<T, 2, kRowPerSlot>(a, s);
+      if (sm == kRowPerSlot) return launch_smooth_rows<T, 2>(a, s);
       if (sm == kSharedRow) return launch_one<T, 2, kSharedRow>(a, s);
       if (sm == kScalar) return launch_one<T, 2, kScalar>(a, s);
       return launch_one<T, 2, kNoSmooth>(a, s);
     case 3:
-      if (sm == kRowPerSlot) return launch_one<T, 3, kRowPerSlot>(a, s);
+      if (sm == kRowPerSlot) return launch_smooth_rows<T, 3>(a, s);
       if (sm == kSharedRow) return launch_one<T, 3, kSharedRow>(a, s);
       if (sm == kScalar) return launch_one<T, 3, kScalar>(a, s);
       return launch_one<T, 3, kNoSmooth>(a, s);

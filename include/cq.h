@@ -82,8 +82,11 @@ enum {
   CQ_ST_BAD_ID = 1,  /* an active pair named an id outside [0, M+Z+C+Q); it was skipped */
   CQ_ST_BAD_MASK = 2, /* a 1-D x_active_mask had a true entry after a false one
                          ([DV3] x_active_mask_optional); entries were honoured as given */
-  CQ_ST_INTERNAL = 4   /* a computed row or code fell outside its buffer (an internal
+  CQ_ST_INTERNAL = 4,  /* a computed row or code fell outside its buffer (an internal
                           consistency guard); the access was skipped */
+  CQ_ST_TIMEOUT = 8    /* a kernel's bounded wait for its own bulk copies gave up (about
+                          one second); the kernel stopped early and its outputs are
+                          incomplete */
 };
 
 /* Codes stored in the inverse map for slots that own no dispatched row. */
@@ -145,6 +148,9 @@ int cq_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
  *                  (1.0 on shared-expert rows).
  *   workspace      >= cq_workspace_size() bytes, 256-byte aligned, zero-filled
  *                  once by cq_workspace_init before first use.
+ * Alignment (else CQ_ERR_ARG): x, expand_x, assist_info and a smooth_scales
+ * row table (smooth_kind 0, 1) 16 bytes; a scalar smooth_scales and f32
+ * dynamic_scales (modes 2, 3) 4 bytes.
  */
 int cq_dispatch(const cq_config* cfg, const void* x, const int32_t* expert_ids,
                 const float* smooth_scales, const uint8_t* x_active_mask,

@@ -89,3 +89,32 @@ def test_fp16_special_experts_and_masks():
 
 def test_fp16_dsv3_small():
     gh.full_parity(workloads.as_fp16(_base("dsv3_small")))
+
+
+@pytest.mark.parametrize("kind", [None, 0, 2])
+def test_mode2_nonfinite_and_extreme_rows(kind):
+    """Per-token int8 on rows that leave the ordinary case: all-zero and -0
+    rows (scale 0, codes 0), NaN elements (code 0, scale from the NaN-ignoring
+    max), infinities (max inf, scale 0), rows so small that 127/max overflows,
+    and huge rows. kind None: no smooth; 0: per-expert rows; 2: one scalar."""
+    wl = _base("dsv3_small")
+    x = workloads.bf16_bits_to_f32(wl.x).copy()
+    x[0, 0] = 0.0
+    x[0, 1] = -0.0
+    x[0, 2, 5] = np.nan
+    x[0, 3] = 0.0
+    x[0, 3, 7] = np.nan
+    x[0, 4, 9] = np.inf
+    x[0, 5, 11] = -np.inf
+    x[0, 5, 12] = np.nan
+    x[1, 0] *= 1e-38
+    x[1, 1] = 0.0
+    x[1, 1, 3] = 1e-39
+    x[1, 2] *= 1e30
+    x[1, 3, 100] = 3.0e38
+    x[2, 4] = -1.0 / 3.0
+    wl.x = workloads.to_bf16_bits(x)
+    if kind is None:
+        gh.full_parity(_with(wl, 2))
+    else:
+        gh.full_parity(_with(wl, 2, _smooth(wl, kind), kind))
