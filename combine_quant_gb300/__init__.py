@@ -8,5 +8,5 @@ synthetic inputs; ``build`` compiles the library in-tree.
 """
 from .api import (Config, DispatchResult, alloc_dispatch_outputs, alloc_workspace,  # noqa: F401
                   assist_views, combine, combine_q8, combine_quant, dispatch, dispatch_permute,
-                  dispatch_route, read_status)
+                  dispatch_route, read_combine_status, read_status)
 from ._lib import CqError  # noqa: F401

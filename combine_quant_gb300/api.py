@@ -325,6 +325,17 @@ def read_status(workspace: torch.Tensor) -> int:
     return int(st.value)
 
 
+def read_combine_status(device=None) -> int:
+    """Synchronise the current stream of `device`, return and clear the
+    combine kernels' status bits (CQ_ST_TIMEOUT) of that device."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    st = ctypes.c_uint32(0)
+    with torch.cuda.device(dev):
+        rc = _lib.load().cq_read_combine_status(ctypes.byref(st), _stream(dev))
+    _lib.check(rc, "cq_read_combine_status")
+    return int(st.value)
+
+
 def assist_views(cfg: Config, assist_info: torch.Tensor):
     """Views into assist_info: rows [R_max, 4], inv [W, BS, NS], rank_row_base [W+1]."""
     R, W, BS, NS = cfg.max_rows, cfg.ep_world_size, cfg.max_bs, cfg.num_slots

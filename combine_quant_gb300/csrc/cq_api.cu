@@ -345,6 +345,13 @@ int cq_read_status(void* workspace, uint32_t* status, void* stream) {
   return CQ_OK;
 }
 
+int cq_read_combine_status(uint32_t* status, void* stream) {
+  if (!status) return CQ_ERR_ARG;
+  return cq::read_combine_status(status, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? CQ_OK
+             : CQ_ERR_CUDA;
+}
+
 const char* cq_strerror(int code) {
   switch (code) {
     case CQ_OK: return "ok";

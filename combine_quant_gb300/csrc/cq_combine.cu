@@ -13,6 +13,8 @@
 // expert scale, sum in float, add the shared expert output, cast back), with
 // the special experts of "low_latency_dispatch" 特殊专家场景. Token, expert
 // output and result rows are bf16 or fp16 (the T template parameter).
+#include <mutex>
+
 #include "cq_internal.cuh"
 
 namespace cq {
@@ -210,6 +212,251 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(CombineArgs a, Src sr
   store8<T, OUT_F32>(a.y, tok * H + col, acc);
 }
 
+// ---------------------------------------------------------------------------
+// Combine from 16-bit expert rows with staged gathers. Persistent CTAs (one
+// wave) take tokens blockIdx.x, blockIdx.x + gridDim.x, ... One producer
+// warp walks the same (token, slot) sequence as the consumers and streams
+// every dispatched row it meets into a ring of shared-memory slots with bulk
+// (TMA) loads, running up to the ring size ahead (a full and an empty
+// mbarrier per slot). The consumer warps sum the rows from shared memory in
+// slot order, exactly as combine_kernel does; copy and const slots read
+// ori_x / const_v directly. Every wait gives up after about a second
+// (CQ_ST_TIMEOUT) and the producer then waits (bounded again) for its loads
+// in flight before the CTA ends.
+constexpr int kRingMax = 16;
+
+// Sticky status of the combine kernels of this device (CQ_ST_* bits), read
+// and cleared by cq_read_combine_status.
+__device__ uint32_t g_combine_status;
+
+constexpr int kUnitsPerThread = 4;  // 8-element units per consumer thread
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+// Bulk copy global -> shared memory completing `bytes` on `bar` (both
+// addresses 16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(void* sdst, const void* gsrc, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(sdst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+// Wait for the completion of phase `parity`; false after about one second.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait(a, parity)) return true;
+    if (globaltimer_ns() - t0 > 1000000000ull) return false;
+  }
+}
+__device__ __forceinline__ uint4 ld_shared_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_u32(p))
+               : "memory");
+  return v;
+}
+
+// Slot k's inverse-map code `code`, with the consistency guard of
+// combine_kernel (a row outside the buffer, a const index outside [0, Q), or
+// a special code on a shared slot counts as "no row").
+__device__ __forceinline__ int guard_code(const Dims& d, int code, int k) {
+  const bool bad_row = code >= 0 && (int64_t)code >= d.R_max;
+  const bool bad_const =
+      code <= CQ_INV_CONST_BASE && (CQ_INV_CONST_BASE - code >= d.Q || k >= d.K);
+  const bool bad_copy = code == CQ_INV_COPY && (d.C == 0 || k >= d.K);
+  return (bad_row || bad_const || bad_copy) ? CQ_INV_NONE : code;
+}
+
+// Lane k's raw slot code of token tok (CQ_INV_NONE past NS or past the last
+// token): loaded one token ahead, guarded when used.
+__device__ __forceinline__ int raw_code(const CombineArgs& a, int64_t tok, int64_t n_tok, int k) {
+  return (tok < n_tok && k < a.d.NS) ? __ldg(a.inv + tok * a.d.NS + k) : CQ_INV_NONE;
+}
+
+// Work item = (token, column chunk of `cw` elements); item i is token
+// i / nchunk, chunk i % nchunk. CTA b takes items b, b + gridDim.x, ...
+template <class T, bool OUT_F32>
+__global__ void __launch_bounds__(288) combine_staged_kernel(CombineArgs a, int nslots, int nchunk,
+                                                            int cw) {
+  extern __shared__ __align__(128) uint8_t s_ring[];  // nslots chunks of 2*cw bytes
+  __shared__ uint64_t s_full[kRingMax];
+  __shared__ uint64_t s_empty[kRingMax];
+  __shared__ volatile int s_fail;
+
+  const Dims& d = a.d;
+  const int H = d.H;
+  const uint32_t slot_bytes = 2u * (uint32_t)cw;
+  const int ncons = (int)blockDim.x - 32;  // consumer threads
+  const int nwc = ncons >> 5;              // consumer warps
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t n_tok = (int64_t)d.W * d.BS;
+  const int64_t n_items = n_tok * nchunk;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < nslots; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&s_empty[s], (uint32_t)nwc);
+    }
+    mbar_fence_init();
+    s_fail = 0;
+  }
+  __syncthreads();
+  griddep_wait();  // the inverse map and the expert rows come from earlier kernels
+
+  if (warp == nwc) {
+    // Producer warp: lane 0 issues; the warp reads each item's slot codes.
+    int64_t issued = 0;
+    bool ok = true;
+    int next = raw_code(a, blockIdx.x / nchunk, n_tok, lane);
+    for (int64_t it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+      const int64_t tok = it / nchunk;
+      const int c0 = (int)(it - tok * nchunk) * cw;
+      const uint32_t bytes = 2u * (uint32_t)min(cw, H - c0);
+      const int code = guard_code(d, next, lane);
+      next = raw_code(a, (it + gridDim.x) / nchunk, n_tok, lane);
+      for (int k = 0; k < d.NS; ++k) {
+        const int ck = __shfl_sync(0xffffffffu, code, k);
+        if (ck < 0) continue;
+        if (lane == 0) {
+          const int s = (int)(issued % nslots);
+          if (issued >= nslots &&
+              !mbar_wait(&s_empty[s], (uint32_t)((issued / nslots) - 1) & 1u)) {
+            s_fail = 1;
+            atomicOr(&g_combine_status, (uint32_t)CQ_ST_TIMEOUT);
+          }
+          if (!s_fail) {
+            mbar_arrive_expect_tx(&s_full[s], bytes);
+            bulk_load(s_ring + (size_t)s * slot_bytes, a.ffn + (int64_t)ck * H + c0, bytes,
+                      &s_full[s]);
+            ++issued;
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, s_fail, 0) == 0;
+        if (!ok) break;
+      }
+    }
+    // Wait (bounded) for the last loads to land before this warp ends, so
+    // that no copy is in flight once the consumers are gone.
+    if (lane == 0)
+      for (int64_t i = issued > nslots ? issued - nslots : 0; i < issued; ++i)
+        mbar_wait(&s_full[i % nslots], (uint32_t)(i / nslots) & 1u);
+    return;
+  }
+
+  // Consumer warps.
+  int64_t consumed = 0;
+  auto raw_w = [&](int64_t t) {
+    return (t < n_tok && lane < d.K) ? __ldg(a.expert_scales + t * d.K + lane) : 1.f;
+  };
+  int next = raw_code(a, blockIdx.x / nchunk, n_tok, lane);
+  float next_w = raw_w(blockIdx.x / nchunk);
+  for (int64_t it = blockIdx.x; it < n_items; it += gridDim.x) {
+    const int64_t tok = it / nchunk;
+    const int c0 = (int)(it - tok * nchunk) * cw;
+    const int cu = min(cw, H - c0) >> 3;  // 8-element units in this chunk
+    const int code = guard_code(d, next, lane);
+    const float wl = next_w;
+    next = raw_code(a, (it + gridDim.x) / nchunk, n_tok, lane);
+    next_w = raw_w((it + gridDim.x) / nchunk);
+    float acc[kUnitsPerThread][8];
+#pragma unroll
+    for (int i = 0; i < kUnitsPerThread; ++i)
+#pragma unroll
+      for (int t = 0; t < 8; ++t) acc[i][t] = 0.f;
+    const uint16_t* xrow = a.ori_x ? a.ori_x + tok * H + c0 : nullptr;
+    for (int k = 0; k < d.NS; ++k) {
+      const int ck = __shfl_sync(0xffffffffu, code, k);
+      const float w = __shfl_sync(0xffffffffu, wl, k);
+      if (ck >= 0) {
+        const int s = (int)(consumed % nslots);
+        // The whole warp leaves together if any lane gave up.
+        if (!__all_sync(0xffffffffu, mbar_wait(&s_full[s], (uint32_t)(consumed / nslots) & 1u))) {
+          s_fail = 1;
+          if (lane == 0) atomicOr(&g_combine_status, (uint32_t)CQ_ST_TIMEOUT);
+          return;
+        }
+        const uint8_t* rowp = s_ring + (size_t)s * slot_bytes;
+#pragma unroll
+        for (int i = 0; i < kUnitsPerThread; ++i) {
+          const int u = threadIdx.x + i * ncons;
+          if (u < cu) {
+            float f[8];
+            unpack8<T>(ld_shared_v4(rowp + 16 * u), f);
+            if (k < d.K) {
+              fma8f(acc[i], w, f);
+            } else {
+              add8f(acc[i], f);  // shared-expert rows: added unweighted
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_empty[s]);
+        ++consumed;
+      } else if (ck == CQ_INV_COPY || ck <= CQ_INV_CONST_BASE) {
+#pragma unroll
+        for (int i = 0; i < kUnitsPerThread; ++i) {
+          const int u = threadIdx.x + i * ncons;
+          if (u < cu) {
+            const int64_t col = 8 * (int64_t)u;
+            if (ck == CQ_INV_COPY) {
+              float f[8];
+              unpack8<T>(ld_nc_v4(xrow + col), f);  // Moe(ori_x) = ori_x
+              fma8f(acc[i], w, f);
+            } else {
+              const int cc = CQ_INV_CONST_BASE - ck;
+              fma8_const<T>(acc[i], w, a.alpha1[cc], a.alpha2[cc], ld_nc_v4(xrow + col),
+                            ld_nc_v4(a.const_v + (int64_t)cc * H + c0 + col));
+            }
+          }
+        }
+      }
+      // CQ_INV_NONE: zero expert, masked pair or inactive token adds nothing.
+    }
+#pragma unroll
+    for (int i = 0; i < kUnitsPerThread; ++i) {
+      const int u = threadIdx.x + i * ncons;
+      if (u < cu) store8<T, OUT_F32>(a.y, tok * H + c0 + 8 * (int64_t)u, acc[i]);
+    }
+  }
+}
+
 // Combine-side int8 quantisation of the expert outputs before they are sent
 // back ("CANN MoE Dispatch/Combine 通信算子性能优化实践", Int8QuantProcess):
 // per block of 8 values, scale = max|v| * fl(1/127), code = RNE(v / scale).
@@ -242,6 +489,61 @@ __global__ void __launch_bounds__(kThreads) combine_quant_kernel(CombineArgs a, 
   a.ffn_scales[row * (H >> 3) + u] = s;
 }
 
+// Number of SMs of the current device.
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+// Column chunks of at most kChunkCols elements; a ring of at most
+// kRingBytes (several CTAs per SM), 2..kRingMax chunks; one CTA per item
+// (kPersistent false) or one wave of CTAs looping over the items.
+constexpr int kChunkCols = 4096;
+constexpr size_t kRingBytes = 29u << 10;
+constexpr bool kPersistent = true;
+
+template <class T, bool OUT_F32>
+cudaError_t launch_staged(const CombineArgs& a, cudaStream_t s) {
+  const int H = a.d.H;
+  const int nchunk = (H + kChunkCols - 1) / kChunkCols;
+  const int cw = ((H + nchunk - 1) / nchunk + 7) / 8 * 8;
+  const int per = (cw / 8 + kUnitsPerThread - 1) / kUnitsPerThread;
+  const int ncons = (per + 31) / 32 * 32;
+  const int threads = ncons + 32;
+  const size_t slot_bytes = 2 * (size_t)cw;
+  int nslots = (int)(kRingBytes / slot_bytes);
+  if (nslots > kRingMax) nslots = kRingMax;
+  if (nslots < 2) nslots = 2;
+  const size_t smem = (size_t)nslots * slot_bytes;
+  auto* kern = combine_staged_kernel<T, OUT_F32>;
+  cudaError_t e = prepare_kernel<combine_staged_kernel<T, OUT_F32>>(smem);
+  if (e != cudaSuccess) return e;
+  // The last occupancy query of this instantiation.
+  static std::mutex mu;
+  static size_t occ_smem = 0;
+  static int occ_threads = 0, occ_blocks = 0;
+  int blocks;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (occ_threads != threads || occ_smem != smem) {
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_blocks, kern, threads, smem);
+      if (e != cudaSuccess) return e;
+      occ_threads = threads;
+      occ_smem = smem;
+    }
+    blocks = occ_blocks;
+  }
+  const int n_sm = sm_count();
+  if (blocks < 1 || n_sm < 1) return cudaErrorInvalidConfiguration;
+  const int64_t items = (int64_t)a.d.W * a.d.BS * nchunk;
+  int64_t grid = kPersistent ? (int64_t)n_sm * blocks : items;
+  if (grid > items) grid = items;
+  if (grid < 1) grid = 1;
+  return launch_pdl(kern, dim3((unsigned)grid), dim3(threads), smem, s, a, nslots, nchunk, cw);
+}
+
 template <class T, class Src>
 cudaError_t launch_combine_t(const CombineArgs& a, const Src& src, cudaStream_t s) {
   const int units = a.d.H >> 3;
@@ -255,8 +557,22 @@ cudaError_t launch_combine_t(const CombineArgs& a, const Src& src, cudaStream_t 
 }  // namespace
 
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) {
-  if (a.d.x_dtype == 1) return launch_combine_t<F16>(a, Src16<F16>{a.ffn}, s);
-  return launch_combine_t<BF16>(a, Src16<BF16>{a.ffn}, s);
+  if (a.d.x_dtype == 1)
+    return a.out_f32 ? launch_staged<F16, true>(a, s) : launch_staged<F16, false>(a, s);
+  return a.out_f32 ? launch_staged<BF16, true>(a, s) : launch_staged<BF16, false>(a, s);
+}
+
+cudaError_t read_combine_status(uint32_t* status, cudaStream_t s) {
+  uint32_t v = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_combine_status, sizeof(v), 0,
+                                            cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return e;
+  const uint32_t zero = 0;
+  e = cudaMemcpyToSymbolAsync(g_combine_status, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  *status = v;
+  return e;
 }
 
 cudaError_t launch_combine_q8(const CombineArgs& a, cudaStream_t s) {

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "cq.h"
 
 namespace cq {
@@ -174,6 +176,36 @@ cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t 
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Params>(args)...);
 }
 
+// Once per device and kernel: ask for the largest shared-memory carveout,
+// and allow `smem` bytes of dynamic shared memory (raised when a later call
+// needs more). Kernels chained with programmatic dependent launch share SMs
+// while one ends and the next starts; an SM set up with a small carveout for
+// one kernel cannot take the next kernel's CTAs that need a large one until
+// it drains, which turns a one-wave grid into two.
+constexpr int kMaxDevices = 64;
+template <auto Kernel>
+cudaError_t prepare_kernel(size_t smem) {
+  static std::mutex mu;
+  static size_t allowed[kMaxDevices];
+  static bool carved[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!carved[dev]) {
+    e = cudaFuncSetAttribute(Kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
+    carved[dev] = true;
+  }
+  if (smem > allowed[dev]) {
+    e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    allowed[dev] = smem;
+  }
+  return cudaSuccess;
+}
+
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -185,5 +217,6 @@ cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);     // from bf16 rows
 cudaError_t launch_combine_q8(const CombineArgs& a, cudaStream_t s);  // from int8 rows
 cudaError_t launch_combine_quant(const CombineArgs& a, cudaStream_t s);
+cudaError_t read_combine_status(uint32_t* status, cudaStream_t s);
 
 }  // namespace cq

@@ -293,7 +293,7 @@ __device__ __forceinline__ void unit_values(const uint4 (&u)[2], const float* sr
 // Quantise this thread's two units of one row: codes at 16 bytes per unit in
 // `codes` (shared staging, or the global row when GLOBAL), the per-group (mode 3, floats) or
 // per-block (modes 4/5, e8m0 bytes) scales in `scales`. Mode 2 returns the
-// row's carried scale. `red` is a block_max buffer (mode 2 only).
+// row's carried scale in the threads of warp 0. `red` is a block_max buffer (mode 2 only).
 // 16 code bytes to shared (staging) or, when GLOBAL, straight to global memory.
 template <bool GLOBAL>
 __device__ __forceinline__ void put16(uint8_t* p, uint4 v) {
@@ -315,7 +315,7 @@ __device__ __forceinline__ float quantise(const float (&f)[2][16], const Units& 
   } else if (MODE == 2) {
     const float amax = block_max(fmaxf(max16(f[0]), max16(f[1])), red);
     const float s = __fdiv_rn(127.f, amax);  // +inf for an all-zero row: codes 0, carried 0
-    carried = __fdiv_rn(1.f, s);
+    if (threadIdx.x < 32) carried = __fdiv_rn(1.f, s);  // only warp 0 stores it
     if (s <= 3.402823466e38f || amax == 0.f) {
       // Every product is in [-127, 127] (|x| <= max, s rounded), or NaN (a
       // NaN element; inf * 0 when the max is infinite): add-and-pack rounding.
@@ -723,19 +723,14 @@ cudaError_t launch_smooth_rows(const PermuteArgs& a, cudaStream_t s) {
   if (threads < 32) threads = 32;
   const size_t smem = (size_t)kXStages * 2 * a.d.H;
   auto* kern = smooth_rows_kernel<T, MODE>;
-  // Per instantiation: the dynamic shared memory limit set so far and the
-  // last occupancy query.
+  if ((e = prepare_kernel<smooth_rows_kernel<T, MODE>>(smem)) != cudaSuccess) return e;
+  // The last occupancy query of this instantiation.
   static std::mutex mu;
-  static size_t smem_set = 0, occ_smem = 0;
+  static size_t occ_smem = 0;
   static int occ_threads = 0, occ_blocks = 0;
   int blocks;
   {
     std::lock_guard<std::mutex> lock(mu);
-    if (smem > smem_set) {
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-      smem_set = smem;
-    }
     if (occ_threads != threads || occ_smem != smem) {
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_blocks, kern, threads, smem);
       if (e != cudaSuccess) return e;
@@ -761,6 +756,8 @@ cudaError_t launch_one(const PermuteArgs& a, cudaStream_t s) {
   const size_t scale_bytes =
       MODE == 3 ? 4 * (size_t)a.d.G3 : ((MODE == 4 || MODE == 5) ? (size_t)a.d.SC : 0);
   const size_t smem = code_bytes + ((scale_bytes + 15) & ~size_t(15));
+  const cudaError_t e = prepare_kernel<permute_kernel<T, MODE, SM>>(smem);
+  if (e != cudaSuccess) return e;
   return launch_pdl(permute_kernel<T, MODE, SM>, dim3((unsigned)grid), dim3(threads), smem, s, a);
 }
 

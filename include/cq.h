@@ -20,7 +20,8 @@
  *   - All tensor pointers are DEVICE pointers, row-major, contiguous, owned
  *     by the caller. The library never allocates or frees memory.
  *   - `stream` is a cudaStream_t passed as void*. Work is enqueued on it and
- *     the call returns without synchronising (except cq_read_status).
+ *     the call returns without synchronising (except cq_read_status and
+ *     cq_read_combine_status).
  *   - Return 0 (CQ_OK) or a negative CQ_ERR_* code. Argument errors are found
  *     on the host before anything is enqueued; nothing is enqueued then.
  *   - Data-dependent problems found on the device (an out-of-range expert
@@ -277,8 +278,16 @@ int cq_dispatch_noalloc(const cq_config* cfg, const void* x, const int32_t* expe
                         int64_t* expert_token_nums, float* expand_scales, void* stream);
 
 /* Synchronise `stream`, copy the workspace status word into *status and clear
- * it. The only call in this library that waits for the device. */
+ * it. One of the two calls in this library that wait for the device. */
 int cq_read_status(void* workspace, uint32_t* status, void* stream);
+
+/* The combine kernels take no workspace; their status word (CQ_ST_TIMEOUT
+ * only: a bounded wait for the kernel's own bulk loads gave up) is one word
+ * per device inside the library, shared by all combine calls on that device.
+ * Synchronise `stream`, copy the word of the current device into *status and
+ * clear it. Returns CQ_ERR_ARG if status is NULL, CQ_ERR_CUDA on a CUDA
+ * error. */
+int cq_read_combine_status(uint32_t* status, void* stream);
 
 /* Static description of an error code. */
 const char* cq_strerror(int code);

@@ -168,6 +168,7 @@ def full_parity(wl):
     ffn = FfnStandin(wl, cfg.max_rows)
     y32 = host(gpu_combine(wl, cfg, out, ffn, torch.float32))
     y16 = host(gpu_combine(wl, cfg, out, ffn, None))
+    assert cq.read_combine_status() == 0, "a combine kernel's bounded wait gave up"
     inv = ffn.remap_inv(route.inv)
     args = (wl.cfg, ffn.pool, inv, wl.expert_scales, wl.x, wl.const_alpha1, wl.const_alpha2,
             wl.const_v)
