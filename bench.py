@@ -43,12 +43,12 @@ L2_FLUSH_BYTES = 256 << 20
 # the SHA-256 of the kernel's source file when it was captured; reported only
 # while the source is unchanged.
 NCU_TRAFFIC = {
-    # profiles/dsv3_kernels_ncu_full.md: read 470.065408 MB + write 50.161408 MB
-    "combine": {"bytes_per_launch": 520226816,
-                "src_sha": "6ec55b69f2c4b6bc4e4f93ae7ab286b905c8ca541fc5cd584011ccc04221c83f"},
-    # read 59.2512 MB + write 175.902976 MB
-    "permute": {"bytes_per_launch": 235154176,
-                "src_sha": "4f67ff779144f681463b901fb709516e62474b245cc0c351d6eda7b58c130758"},
+    # profiles/dsv3_kernels_ncu_full.md: read 470.106624 MB + write 48.222976 MB
+    "combine": {"bytes_per_launch": 518329600,
+                "src_sha": "ecd4a070107dc6ab90ee65727e91702403e45e086dda3b1dee1c4aa08749d5b5"},
+    # read 59.21664 MB + write 175.385088 MB
+    "permute": {"bytes_per_launch": 234601728,
+                "src_sha": "f8776286f4021b6290db313b28889a21e231a6d74908c52590e56a7a8c24857d"},
 }
 
 
