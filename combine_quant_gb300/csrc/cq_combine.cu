@@ -460,33 +460,69 @@ __global__ void __launch_bounds__(288) combine_staged_kernel(CombineArgs a, int 
 // Combine-side int8 quantisation of the expert outputs before they are sent
 // back ("CANN MoE Dispatch/Combine 通信算子性能优化实践", Int8QuantProcess):
 // per block of 8 values, scale = max|v| * fl(1/127), code = RNE(v / scale).
-// One CTA per (row, chunk); rows past the dispatched total are skipped.
+// One wave of CTAs; CTA b takes rows b, b + gridDim.x, ... below the
+// dispatched total, each thread up to kQUnits 8-element units of the row with
+// all its loads issued before the first division.
+constexpr int kQThreads = 256;
+constexpr int kQUnits = 4;  // kQThreads * kQUnits * 8 >= the largest H (8192)
+
+// RNE(fl(v / s)) as the low byte of a float, for a block whose scale s is
+// normal or infinite, or whose max is 0: every quotient is then NaN or lies
+// in [-128, 128]. max(q, -256) maps NaN (0/0, inf/inf) to -256; adding
+// 1.5 * 2^23 leaves RNE(q) in the low byte of the sum (-256 -> 0).
+__device__ __forceinline__ uint32_t q8_div_magic(float v, float s) {
+  return __float_as_uint(__fadd_rn(fmaxf(__fdiv_rn(v, s), -256.f), 12582912.f));
+}
+
 template <class T>
-__global__ void __launch_bounds__(kThreads) combine_quant_kernel(CombineArgs a, int nchunk) {
+__global__ void __launch_bounds__(kQThreads) combine_quant_kernel(CombineArgs a) {
   griddep_wait();  // the rows may come from the preceding kernel
   const Dims& d = a.d;
-  const int64_t row = blockIdx.x / nchunk;
-  const int chunk = blockIdx.x - (int)(row * nchunk);
-  if (row >= (int64_t)*a.total_rows) return;
   const int H = d.H;
-  const int u = chunk * kThreads + threadIdx.x;
-  if (u >= (H >> 3)) return;
-  float f[8];
-  unpack8<T>(ld_nc_v4(a.ffn + row * H + 8 * (int64_t)u), f);
-  float m = 0.f;
+  const int units = H >> 3;
+  int64_t total = *a.total_rows;
+  if (total > d.R_max) total = d.R_max;  // never read or write past the buffers
+  for (int64_t row = blockIdx.x; row < total; row += gridDim.x) {
+    uint4 v[kQUnits];
 #pragma unroll
-  for (int t = 0; t < 8; ++t) m = fmaxf(m, fabsf(f[t]));
-  const float s = __fmul_rn(m, __fdiv_rn(1.f, 127.f));
-  uint32_t w[2] = {0u, 0u};
+    for (int i = 0; i < kQUnits; ++i) {
+      const int u = threadIdx.x + i * kQThreads;
+      if (u < units) v[i] = ld_nc_v4(a.ffn + row * H + 8 * (int64_t)u);
+    }
 #pragma unroll
-  for (int t = 0; t < 8; ++t) {
-    int c = __float2int_rn(__fdiv_rn(f[t], s));  // 0/0 is NaN, which converts to 0
-    c = max(-128, min(127, c));
-    w[t >> 2] |= ((uint32_t)c & 0xffu) << (8 * (t & 3));
+    for (int i = 0; i < kQUnits; ++i) {
+      const int u = threadIdx.x + i * kQThreads;
+      if (u >= units) continue;
+      float f[8];
+      unpack8<T>(v[i], f);
+      float m = 0.f;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) m = fmaxf(m, fabsf(f[t]));
+      const float s = __fmul_rn(m, __fdiv_rn(1.f, 127.f));
+      uint32_t w[2];
+      if (m == 0.f || s >= 1.17549435e-38f) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          w[h] = __byte_perm(
+              __byte_perm(q8_div_magic(f[4 * h], s), q8_div_magic(f[4 * h + 1], s), 0x0040),
+              __byte_perm(q8_div_magic(f[4 * h + 2], s), q8_div_magic(f[4 * h + 3], s), 0x0040),
+              0x5410);
+      } else {
+        // A subnormal or zero scale of a non-zero block: quotients may leave
+        // the int8 range and saturate.
+        w[0] = w[1] = 0u;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          int c = __float2int_rn(__fdiv_rn(f[t], s));
+          c = max(-128, min(127, c));
+          w[t >> 2] |= ((uint32_t)c & 0xffu) << (8 * (t & 3));
+        }
+      }
+      int8_t* dst = a.ffn_q + row * H + 8 * (int64_t)u;
+      asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(dst), "r"(w[0]), "r"(w[1]) : "memory");
+      a.ffn_scales[row * units + u] = s;
+    }
   }
-  int8_t* dst = a.ffn_q + row * H + 8 * (int64_t)u;
-  asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(dst), "r"(w[0]), "r"(w[1]) : "memory");
-  a.ffn_scales[row * (H >> 3) + u] = s;
 }
 
 // Number of SMs of the current device.
@@ -582,12 +618,18 @@ cudaError_t launch_combine_q8(const CombineArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_combine_quant(const CombineArgs& a, cudaStream_t s) {
-  const int units = a.d.H >> 3;
-  const int nchunk = (units + kThreads - 1) / kThreads;
-  const dim3 grid((unsigned)(a.d.R_max * nchunk));
+  static int blocks_per_sm = 0;  // the kernels' occupancy (the same for both types)
+  if (blocks_per_sm == 0) {
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &blocks_per_sm, combine_quant_kernel<BF16>, kQThreads, 0);
+    if (e != cudaSuccess) return e;
+  }
+  int64_t grid = (int64_t)sm_count() * blocks_per_sm;
+  if (grid > a.d.R_max) grid = a.d.R_max;
+  if (grid < 1) grid = 1;
   if (a.d.x_dtype == 1)
-    return launch_pdl(combine_quant_kernel<F16>, grid, dim3(kThreads), 0, s, a, nchunk);
-  return launch_pdl(combine_quant_kernel<BF16>, grid, dim3(kThreads), 0, s, a, nchunk);
+    return launch_pdl(combine_quant_kernel<F16>, dim3((unsigned)grid), dim3(kQThreads), 0, s, a);
+  return launch_pdl(combine_quant_kernel<BF16>, dim3((unsigned)grid), dim3(kQThreads), 0, s, a);
 }
 
 }  // namespace cq

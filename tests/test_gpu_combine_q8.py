@@ -84,3 +84,40 @@ def test_combine_quant_zero_rows():
     y = cq.combine_q8(cfg, codes, scales, out.assist_info, gh.dev(wl.expert_scales, torch.float32),
                       out_dtype=torch.float32)
     assert torch.count_nonzero(y) == 0
+
+
+@pytest.mark.parametrize("x_dtype", [0, 1])
+def test_combine_quant_extreme_blocks(x_dtype):
+    """Block quantiser on blocks that leave the ordinary case, every dispatched
+    row against the oracle bit for bit: all-zero and -0 blocks, NaN and +-inf
+    elements, subnormal blocks (the scale max * fl(1/127) underflows to a
+    subnormal or zero and the quotients saturate), huge values, and values
+    whose quotients sit on .5 ties."""
+    import combine_quant_gb300 as cq
+    wl = workloads.tiny(5, 2)
+    if x_dtype:
+        wl = workloads.as_fp16(wl)
+    cfg, out, status, _ = gh.gpu_dispatch(wl)
+    R = int(gh.host(cq.assist_views(cfg, out.assist_info)[2])[-1])
+    H = cfg.hidden
+    rng = np.random.default_rng(6)
+    f = rng.standard_normal((cfg.max_rows, H)).astype(np.float32)
+    f[0, :8] = 0.0
+    f[0, 8:16] = -0.0
+    f[0, 16:24] = 1.0
+    f[0, 17] = np.nan
+    f[0, 24:32] = 2.0
+    f[0, 25] = np.inf
+    f[0, 32:40] = -np.inf
+    f[0, 40:48] = np.nan
+    f[1, :64] *= 1e-39 if x_dtype == 0 else 1e-7   # subnormal in the 16-bit type
+    f[1, 64:72] = 3.0e38 if x_dtype == 0 else 60000.0
+    f[2, :8] = [127.0, 63.5, 0.5, 1.5, -0.5, -2.5, 31.75, 100.0]  # max 127: scale ~1, ties
+    f[2, 8:16] = [-127.0, 0.25, 64.25, -63.5, 126.5, 3.5, -4.5, 12.0]
+    bits = workloads.to_f16_bits(f) if x_dtype else workloads.to_bf16_bits(f)
+    rows = torch.from_numpy(bits).to(gh.DEV).view(cfg.token_dtype)
+    codes, scales = cq.combine_quant(cfg, rows, out.assist_info)
+    pc, ps = oracle.combine_quant_rows(bits[:R], x_dtype)
+    assert np.array_equal(gh.host(codes[:R]), pc), "int8 codes differ"
+    assert np.array_equal(gh.host(scales[:R]).view(np.uint32), ps.view(np.uint32)), \
+        "block scales differ"
