@@ -37,6 +37,7 @@ _FIELDS = (
     "ep_world_size", "moe_expert_num", "shared_expert_num", "shared_expert_rank_num",
     "zero_expert_num", "copy_expert_num", "const_expert_num", "max_bs", "topk", "hidden",
     "global_bs", "quant_mode", "expert_token_nums_type", "mask_ndim", "x_dtype", "smooth_kind",
+    "y_dtype",
 )
 
 
@@ -81,6 +82,8 @@ def lib() -> ctypes.CDLL:
         L.cqo_quant_row.restype = ctypes.c_int
         L.cqo_quant_row2.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P, P, P, P, P]
         L.cqo_quant_row2.restype = ctypes.c_int
+        L.cqo_quant_row3.argtypes = [ctypes.c_int32] * 4 + [P] * 5
+        L.cqo_quant_row3.restype = ctypes.c_int
         L.cqo_group_cols.argtypes = [cfgp]
         L.cqo_group_cols.restype = ctypes.c_int32
         L.cqo_f16_to_f32.argtypes = [ctypes.c_uint16]
@@ -100,13 +103,18 @@ def lib() -> ctypes.CDLL:
         L.cqo_e4m3_encode.restype = ctypes.c_uint8
         L.cqo_e4m3_decode.argtypes = [ctypes.c_uint8]
         L.cqo_e4m3_decode.restype = ctypes.c_float
+        L.cqo_e5m2_encode.argtypes = [ctypes.c_float]
+        L.cqo_e5m2_encode.restype = ctypes.c_uint8
+        L.cqo_e5m2_decode.argtypes = [ctypes.c_uint8]
+        L.cqo_e5m2_decode.restype = ctypes.c_float
         L.cqo_bf16_from_f32.argtypes = [ctypes.c_float]
         L.cqo_bf16_from_f32.restype = ctypes.c_uint16
         L.cqo_bf16_to_f32.argtypes = [ctypes.c_uint16]
         L.cqo_bf16_to_f32.restype = ctypes.c_float
         L.cqo_ceil_log2.argtypes = [ctypes.c_float]
         L.cqo_ceil_log2.restype = ctypes.c_int32
-        for name in ("cqo_e4m3_encode_n", "cqo_bf16_from_f32_n", "cqo_ceil_log2_n"):
+        for name in ("cqo_e4m3_encode_n", "cqo_e5m2_encode_n", "cqo_bf16_from_f32_n",
+                     "cqo_ceil_log2_n"):
             getattr(L, name).argtypes = [P, P, ctypes.c_int64]
             getattr(L, name).restype = None
         L.cqo_combine_quant_row.argtypes = [ctypes.c_int32, ctypes.c_int32, P, P, P]
@@ -206,18 +214,20 @@ def _scale_buffer(mode: int, H: int):
     return None
 
 
-def quant_row(mode: int, x_row_bits, smooth_row=None, x_dtype: int = 0, smooth_scalar=None):
+def quant_row(mode: int, x_row_bits, smooth_row=None, x_dtype: int = 0, smooth_scalar=None,
+              y_dtype: int = 0):
     """Quantise one 16-bit row (uint16 bit patterns of bf16, or fp16 when
     x_dtype == 1). Returns (codes, scale): scale is a float (mode 2), a
-    per-group float row (mode 3), an e8m0 byte row (modes 4, 5) or None."""
+    per-group float row (mode 3), an e8m0 byte row (modes 4, 5) or None.
+    y_dtype picks the fp8 code type of modes 3-5 (0 e4m3fn, 1 e5m2)."""
     x = _c(x_row_bits, np.uint16)
     H = x.shape[0]
     sm = _c(smooth_row, np.float32)
     sc = None if smooth_scalar is None else np.asarray([smooth_scalar], np.float32)
     codes = np.empty(H, code_dtype(mode))
     scale = _scale_buffer(mode, H)
-    rc = lib().cqo_quant_row2(mode, x_dtype, H, _ptr(x), _ptr(sm), _ptr(sc), _ptr(codes),
-                              _ptr(scale))
+    rc = lib().cqo_quant_row3(mode, x_dtype, y_dtype, H, _ptr(x), _ptr(sm), _ptr(sc),
+                              _ptr(codes), _ptr(scale))
     if rc != OK:
         raise ValueError(f"oracle quant_row failed: {rc}")
     return codes, (None if scale is None else (scale[0] if mode == 2 else scale))
@@ -311,6 +321,14 @@ def e4m3_decode(b: int) -> float:
     return float(lib().cqo_e4m3_decode(int(b)))
 
 
+def e5m2_encode(v: float) -> int:
+    return int(lib().cqo_e5m2_encode(float(v)))
+
+
+def e5m2_decode(b: int) -> float:
+    return float(lib().cqo_e5m2_decode(int(b)))
+
+
 def bf16_from_f32(f: float) -> int:
     return int(lib().cqo_bf16_from_f32(float(f)))
 
@@ -335,6 +353,13 @@ def e4m3_encode_array(v) -> np.ndarray:
     a = _c(v, np.float32).reshape(-1)
     out = np.empty(a.shape, np.uint8)
     lib().cqo_e4m3_encode_n(_ptr(a), _ptr(out), a.size)
+    return out
+
+
+def e5m2_encode_array(v) -> np.ndarray:
+    a = _c(v, np.float32).reshape(-1)
+    out = np.empty(a.shape, np.uint8)
+    lib().cqo_e5m2_encode_n(_ptr(a), _ptr(out), a.size)
     return out
 
 

@@ -78,6 +78,10 @@ int cqo_check_config(const cqo_config* c) {
   if (c->quant_mode < 0 || c->quant_mode > 5) return CQO_ERR_ARG;
   if (c->x_dtype != 0 && c->x_dtype != 1) return CQO_ERR_ARG;
   if (c->smooth_kind < 0 || c->smooth_kind > 2) return CQO_ERR_ARG;
+  /* y_dtype ([LLD] y_dtype: float8_e4m3fn or float8_e5m2 codes): the fp8
+   * type of modes 3-5; modes 0-2 have no choice (16-bit or int8). */
+  if (c->y_dtype != 0 && c->y_dtype != 1) return CQO_ERR_ARG;
+  if (c->y_dtype == 1 && c->quant_mode < 3) return CQO_ERR_ARG;
   return CQO_OK;
 }
 
@@ -193,6 +197,51 @@ uint8_t cqo_e4m3_encode(float v) {
   return sign | (uint8_t)code;
 }
 
+float cqo_e5m2_decode(uint8_t b) {
+  /* FP8 E5M2: 1 sign, 5 exponent bits with bias 15, 2 mantissa bits; the
+   * all-ones exponent holds infinity (mantissa 0) and NaN; largest finite
+   * 1.75 * 2^15 = 57344. */
+  int sign = b >> 7, e = (b >> 2) & 0x1f, m = b & 3;
+  float mag;
+  if (e == 31) {
+    mag = m == 0 ? INFINITY : NAN;
+  } else {
+    mag = (e == 0) ? ldexpf((float)m, -16) : ldexpf(1.0f + (float)m / 4.0f, e - 15);
+  }
+  return sign ? -mag : mag;
+}
+
+uint8_t cqo_e5m2_encode(float v) {
+  /* Round to nearest even; magnitudes beyond 57344 (infinity included)
+   * saturate to 57344 (satfinite); NaN maps to the NaN code 0x7f. */
+  if (isnan(v)) return 0x7f;
+  uint8_t sign = signbit(v) ? 0x80 : 0x00;
+  float a = fabsf(v);
+  if (a >= 57344.0f) return sign | 0x7b;
+  if (a < 0x1p-14f) {
+    /* Subnormal range: value = m * 2^-16, m = 0..3; m == 4 is the smallest
+     * normal, whose code is also 4. a * 65536 is exact. */
+    float m = rintf(a * 65536.0f);
+    return sign | (uint8_t)m;
+  }
+  int e;
+  frexpf(a, &e);                       /* a = f * 2^e, f in [0.5, 1) */
+  int ex = e - 1;                      /* unbiased exponent, -14..15 */
+  float t = ldexpf(a, -ex);            /* in [1, 2), exact */
+  float mq = rintf((t - 1.0f) * 4.0f); /* 0..4, ties to even */
+  if (mq == 4.0f) {
+    mq = 0.0f;
+    ex += 1;
+  }
+  int code = ((ex + 15) << 2) | (int)mq;
+  if (code > 0x7b) code = 0x7b; /* rounding up past 57344 saturates */
+  return sign | (uint8_t)code;
+}
+
+void cqo_e5m2_encode_n(const float* in, uint8_t* out, int64_t n) {
+  for (int64_t t = 0; t < n; ++t) out[t] = cqo_e5m2_encode(in[t]);
+}
+
 void cqo_e4m3_encode_n(const float* in, uint8_t* out, int64_t n) {
   for (int64_t t = 0; t < n; ++t) out[t] = cqo_e4m3_encode(in[t]);
 }
@@ -229,6 +278,18 @@ static uint16_t out16(int32_t dtype, float f) {
 
 int cqo_quant_row2(int32_t mode, int32_t dt, int32_t H, const uint16_t* x, const float* smooth,
                    const float* smooth_scalar, void* codes, void* scale) {
+  return cqo_quant_row3(mode, dt, 0, H, x, smooth, smooth_scalar, codes, scale);
+}
+
+int cqo_quant_row3(int32_t mode, int32_t dt, int32_t yt, int32_t H, const uint16_t* x,
+                   const float* smooth, const float* smooth_scalar, void* codes, void* scale) {
+  /* The fp8 code type of modes 3-5: its largest finite value (dst_type_max)
+   * and the exponent of that value (emax). */
+  if (yt != 0 && yt != 1) return CQO_ERR_ARG;
+  if (yt == 1 && mode < 3) return CQO_ERR_ARG;
+  const float fp8_max = yt ? 57344.0f : 448.0f; /* 1.75 * 2^15, 1.75 * 2^8 */
+  const int32_t emax = yt ? 15 : 8;
+  uint8_t (*fp8_encode)(float) = yt ? cqo_e5m2_encode : cqo_e4m3_encode;
   if (mode == 0) {
     /* quant_out = x: the 16-bit row travels unchanged. */
     memcpy(codes, x, (size_t)H * sizeof(uint16_t));
@@ -266,8 +327,8 @@ int cqo_quant_row2(int32_t mode, int32_t dt, int32_t H, const uint16_t* x, const
     *(float*)scale = 1.0f / s;
   } else if (mode == 3) {
     /* pergroup: the mode-2 formulas on each group of 128 values, into
-     * e4m3 (dst_type_max 448); one carried scale per group. An all-zero
-     * group gives codes 0 and scale 0. */
+     * the fp8 type (dst_type_max 448 for e4m3, 57344 for e5m2); one carried
+     * scale per group. An all-zero group gives codes 0 and scale 0. */
     uint8_t* q = (uint8_t*)codes;
     float* sc = (float*)scale;
     for (int32_t g = 0; g * 128 < H; ++g) {
@@ -277,16 +338,17 @@ int cqo_quant_row2(int32_t mode, int32_t dt, int32_t H, const uint16_t* x, const
         const float a = fabsf(xf[h]);
         if (a > amax) amax = a;
       }
-      const float s = 448.0f / amax;
+      const float s = fp8_max / amax;
       const float mult = amax == 0.0f ? 0.0f : s;
-      for (int32_t h = h0; h < h1; ++h) q[h] = cqo_e4m3_encode(xf[h] * mult);
+      for (int32_t h = h0; h < h1; ++h) q[h] = fp8_encode(xf[h] * mult);
       sc[g] = 1.0f / s;
     }
   } else {
     /* mode 4 (mx): shared_exp = floor(log2(max|x|)) - emax, emax = 8 for
-     *   e4m3 (448 = 1.75 * 2^8); an all-zero block uses the smallest scale;
-     * mode 5 (mx clip): shared_exp = ceil(log2(max(max|x|, 1e-4) / 448)).
-     * Both: quant_out = CastToFp8E4M3(x / 2^shared_exp), the block scale
+     *   e4m3 (448 = 1.75 * 2^8), 15 for e5m2 (57344 = 1.75 * 2^15); an
+     *   all-zero block uses the smallest scale;
+     * mode 5 (mx clip): shared_exp = ceil(log2(max(max|x|, 1e-4) / fp8_max)).
+     * Both: quant_out = CastToFp8(x / 2^shared_exp), the block scale
      * 2^shared_exp stored as e8m0 (shared_exp + 127), blocks of 32. */
     uint8_t* q = (uint8_t*)codes;
     uint8_t* sc = (uint8_t*)scale;
@@ -301,15 +363,15 @@ int cqo_quant_row2(int32_t mode, int32_t dt, int32_t H, const uint16_t* x, const
       }
       int32_t e;
       if (mode == 4) {
-        e = amax == 0.0f ? -127 : cqo_floor_log2(amax) - 8;
+        e = amax == 0.0f ? -127 : cqo_floor_log2(amax) - emax;
         if (e < -127) e = -127;
       } else {
         if (amax < 1e-4f) amax = 1e-4f;
-        e = cqo_ceil_log2(amax / 448.0f);
+        e = cqo_ceil_log2(amax / fp8_max);
       }
       for (int32_t h = h0; h < h1; ++h) {
         /* x / 2^e; 2^-e is a normal binary32 here, so ldexpf is exact. */
-        q[h] = cqo_e4m3_encode(ldexpf(xf[h], -e));
+        q[h] = fp8_encode(ldexpf(xf[h], -e));
       }
       sc[b] = (uint8_t)(e + 127);
     }
@@ -528,7 +590,8 @@ int64_t cqo_dispatch(const cqo_config* c, const uint16_t* x, const int32_t* expe
       codes = (uint8_t*)expand_x + row * H;
       scale = (uint8_t*)dynamic_scales + row * cols;
     }
-    int rc = cqo_quant_row2(c->quant_mode, c->x_dtype, H, xr, sm, sm_scalar, codes, scale);
+    int rc = cqo_quant_row3(c->quant_mode, c->x_dtype, c->y_dtype, H, xr, sm, sm_scalar, codes,
+                            scale);
     if (rc != CQO_OK) return rc;
     /* [DV3] expand_scales: the routing weight travels with its row; a shared
      * expert row carries weight 1 (its output is added unweighted). */

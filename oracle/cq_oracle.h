@@ -47,6 +47,7 @@ typedef struct cqo_config {
   int32_t x_dtype;                /* 0 = bf16, 1 = fp16 (x, ori_x, const_v, ffn rows, y) */
   int32_t smooth_kind;            /* scales shape: 0 = per expert rows [(S)+M, H],
                                      1 = one row [H] for every expert, 2 = one scalar */
+  int32_t y_dtype;                /* fp8 code type of modes 3-5: 0 = e4m3fn, 1 = e5m2 */
 } cqo_config;
 
 /* Return codes. */
@@ -95,6 +96,12 @@ int64_t cqo_route(const cqo_config* c, const int32_t* expert_ids, const uint8_t*
 int cqo_quant_row2(int32_t mode, int32_t x_dtype, int32_t hidden, const uint16_t* x_row,
                    const float* smooth_row, const float* smooth_scalar, void* codes,
                    void* scale);
+
+/* cqo_quant_row2 with the fp8 code type of modes 3-5 chosen by y_dtype
+ * (0 = e4m3fn, dst_type_max 448, emax 8; 1 = e5m2, 57344, emax 15). */
+int cqo_quant_row3(int32_t mode, int32_t x_dtype, int32_t y_dtype, int32_t hidden,
+                   const uint16_t* x_row, const float* smooth_row, const float* smooth_scalar,
+                   void* codes, void* scale);
 /* bf16 input, per-element smooth row or none (the original entry point). */
 int cqo_quant_row(int32_t mode, int32_t hidden, const uint16_t* x_row, const float* smooth_row,
                   void* codes, void* scale);
@@ -145,11 +152,14 @@ int cqo_combine_token_q8(const cqo_config* c, int32_t r, int32_t i, const int8_t
 /* Format helpers, exposed so the tests can pin them on their own. */
 uint8_t cqo_e4m3_encode(float v);  /* round to nearest even, saturate to +-448 */
 float cqo_e4m3_decode(uint8_t b);
+uint8_t cqo_e5m2_encode(float v);  /* round to nearest even, saturate to +-57344 */
+float cqo_e5m2_decode(uint8_t b);
 uint16_t cqo_bf16_from_f32(float f); /* round to nearest even */
 float cqo_bf16_to_f32(uint16_t b);
 int32_t cqo_ceil_log2(float q);     /* exact ceil(log2(q)) for finite q > 0 */
 /* Array forms of the helpers above (n elements). */
 void cqo_e4m3_encode_n(const float* in, uint8_t* out, int64_t n);
+void cqo_e5m2_encode_n(const float* in, uint8_t* out, int64_t n);
 void cqo_bf16_from_f32_n(const float* in, uint16_t* out, int64_t n);
 void cqo_ceil_log2_n(const float* in, int32_t* out, int64_t n);
 
