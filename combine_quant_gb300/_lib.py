@@ -15,6 +15,7 @@ CONFIG_FIELDS = (
     "ep_world_size", "moe_expert_num", "shared_expert_num", "shared_expert_rank_num",
     "zero_expert_num", "copy_expert_num", "const_expert_num", "max_bs", "topk", "hidden",
     "global_bs", "quant_mode", "expert_token_nums_type", "mask_ndim", "x_dtype", "smooth_kind",
+    "y_dtype",
 )
 
 CQ_OK = 0

@@ -35,6 +35,7 @@ class Config:
     mask_ndim: int = 0
     x_dtype: int = 0       # 0 bf16, 1 fp16
     smooth_kind: int = 0   # 0 per-expert rows, 1 one row for all experts, 2 one scalar
+    y_dtype: int = 0       # fp8 codes of modes 3-5: 0 e4m3fn, 1 e5m2
 
     @classmethod
     def from_dict(cls, d: dict) -> "Config":
@@ -85,7 +86,7 @@ class Config:
 
     def code_dtype(self) -> torch.dtype:
         return {0: self.token_dtype, 1: torch.int8, 2: torch.int8, 3: torch.uint8,
-                4: torch.uint8, 5: torch.uint8}[self.quant_mode]
+                4: torch.uint8, 5: torch.uint8}[self.quant_mode]  # fp8 codes as raw bytes
 
 
 @functools.lru_cache(maxsize=256)

@@ -38,6 +38,8 @@ int validate(const cq_config* c) {
   if (c->quant_mode < 0 || c->quant_mode > 5) return CQ_ERR_ARG;
   if (c->x_dtype != 0 && c->x_dtype != 1) return CQ_ERR_ARG;
   if (c->smooth_kind < 0 || c->smooth_kind > 2) return CQ_ERR_ARG;
+  if (c->y_dtype != 0 && c->y_dtype != 1) return CQ_ERR_ARG;
+  if (c->y_dtype == 1 && c->quant_mode < 3) return CQ_ERR_ARG;  // e5m2 codes: modes 3-5
   // Vector paths: 16-element units (16-byte stores of int8 / e4m3 rows); mx
   // blocks of 32 never straddle two threads' units.
   if (c->hidden % 16 != 0) return CQ_ERR_UNSUPPORTED;
@@ -66,6 +68,7 @@ Dims dims_of(const cq_config* c) {
   d.etn_type = c->expert_token_nums_type;
   d.mask_ndim = c->mask_ndim;
   d.x_dtype = c->x_dtype;
+  d.y_dtype = c->y_dtype;
   const int32_t blocks = (d.H + 31) / 32;
   d.SC = (blocks + 1) / 2 * 2;
   d.G3 = (d.H + 127) / 128;

@@ -18,6 +18,7 @@ struct Dims {
   int32_t Z, C, Q, BS, K, H, L, NS, G;  // G = S_r + M global expert slots
   int32_t mode, etn_type, mask_ndim;
   int32_t x_dtype;                // 0 bf16, 1 fp16
+  int32_t y_dtype;                // fp8 codes of modes 3-5: 0 e4m3fn, 1 e5m2
   int32_t SC;                     // mx scale columns: Align2(Ceil(H, 32))
   int32_t G3;                     // mode-3 groups per row: Ceil(H, 128)
   int64_t R_max;

@@ -164,6 +164,18 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
   return r;
 }
 
+// The same into two e5m2 bytes, saturating to +-57344.
+__device__ __forceinline__ uint32_t e5m2x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Quantisation variant Q: quant_mode Q % 10; Q >= 10 selects e5m2 codes for
+// modes 3-5 (e4m3fn otherwise).
+__host__ __device__ constexpr int q_mode(int q) { return q % 10; }
+__host__ __device__ constexpr bool q_e5m2(int q) { return q >= 10; }
+
 // Exact ceil(log2(q)) for a positive normal binary32 q.
 __device__ __forceinline__ int ceil_log2_bits(float q) {
   const uint32_t b = __float_as_uint(q);
@@ -233,12 +245,18 @@ __device__ __forceinline__ uint4 q8_16_magic(const float (&v)[16], float m) {
                     q8x4_magic(v[12], v[13], v[14], v[15], m));
 }
 
-__device__ __forceinline__ uint4 e4m3_16(const float (&v)[16], float mult) {
+template <bool E5>
+__device__ __forceinline__ uint32_t fp8x2(float lo, float hi) {
+  return E5 ? e5m2x2(lo, hi) : e4m3x2(lo, hi);
+}
+
+template <bool E5>
+__device__ __forceinline__ uint4 fp8_16(const float (&v)[16], float mult) {
   uint32_t o[4];
 #pragma unroll
   for (int t = 0; t < 4; ++t)
-    o[t] = e4m3x2(__fmul_rn(v[4 * t], mult), __fmul_rn(v[4 * t + 1], mult)) |
-           (e4m3x2(__fmul_rn(v[4 * t + 2], mult), __fmul_rn(v[4 * t + 3], mult)) << 16);
+    o[t] = fp8x2<E5>(__fmul_rn(v[4 * t], mult), __fmul_rn(v[4 * t + 1], mult)) |
+           (fp8x2<E5>(__fmul_rn(v[4 * t + 2], mult), __fmul_rn(v[4 * t + 3], mult)) << 16);
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
@@ -304,9 +322,14 @@ __device__ __forceinline__ void put16(uint8_t* p, uint4 v) {
   }
 }
 
-template <int MODE, bool GLOBAL = false>
+template <int Q, bool GLOBAL = false>
 __device__ __forceinline__ float quantise(const float (&f)[2][16], const Units& U,
                                           uint8_t* codes, uint8_t* scales, float* red) {
+  constexpr int MODE = q_mode(Q);
+  constexpr bool E5 = q_e5m2(Q);
+  // The fp8 type's largest value and its exponent (emax).
+  constexpr float kFp8Max = E5 ? 57344.f : 448.f;
+  constexpr int kEmax = E5 ? 15 : 8;
   float carried = 0.f;
   if (MODE == 1) {
 #pragma unroll
@@ -337,11 +360,11 @@ __device__ __forceinline__ float quantise(const float (&f)[2][16], const Units& 
       m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
       m = fmaxf(m, __shfl_xor_sync(kFull, m, 2));
       m = fmaxf(m, __shfl_xor_sync(kFull, m, 4));
-      const float s = __fdiv_rn(448.f, m);
+      const float s = __fdiv_rn(kFp8Max, m);
       const float mult = m == 0.f ? 0.f : s;  // an all-zero group: codes 0, scale 0
       const int u = threadIdx.x + q * blockDim.x;
       if (U.ok[q]) {
-        put16<GLOBAL>(codes + 16 * u, e4m3_16(f[q], mult));
+        put16<GLOBAL>(codes + 16 * u, fp8_16<E5>(f[q], mult));
         if ((u & 7) == 0) reinterpret_cast<float*>(scales)[u >> 3] = __fdiv_rn(1.f, s);
       }
     }
@@ -353,13 +376,13 @@ __device__ __forceinline__ float quantise(const float (&f)[2][16], const Units& 
       m = fmaxf(m, __shfl_xor_sync(kFull, m, 1));
       int e;
       if (MODE == 4) {
-        e = m == 0.f ? -127 : max(floor_log2_bits(m) - 8, -127);  // emax(e4m3) = 8
+        e = m == 0.f ? -127 : max(floor_log2_bits(m) - kEmax, -127);
       } else {
-        e = ceil_log2_bits(__fdiv_rn(fmaxf(m, 1e-4f), 448.f));
+        e = ceil_log2_bits(__fdiv_rn(fmaxf(m, 1e-4f), kFp8Max));
       }
       const int u = threadIdx.x + q * blockDim.x;
       if (U.ok[q]) {
-        put16<GLOBAL>(codes + 16 * u, e4m3_16(f[q], pow2(-e)));  // x / 2^e, exact scaling
+        put16<GLOBAL>(codes + 16 * u, fp8_16<E5>(f[q], pow2(-e)));  // x / 2^e, exact scaling
         if ((u & 1) == 0) scales[u >> 1] = (uint8_t)(e + 127);
       }
     }
@@ -410,9 +433,10 @@ __device__ __forceinline__ int map_slot(const PermuteArgs& a, int64_t tok, int r
 }
 
 // Token-major permute for every smooth shape but per-expert rows.
-// T: token type; MODE: quant_mode; SM: SmoothKind.
-template <class T, int MODE, int SM>
+// T: token type; Q: quantisation variant (q_mode, q_e5m2); SM: SmoothKind.
+template <class T, int Q, int SM>
 __global__ void __launch_bounds__(256) permute_kernel(PermuteArgs a) {
+  constexpr int MODE = q_mode(Q);
   __shared__ int s_row[kMaxSlots];   // compact list of routed rows
   __shared__ int s_srow[kMaxSlots];  // their smooth-table rows
   __shared__ int s_nrows;
@@ -513,7 +537,7 @@ __global__ void __launch_bounds__(256) permute_kernel(PermuteArgs a) {
         for (int t = 0; t < 16; ++t) f[q][t] = 0.f;
       }
     }
-    const float carried = quantise<MODE>(f, U, s_stage, s_stage + code_bytes, s_red[0]);
+    const float carried = quantise<Q>(f, U, s_stage, s_stage + code_bytes, s_red[0]);
     if (MODE == 5 || MODE == 4) {
       if (threadIdx.x == 0 && d.SC > (units >> 1)) s_stage[code_bytes + (units >> 1)] = 0;
     }
@@ -573,8 +597,9 @@ __global__ void __launch_bounds__(256) index_kernel(PermuteArgs a) {
   griddep_launch_dependents();
 }
 
-template <class T, int MODE>
+template <class T, int Q>
 __global__ void __launch_bounds__(256, 2) smooth_rows_kernel(PermuteArgs a) {
+  constexpr int MODE = q_mode(Q);
   __shared__ uint64_t s_bar[kXStages];
   __shared__ int s_srow[kXStages];
   __shared__ float s_red[2][32];
@@ -678,7 +703,7 @@ __global__ void __launch_bounds__(256, 2) smooth_rows_kernel(PermuteArgs a) {
     // it every thread has read ring slot st.
     if (MODE != 2) __syncthreads();
     const float carried =
-        quantise<MODE, true>(f, U, out + row * H, dyn + row * scale_bytes, s_red[j & 1]);
+        quantise<Q, true>(f, U, out + row * H, dyn + row * scale_bytes, s_red[j & 1]);
     if (s_fail) break;  // set only before the barrier above: the same in all threads
     if (threadIdx.x == 0) {
       if (MODE == 2) reinterpret_cast<float*>(dyn)[row] = carried;
@@ -712,8 +737,9 @@ inline int sm_count() {
 
 // The per-expert-smooth path: index_kernel, then smooth_rows_kernel with one
 // wave of CTAs (SMs x resident CTAs per SM).
-template <class T, int MODE>
+template <class T, int Q>
 cudaError_t launch_smooth_rows(const PermuteArgs& a, cudaStream_t s) {
+  constexpr int MODE = q_mode(Q);
   const int64_t tokens = (int64_t)a.d.W * a.d.BS;
   cudaError_t e =
       launch_pdl(index_kernel<T>, dim3((unsigned)((tokens + 7) / 8)), dim3(256), 0, s, a);
@@ -722,8 +748,8 @@ cudaError_t launch_smooth_rows(const PermuteArgs& a, cudaStream_t s) {
   int threads = ((units + 1) / 2 + 31) / 32 * 32;
   if (threads < 32) threads = 32;
   const size_t smem = (size_t)kXStages * 2 * a.d.H;
-  auto* kern = smooth_rows_kernel<T, MODE>;
-  if ((e = prepare_kernel<smooth_rows_kernel<T, MODE>>(smem)) != cudaSuccess) return e;
+  auto* kern = smooth_rows_kernel<T, Q>;
+  if ((e = prepare_kernel<smooth_rows_kernel<T, Q>>(smem)) != cudaSuccess) return e;
   // The last occupancy query of this instantiation.
   static std::mutex mu;
   static size_t occ_smem = 0;
@@ -746,8 +772,9 @@ cudaError_t launch_smooth_rows(const PermuteArgs& a, cudaStream_t s) {
   return launch_pdl(kern, dim3((unsigned)grid), dim3(threads), smem, s, a);
 }
 
-template <class T, int MODE, int SM>
+template <class T, int Q, int SM>
 cudaError_t launch_one(const PermuteArgs& a, cudaStream_t s) {
+  constexpr int MODE = q_mode(Q);
   const int units = a.d.H >> 4;
   int threads = ((units + 1) / 2 + 31) / 32 * 32;
   if (threads < 32) threads = 32;
@@ -756,9 +783,18 @@ cudaError_t launch_one(const PermuteArgs& a, cudaStream_t s) {
   const size_t scale_bytes =
       MODE == 3 ? 4 * (size_t)a.d.G3 : ((MODE == 4 || MODE == 5) ? (size_t)a.d.SC : 0);
   const size_t smem = code_bytes + ((scale_bytes + 15) & ~size_t(15));
-  const cudaError_t e = prepare_kernel<permute_kernel<T, MODE, SM>>(smem);
+  const cudaError_t e = prepare_kernel<permute_kernel<T, Q, SM>>(smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(permute_kernel<T, MODE, SM>, dim3((unsigned)grid), dim3(threads), smem, s, a);
+  return launch_pdl(permute_kernel<T, Q, SM>, dim3((unsigned)grid), dim3(threads), smem, s, a);
+}
+
+// Per-128-group fp8 (Q = 3 e4m3fn, 13 e5m2) for each smooth shape.
+template <class T, int Q>
+cudaError_t launch_mode3(const PermuteArgs& a, cudaStream_t s, int sm) {
+  if (sm == kRowPerSlot) return launch_smooth_rows<T, Q>(a, s);
+  if (sm == kSharedRow) return launch_one<T, Q, kSharedRow>(a, s);
+  if (sm == kScalar) return launch_one<T, Q, kScalar>(a, s);
+  return launch_one<T, Q, kNoSmooth>(a, s);
 }
 
 // Choose the instantiation for the call's mode and smooth shape.
@@ -778,13 +814,11 @@ cudaError_t launch_typed(const PermuteArgs& a, cudaStream_t s) {
       if (sm == kSharedRow) return launch_one<T, 2, kSharedRow>(a, s);
       if (sm == kScalar) return launch_one<T, 2, kScalar>(a, s);
       return launch_one<T, 2, kNoSmooth>(a, s);
-    case 3:
-      if (sm == kRowPerSlot) return launch_smooth_rows<T, 3>(a, s);
-      if (sm == kSharedRow) return launch_one<T, 3, kSharedRow>(a, s);
-      if (sm == kScalar) return launch_one<T, 3, kScalar>(a, s);
-      return launch_one<T, 3, kNoSmooth>(a, s);
-    case 4: return launch_one<T, 4, kNoSmooth>(a, s);
-    case 5: return launch_one<T, 5, kNoSmooth>(a, s);
+    case 3: return a.d.y_dtype ? launch_mode3<T, 13>(a, s, sm) : launch_mode3<T, 3>(a, s, sm);
+    case 4:
+      return a.d.y_dtype ? launch_one<T, 14, kNoSmooth>(a, s) : launch_one<T, 4, kNoSmooth>(a, s);
+    case 5:
+      return a.d.y_dtype ? launch_one<T, 15, kNoSmooth>(a, s) : launch_one<T, 5, kNoSmooth>(a, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -59,13 +59,16 @@ typedef struct cq_config {
                                      (H % 32 == 0 for quant_mode 5) */
   int32_t global_bs;              /* 0 or BS * W ([DV3] global_bs) */
   int32_t quant_mode;             /* 0 none, 1 static int8, 2 per-token int8, 3 per-128-group
-                                     e4m3, 4 mx e4m3, 5 mx-clip e4m3 ([LLD] 计算公式) */
+                                     fp8, 4 mx fp8, 5 mx-clip fp8 ([LLD] 计算公式) */
   int32_t expert_token_nums_type; /* 0 cumulative sums, 1 counts */
   int32_t mask_ndim;              /* 0 none, 1 per token [W,BS], 2 per pair [W,BS,K] */
   int32_t x_dtype;                /* 0 bf16, 1 fp16: x, ori_x, const_v, expert outputs, y */
   int32_t smooth_kind;            /* shape of smooth_scales ("scales"): 0 one row per expert
                                      [(S_r>0 ? S : 0) + M, H], 1 one row [H] for every
                                      expert, 2 one scalar [1] */
+  int32_t y_dtype;                /* fp8 code type of modes 3-5 ([LLD] y_dtype): 0 e4m3fn
+                                     (largest value 448, emax 8), 1 e5m2 (57344, emax 15);
+                                     must be 0 in modes 0-2 */
 } cq_config;
 
 enum {
@@ -129,7 +132,8 @@ int cq_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
  *                  then unused)
  * Outputs (rows past the true total are left untouched):
  *   expand_x       [R_max, H]: the token type (mode 0), int8 (modes 1, 2),
- *                  e4m3 bytes (modes 3, 4, 5). Rank d's rows, expert-contiguous
+ *                  fp8 bytes (modes 3, 4, 5: e4m3fn, or e5m2 when y_dtype is 1).
+ *                  Rank d's rows, expert-contiguous
  *                  (local expert ascending, then source rank ascending, then
  *                  arrival order).
  *   dynamic_scales dequantisation multipliers: f32 [R_max] (mode 2), f32

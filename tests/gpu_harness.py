@@ -87,7 +87,7 @@ def compare_rows(wl, out, ref_route, sample):
         src, tok, k = ref_route.assist[row, :3]
         sm_row, sm_scalar = smooth_args(wl, src, tok, k)
         codes, scale = oracle.quant_row(mode, wl.x[src, tok], sm_row, wl.cfg.get("x_dtype", 0),
-                                        sm_scalar)
+                                        sm_scalar, wl.cfg.get("y_dtype", 0))
         assert np.array_equal(ex[n].view(codes.dtype), codes), f"expand_x row {row}"
         if mode == 2:
             assert dyn[n] == scale, f"dynamic_scales row {row}"

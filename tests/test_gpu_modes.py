@@ -118,3 +118,39 @@ def test_mode2_nonfinite_and_extreme_rows(kind):
         gh.full_parity(_with(wl, 2))
     else:
         gh.full_parity(_with(wl, 2, _smooth(wl, kind), kind))
+
+
+def _e5(wl, mode, smooth=None, kind=0):
+    w = _with(wl, mode, smooth, kind)
+    w.cfg["y_dtype"] = 1
+    return w
+
+
+@pytest.mark.parametrize("base", ["tiny", "dsv3_small", "h1040"])
+@pytest.mark.parametrize("kind", [None, 0, 1, 2])
+def test_mode3_e5m2(base, kind):
+    """Per-128-group e5m2 codes (y_dtype 1, dst_type_max 57344), with every
+    smooth shape (kind 0 runs the expert-major per-expert-smooth kernel)."""
+    wl = _base(base)
+    gh.full_parity(_e5(wl, 3) if kind is None else _e5(wl, 3, _smooth(wl, kind), kind))
+
+
+@pytest.mark.parametrize("mode", [4, 5])
+@pytest.mark.parametrize("base", ["tiny", "dsv3_small", "special_small"])
+def test_mx_e5m2(mode, base):
+    """mx e5m2 codes (emax 15; clip against 57344)."""
+    gh.full_parity(_e5(_base(base), mode))
+
+
+@pytest.mark.parametrize("mode", [3, 4, 5])
+def test_e5m2_extremes_and_fp16(mode):
+    wl = _e5(workloads.tiny(4, 2), mode)
+    x = workloads.bf16_bits_to_f32(wl.x).copy()
+    x[0, 0] = 0.0
+    x[0, 1, :64] = 57344.0
+    x[1, 2] *= 1e-38
+    x[2, 3] *= 1e30
+    x[3, 4, 5] = np.nan
+    wl.x = workloads.to_bf16_bits(x)
+    gh.full_parity(wl)
+    gh.full_parity(workloads.as_fp16(_e5(_base("tiny"), mode)))
