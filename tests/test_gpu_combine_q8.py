@@ -19,10 +19,12 @@ def _case(name):
         "special_small": lambda: workloads.special(seed=23, W=8, BS=20, H=1024, M=48),
         "skew_small": lambda: workloads.skew(seed=24, W=4, BS=64, M=32, K=16, H=2048),
         "dsv3": lambda: workloads.dsv3(),
+        # H % 32 != 0: the direct-gather combine instead of the staged one
+        "h1040": lambda: workloads.dsv3(seed=25, W=4, BS=9, M=16, K=4, H=1040),
     }[name]()
 
 
-@pytest.mark.parametrize("name", ["tiny", "special_small", "skew_small", "dsv3"])
+@pytest.mark.parametrize("name", ["tiny", "special_small", "skew_small", "dsv3", "h1040"])
 def test_combine_q8_parity(name):
     import combine_quant_gb300 as cq
     wl = _case(name)
