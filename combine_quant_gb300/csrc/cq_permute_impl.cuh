@@ -196,13 +196,27 @@ __device__ __forceinline__ float pow2(int k) { return __uint_as_float((uint32_t)
 
 // max(0, |v_t|) over the 16 values, NaN ignored, as a balanced tree (max is
 // exact and associative; the final max with 0 turns an all-NaN unit into 0).
+// Three-operand max: NaN operands ignored, or (NAN) propagated.
+template <bool NAN_OUT = false>
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  if (NAN_OUT) {
+    asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  } else {
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  }
+  return r;
+}
+// max(0, |v_t|) over 16 values; NaN values are ignored, or (NAN_OUT) make the
+// result NaN. Max is exact, so the order of the tree does not matter.
+template <bool NAN_OUT = false>
 __device__ __forceinline__ float max16(const float (&v)[16]) {
-  float m[8];
+  float m[5];
 #pragma unroll
-  for (int t = 0; t < 8; ++t) m[t] = fmaxf(fabsf(v[t]), fabsf(v[t + 8]));
-#pragma unroll
-  for (int t = 0; t < 4; ++t) m[t] = fmaxf(m[t], m[t + 4]);
-  return fmaxf(fmaxf(fmaxf(m[0], m[2]), fmaxf(m[1], m[3])), 0.f);
+  for (int t = 0; t < 5; ++t)
+    m[t] = max3<NAN_OUT>(fabsf(v[3 * t]), fabsf(v[3 * t + 1]), fabsf(v[3 * t + 2]));
+  return max3<NAN_OUT>(max3<NAN_OUT>(m[0], m[1], m[2]), max3<NAN_OUT>(m[3], m[4], fabsf(v[15])),
+                       0.f);
 }
 
 __device__ __forceinline__ uint4 q8_16(const float (&v)[16], float s) {
@@ -223,15 +237,29 @@ __device__ __forceinline__ uint4 q8_16_direct(const float (&v)[16]) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// Four int8 codes RNE(fl(v * m)) for products that are NaN or lie in
-// [-128, 128]; a NaN product gives 0. Clamping from below at -256 maps NaN to
-// -256 (max ignores NaN) and leaves the others alone; adding 1.5 * 2^23 then
-// gives a sum whose ulp is 1, so its low mantissa bits hold the nearest-even
-// integer n, and the low byte of its bit pattern is n in two's complement
-// (-256 -> 0). Three byte permutes pack the four codes.
+// Two binary32 products in one packed instruction, each lane rounded to
+// nearest even on its own (the same results as two scalar _rn products). Use
+// only where no add follows the product: ptxas may fuse a packed multiply
+// and a packed add into one multiply-add with a single rounding.
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  float2 r;
+  asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mul.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return r;
+}
+
+// Four int8 codes RNE(fl(v * m)) for products that lie in [-128, 128]:
+// adding 1.5 * 2^23 gives a sum whose ulp is 1, so its low mantissa bits
+// hold the nearest-even integer n, and the low byte of its bit pattern is n
+// in two's complement. Three byte permutes pack the four codes.
+// The product and the add are scalar _rn operations, which are never fused:
+// a fused multiply-add would round x * m once, straight to an integer, and
+// differ from RNE(fl(x * m)) where fl(x * m) is an exact tie (ptxas does
+// contract the packed f32x2 forms).
 __device__ __forceinline__ uint32_t q8_magic(float v, float m) {
-  constexpr float kMagic = 12582912.f;  // 1.5 * 2^23
-  return __float_as_uint(__fadd_rn(fmaxf(__fmul_rn(v, m), -256.f), kMagic));
+  return __float_as_uint(__fadd_rn(__fmul_rn(v, m), 12582912.f));  // + 1.5 * 2^23
 }
 
 __device__ __forceinline__ uint32_t q8x4_magic(float a, float b, float c, float d, float m) {
@@ -260,19 +288,20 @@ __device__ __forceinline__ uint4 fp8_16(const float (&v)[16], float mult) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// Block-wide max of one float per thread, for blocks of at most 256 threads
-// (8 warps); `buf` holds >= 8 floats and must not be reused by another
-// block_max until the next __syncthreads.
+// Block-wide max of one float per thread (NaN-propagating when NAN_OUT), for
+// blocks of at most 256 threads (8 warps); `buf` holds >= 8 floats and must
+// not be reused by another block_max until the next __syncthreads.
+template <bool NAN_OUT = false>
 __device__ __forceinline__ float block_max(float v, float* buf) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+  for (int o = 16; o > 0; o >>= 1) v = max3<NAN_OUT>(v, __shfl_xor_sync(kFull, v, o), v);
   const int lane = threadIdx.x & 31;
   if (lane == 0) buf[threadIdx.x >> 5] = v;
   __syncthreads();
   // Every group of 8 lanes reduces the same (up to) 8 warp maxima.
   float m = (lane & 7) < (int)(blockDim.x >> 5) ? buf[lane & 7] : 0.f;
 #pragma unroll
-  for (int o = 4; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o));
+  for (int o = 4; o > 0; o >>= 1) m = max3<NAN_OUT>(m, __shfl_xor_sync(kFull, m, o), m);
   return m;
 }
 
@@ -311,7 +340,7 @@ __device__ __forceinline__ void unit_values(const uint4 (&u)[2], const float* sr
 // Quantise this thread's two units of one row: codes at 16 bytes per unit in
 // `codes` (shared staging, or the global row when GLOBAL), the per-group (mode 3, floats) or
 // per-block (modes 4/5, e8m0 bytes) scales in `scales`. Mode 2 returns the
-// row's carried scale in the threads of warp 0. `red` is a block_max buffer (mode 2 only).
+// row's carried scale in the threads of warp 0. `red` holds 64 floats (mode 2 only).
 // 16 code bytes to shared (staging) or, when GLOBAL, straight to global memory.
 template <bool GLOBAL>
 __device__ __forceinline__ void put16(uint8_t* p, uint4 v) {
@@ -336,18 +365,21 @@ __device__ __forceinline__ float quantise(const float (&f)[2][16], const Units& 
     for (int q = 0; q < 2; ++q)
       if (U.ok[q]) put16<GLOBAL>(codes + 16 * (threadIdx.x + q * blockDim.x), q8_16_direct(f[q]));
   } else if (MODE == 2) {
-    const float amax = block_max(fmaxf(max16(f[0]), max16(f[1])), red);
+    // The row max with NaN propagated. A row with neither NaN nor infinity
+    // whose 127/max is finite (or whose max is 0) has every product x * s in
+    // [-127, 127]: add-and-pack rounding. Any other row takes the
+    // convert-and-saturate path with the scale from the NaN-ignoring max.
+    float amax = block_max<true>(max3<true>(max16<true>(f[0]), max16<true>(f[1]), 0.f), red);
+    const bool clean = amax <= 3.402823466e38f;  // false for NaN and +inf
+    if (!clean) amax = block_max(fmaxf(max16(f[0]), max16(f[1])), red + 32);  // block-uniform
     const float s = __fdiv_rn(127.f, amax);  // +inf for an all-zero row: codes 0, carried 0
     if (threadIdx.x < 32) carried = __fdiv_rn(1.f, s);  // only warp 0 stores it
-    if (s <= 3.402823466e38f || amax == 0.f) {
-      // Every product is in [-127, 127] (|x| <= max, s rounded), or NaN (a
-      // NaN element; inf * 0 when the max is infinite): add-and-pack rounding.
+    if (clean && (s <= 3.402823466e38f || amax == 0.f)) {
       const float mult = amax == 0.f ? 0.f : s;
 #pragma unroll
       for (int q = 0; q < 2; ++q)
         if (U.ok[q]) put16<GLOBAL>(codes + 16 * (threadIdx.x + q * blockDim.x), q8_16_magic(f[q], mult));
     } else {
-      // 127 / max overflowed (max below about 3.7e-37): saturating conversion.
 #pragma unroll
       for (int q = 0; q < 2; ++q)
         if (U.ok[q]) put16<GLOBAL>(codes + 16 * (threadIdx.x + q * blockDim.x), q8_16(f[q], s));
@@ -440,7 +472,7 @@ __global__ void __launch_bounds__(256) permute_kernel(PermuteArgs a) {
   __shared__ int s_row[kMaxSlots];   // compact list of routed rows
   __shared__ int s_srow[kMaxSlots];  // their smooth-table rows
   __shared__ int s_nrows;
-  __shared__ float s_red[2][32];
+  __shared__ float s_red[2][64];
   extern __shared__ __align__(128) uint8_t s_stage[];  // staged code row(s) + scale row(s)
 
   const Dims& d = a.d;
@@ -602,7 +634,7 @@ __global__ void __launch_bounds__(256, 2) smooth_rows_kernel(PermuteArgs a) {
   constexpr int MODE = q_mode(Q);
   __shared__ uint64_t s_bar[kXStages];
   __shared__ int s_srow[kXStages];
-  __shared__ float s_red[2][32];
+  __shared__ float s_red[2][64];
   __shared__ int s_fail;
   extern __shared__ __align__(128) uint8_t s_ring[];  // kXStages token rows
 
@@ -694,8 +726,10 @@ __global__ void __launch_bounds__(256, 2) smooth_rows_kernel(PermuteArgs a) {
       const uint32_t* wv = reinterpret_cast<const uint32_t*>(w);
 #pragma unroll
       for (int t = 0; t < 8; ++t) {
-        f[q][2 * t] = __fmul_rn(T::lo(wv[t]), sm[q][2 * t]);
-        f[q][2 * t + 1] = __fmul_rn(T::hi(wv[t]), sm[q][2 * t + 1]);
+        const float2 p = mul2(make_float2(T::lo(wv[t]), T::hi(wv[t])),
+                              make_float2(sm[q][2 * t], sm[q][2 * t + 1]));
+        f[q][2 * t] = p.x;
+        f[q][2 * t + 1] = p.y;
       }
     }
     const int64_t row = lo + j;
