@@ -28,6 +28,7 @@
 #include <cuda_fp16.h>
 
 #include <atomic>
+#include <climits>
 #include <mutex>
 
 #include "cq_internal.cuh"
@@ -89,6 +90,9 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 }
 __device__ __forceinline__ void mbar_fence_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 // The producer's one arrival, announcing `bytes` of bulk copies.
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
@@ -288,18 +292,24 @@ __device__ __forceinline__ uint4 fp8_16(const float (&v)[16], float mult) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// Block-wide max of one float per thread (NaN-propagating when NAN_OUT), for
-// blocks of at most 256 threads (8 warps); `buf` holds >= 8 floats and must
-// not be reused by another block_max until the next __syncthreads.
-template <bool NAN_OUT = false>
-__device__ __forceinline__ float block_max(float v, float* buf) {
+// Max of one float per thread over the first nt threads of the block
+// (NaN-propagating when NAN_OUT); nt is a multiple of 32, at most 256 (8
+// warps). The threads meet at __syncthreads, or (NAMED, when other warps of
+// the block do not take part) at named barrier 1. `buf` holds >= 8 floats and
+// must not be reused by another block_max until the next such barrier.
+template <bool NAN_OUT = false, bool NAMED = false>
+__device__ __forceinline__ float block_max(float v, float* buf, int nt) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = max3<NAN_OUT>(v, __shfl_xor_sync(kFull, v, o), v);
   const int lane = threadIdx.x & 31;
   if (lane == 0) buf[threadIdx.x >> 5] = v;
-  __syncthreads();
+  if (NAMED) {
+    asm volatile("bar.sync 1, %0;" ::"r"(nt) : "memory");
+  } else {
+    __syncthreads();
+  }
   // Every group of 8 lanes reduces the same (up to) 8 warp maxima.
-  float m = (lane & 7) < (int)(blockDim.x >> 5) ? buf[lane & 7] : 0.f;
+  float m = (lane & 7) < (nt >> 5) ? buf[lane & 7] : 0.f;
 #pragma unroll
   for (int o = 4; o > 0; o >>= 1) m = max3<NAN_OUT>(m, __shfl_xor_sync(kFull, m, o), m);
   return m;
@@ -340,7 +350,8 @@ __device__ __forceinline__ void unit_values(const uint4 (&u)[2], const float* sr
 // Quantise this thread's two units of one row: codes at 16 bytes per unit in
 // `codes` (shared staging, or the global row when GLOBAL), the per-group (mode 3, floats) or
 // per-block (modes 4/5, e8m0 bytes) scales in `scales`. Mode 2 returns the
-// row's carried scale in the threads of warp 0. `red` holds 64 floats (mode 2 only).
+// row's carried scale in the threads of warp 0. `red` holds 64 floats (mode 2
+// only). nt threads share the row; NAMED as for block_max.
 // 16 code bytes to shared (staging) or, when GLOBAL, straight to global memory.
 template <bool GLOBAL>
 __device__ __forceinline__ void put16(uint8_t* p, uint4 v) {
@@ -351,9 +362,9 @@ __device__ __forceinline__ void put16(uint8_t* p, uint4 v) {
   }
 }
 
-template <int Q, bool GLOBAL = false>
+template <int Q, bool GLOBAL = false, bool NAMED = false>
 __device__ __forceinline__ float quantise(const float (&f)[2][16], const Units& U,
-                                          uint8_t* codes, uint8_t* scales, float* red) {
+                                          uint8_t* codes, uint8_t* scales, float* red, int nt) {
   constexpr int MODE = q_mode(Q);
   constexpr bool E5 = q_e5m2(Q);
   // The fp8 type's largest value and its exponent (emax).
@@ -363,26 +374,27 @@ __device__ __forceinline__ float quantise(const float (&f)[2][16], const Units& 
   if (MODE == 1) {
 #pragma unroll
     for (int q = 0; q < 2; ++q)
-      if (U.ok[q]) put16<GLOBAL>(codes + 16 * (threadIdx.x + q * blockDim.x), q8_16_direct(f[q]));
+      if (U.ok[q]) put16<GLOBAL>(codes + 16 * (threadIdx.x + q * nt), q8_16_direct(f[q]));
   } else if (MODE == 2) {
     // The row max with NaN propagated. A row with neither NaN nor infinity
     // whose 127/max is finite (or whose max is 0) has every product x * s in
     // [-127, 127]: add-and-pack rounding. Any other row takes the
     // convert-and-saturate path with the scale from the NaN-ignoring max.
-    float amax = block_max<true>(max3<true>(max16<true>(f[0]), max16<true>(f[1]), 0.f), red);
+    float amax =
+        block_max<true, NAMED>(max3<true>(max16<true>(f[0]), max16<true>(f[1]), 0.f), red, nt);
     const bool clean = amax <= 3.402823466e38f;  // false for NaN and +inf
-    if (!clean) amax = block_max(fmaxf(max16(f[0]), max16(f[1])), red + 32);  // block-uniform
+    if (!clean) amax = block_max<false, NAMED>(fmaxf(max16(f[0]), max16(f[1])), red + 32, nt);
     const float s = __fdiv_rn(127.f, amax);  // +inf for an all-zero row: codes 0, carried 0
     if (threadIdx.x < 32) carried = __fdiv_rn(1.f, s);  // only warp 0 stores it
     if (clean && (s <= 3.402823466e38f || amax == 0.f)) {
       const float mult = amax == 0.f ? 0.f : s;
 #pragma unroll
       for (int q = 0; q < 2; ++q)
-        if (U.ok[q]) put16<GLOBAL>(codes + 16 * (threadIdx.x + q * blockDim.x), q8_16_magic(f[q], mult));
+        if (U.ok[q]) put16<GLOBAL>(codes + 16 * (threadIdx.x + q * nt), q8_16_magic(f[q], mult));
     } else {
 #pragma unroll
       for (int q = 0; q < 2; ++q)
-        if (U.ok[q]) put16<GLOBAL>(codes + 16 * (threadIdx.x + q * blockDim.x), q8_16(f[q], s));
+        if (U.ok[q]) put16<GLOBAL>(codes + 16 * (threadIdx.x + q * nt), q8_16(f[q], s));
     }
   } else if (MODE == 3) {
     // A 128-group is 8 units held by 8 consecutive lanes.
@@ -394,7 +406,7 @@ __device__ __forceinline__ float quantise(const float (&f)[2][16], const Units& 
       m = fmaxf(m, __shfl_xor_sync(kFull, m, 4));
       const float s = __fdiv_rn(kFp8Max, m);
       const float mult = m == 0.f ? 0.f : s;  // an all-zero group: codes 0, scale 0
-      const int u = threadIdx.x + q * blockDim.x;
+      const int u = threadIdx.x + q * nt;
       if (U.ok[q]) {
         put16<GLOBAL>(codes + 16 * u, fp8_16<E5>(f[q], mult));
         if ((u & 7) == 0) reinterpret_cast<float*>(scales)[u >> 3] = __fdiv_rn(1.f, s);
@@ -412,7 +424,7 @@ __device__ __forceinline__ float quantise(const float (&f)[2][16], const Units& 
       } else {
         e = ceil_log2_bits(__fdiv_rn(fmaxf(m, 1e-4f), kFp8Max));
       }
-      const int u = threadIdx.x + q * blockDim.x;
+      const int u = threadIdx.x + q * nt;
       if (U.ok[q]) {
         put16<GLOBAL>(codes + 16 * u, fp8_16<E5>(f[q], pow2(-e)));  // x / 2^e, exact scaling
         if ((u & 1) == 0) scales[u >> 1] = (uint8_t)(e + 127);
@@ -569,7 +581,7 @@ __global__ void __launch_bounds__(256) permute_kernel(PermuteArgs a) {
         for (int t = 0; t < 16; ++t) f[q][t] = 0.f;
       }
     }
-    const float carried = quantise<Q>(f, U, s_stage, s_stage + code_bytes, s_red[0]);
+    const float carried = quantise<Q>(f, U, s_stage, s_stage + code_bytes, s_red[0], blockDim.x);
     if (MODE == 5 || MODE == 4) {
       if (threadIdx.x == 0 && d.SC > (units >> 1)) s_stage[code_bytes + (units >> 1)] = 0;
     }
@@ -630,12 +642,14 @@ __global__ void __launch_bounds__(256) index_kernel(PermuteArgs a) {
 }
 
 template <class T, int Q>
-__global__ void __launch_bounds__(256, 2) smooth_rows_kernel(PermuteArgs a) {
+__global__ void __launch_bounds__(288, 2) smooth_rows_kernel(PermuteArgs a) {
   constexpr int MODE = q_mode(Q);
-  __shared__ uint64_t s_bar[kXStages];
+  __shared__ uint64_t s_full[kXStages];
+  __shared__ uint64_t s_empty[kXStages];
   __shared__ int s_srow[kXStages];
   __shared__ float s_red[2][64];
-  __shared__ int s_fail;
+  __shared__ volatile int s_pfail;  // set by the producer only
+  __shared__ int s_cfail;  // 1 + the first row a consumer gave up on, or INT_MAX
   extern __shared__ __align__(128) uint8_t s_ring[];  // kXStages token rows
 
   const Dims& d = a.d;
@@ -643,13 +657,20 @@ __global__ void __launch_bounds__(256, 2) smooth_rows_kernel(PermuteArgs a) {
   const int units = H >> 4;
   const uint32_t xbytes = 2u * (uint32_t)H;
   const int scale_bytes = MODE == 3 ? 4 * d.G3 : 0;
+  const int ncons = (int)blockDim.x - 32;  // consumer threads; the last warp produces
+  const int nwc = ncons >> 5;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* const dyn = static_cast<uint8_t*>(a.dynamic_scales);
   uint8_t* const out = static_cast<uint8_t*>(a.expand_x);
 
   if (threadIdx.x == 0) {
-    for (int st = 0; st < kXStages; ++st) mbar_init(&s_bar[st], 1);
+    for (int st = 0; st < kXStages; ++st) {
+      mbar_init(&s_full[st], 1);
+      mbar_init(&s_empty[st], (uint32_t)nwc);
+    }
     mbar_fence_init();
-    s_fail = 0;
+    s_pfail = 0;
+    s_cfail = INT_MAX;
   }
   __syncthreads();
   griddep_wait();  // the row table and the total come from the earlier kernels
@@ -661,39 +682,62 @@ __global__ void __launch_bounds__(256, 2) smooth_rows_kernel(PermuteArgs a) {
   }
   const int64_t lo = total * blockIdx.x / gridDim.x;
   const int n_rows = (int)(total * (blockIdx.x + 1) / gridDim.x - lo);
-  const int64_t n_tok = (int64_t)d.W * d.BS;
 
-  // Thread 0: start the token row of local row `issued` into its ring slot.
-  int issued = 0;
-  int2 next = make_int2(0, 0);
-  auto issue = [&](int2 p) {
-    const int st = issued % kXStages;
-    if (p.x < 0 || (int64_t)p.x >= n_tok || p.y < 0 || p.y >= d.S_eff + d.M) {
-      // consistency guard: never read outside x or the smooth table
-      atomicOr(a.ws.status, (uint32_t)CQ_ST_INTERNAL);
-      p = make_int2(0, 0);
+  if (warp == nwc) {
+    // Producer warp: reads 32 row-table entries at a time; lane 0 streams the
+    // token rows into the ring, kXStages rows ahead of the slowest consumer.
+    const int64_t n_tok = (int64_t)d.W * d.BS;
+    int issued = 0;
+    for (int j0 = 0; j0 < n_rows; j0 += 32) {
+      // Stop (the whole warp) once either side gave up.
+      if (__any_sync(kFull, s_pfail != 0 || *(volatile int*)&s_cfail != INT_MAX)) break;
+      int2 p = make_int2(0, 0);
+      if (j0 + lane < n_rows) {
+        p = a.ws.row_src[lo + j0 + lane];
+        if (p.x < 0 || (int64_t)p.x >= n_tok || p.y < 0 || p.y >= d.S_eff + d.M) {
+          // consistency guard: never read outside x or the smooth table
+          atomicOr(a.ws.status, (uint32_t)CQ_ST_INTERNAL);
+          p = make_int2(0, 0);
+        }
+      }
+      const int nb = min(32, n_rows - j0);
+      for (int b = 0; b < nb; ++b) {
+        const int px = __shfl_sync(kFull, p.x, b), py = __shfl_sync(kFull, p.y, b);
+        if (lane == 0 && !s_pfail) {
+          const int j = j0 + b, st = j % kXStages;
+          if (j >= kXStages &&
+              !mbar_wait(&s_empty[st], (uint32_t)((j / kXStages) - 1) & 1u)) {
+            s_pfail = 1;
+            atomicOr(a.ws.status, (uint32_t)CQ_ST_TIMEOUT);
+          } else {
+            s_srow[st] = py;
+            mbar_arrive_expect_tx(&s_full[st], xbytes);
+            bulk_load(s_ring + (size_t)st * xbytes, a.x + (int64_t)px * H, xbytes, &s_full[st]);
+            issued = j + 1;
+          }
+        }
+        __syncwarp();
+      }
     }
-    s_srow[st] = p.y;
-    mbar_arrive_expect_tx(&s_bar[st], xbytes);
-    bulk_load(s_ring + (size_t)st * xbytes, a.x + (int64_t)p.x * H, xbytes, &s_bar[st]);
-    ++issued;
-  };
-  if (threadIdx.x == 0) {
-    while (issued < n_rows && issued < kXStages) issue(a.ws.row_src[lo + issued]);
-    if (issued < n_rows) next = a.ws.row_src[lo + issued];
+    // Wait (bounded) for the last loads to land before this warp ends, so
+    // that no copy is in flight once the consumers are gone.
+    if (lane == 0)
+      for (int jj = issued > kXStages ? issued - kXStages : 0; jj < issued; ++jj)
+        mbar_wait(&s_full[jj % kXStages], (uint32_t)(jj / kXStages) & 1u);
+    griddep_launch_dependents();
+    return;
   }
-  __syncthreads();
 
+  // Consumer warps: each row is quantised by all of them together.
   Units U;
 #pragma unroll
-  for (int q = 0; q < 2; ++q) U.ok[q] = (int)threadIdx.x + q * (int)blockDim.x < units;
+  for (int q = 0; q < 2; ++q) U.ok[q] = (int)threadIdx.x + q * ncons < units;
   float sm[2][16];
   int cur = -1;
-  int j = 0;
-  for (; j < n_rows; ++j) {
+  for (int j = 0; j < n_rows; ++j) {
     const int st = j % kXStages;
-    if (!mbar_wait(&s_bar[st], (uint32_t)(j / kXStages) & 1u)) {
-      s_fail = 1;
+    if (!__all_sync(kFull, mbar_wait(&s_full[st], (uint32_t)(j / kXStages) & 1u)) && lane == 0) {
+      atomicMin(&s_cfail, j + 1);
       atomicOr(a.ws.status, (uint32_t)CQ_ST_TIMEOUT);
     }
     const int srow = s_srow[st];
@@ -702,7 +746,7 @@ __global__ void __launch_bounds__(256, 2) smooth_rows_kernel(PermuteArgs a) {
       const float* srcs = a.smooth + (int64_t)srow * H;
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
-        const int u = threadIdx.x + q * blockDim.x;
+        const int u = threadIdx.x + q * ncons;
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
           const uint4 v = U.ok[q] ? ld_nc_v4(srcs + 16 * u + 4 * t) : make_uint4(0, 0, 0, 0);
@@ -717,7 +761,7 @@ __global__ void __launch_bounds__(256, 2) smooth_rows_kernel(PermuteArgs a) {
     const uint8_t* xs = s_ring + (size_t)st * xbytes;
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
-      const int u = threadIdx.x + q * blockDim.x;
+      const int u = threadIdx.x + q * ncons;
       uint4 w[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
       if (U.ok[q]) {
         w[0] = ld_shared_v4(xs + 32 * u);
@@ -732,26 +776,20 @@ __global__ void __launch_bounds__(256, 2) smooth_rows_kernel(PermuteArgs a) {
         f[q][2 * t + 1] = p.y;
       }
     }
+    // This warp is done with the slot (token row and its smooth-row index).
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&s_empty[st]);
     const int64_t row = lo + j;
-    // Mode 2's row max holds a barrier; the other modes take one here. Past
-    // it every thread has read ring slot st.
-    if (MODE != 2) __syncthreads();
-    const float carried =
-        quantise<Q, true>(f, U, out + row * H, dyn + row * scale_bytes, s_red[j & 1]);
-    if (s_fail) break;  // set only before the barrier above: the same in all threads
-    if (threadIdx.x == 0) {
-      if (MODE == 2) reinterpret_cast<float*>(dyn)[row] = carried;
-      if (issued < n_rows) {  // refill the slot this row used
-        issue(next);
-        if (issued < n_rows) next = a.ws.row_src[lo + issued];
-      }
-    }
+    const float carried = quantise<Q, true, true>(f, U, out + row * H, dyn + row * scale_bytes,
+                                                  s_red[j & 1], ncons);
+    if (MODE == 2 && threadIdx.x == 0) reinterpret_cast<float*>(dyn)[row] = carried;
+    // Leave after row j if a consumer gave up on a row <= j. In mode 2 every
+    // such record was written before row j's barrier and every warp reads
+    // after it, so the warps leave together (a record for a later row does
+    // not count yet); the other modes have no barrier and each warp leaves on
+    // its own.
+    if (*(volatile int*)&s_cfail <= j + 1) break;
   }
-  // After a timeout, wait (bounded again) for the loads still in flight
-  // before the CTA's shared memory is released.
-  if (threadIdx.x == 0)
-    for (int jj = j; jj < issued; ++jj)
-      mbar_wait(&s_bar[jj % kXStages], (uint32_t)(jj / kXStages) & 1u);
   griddep_launch_dependents();
 }
 
@@ -781,6 +819,7 @@ cudaError_t launch_smooth_rows(const PermuteArgs& a, cudaStream_t s) {
   const int units = a.d.H >> 4;
   int threads = ((units + 1) / 2 + 31) / 32 * 32;
   if (threads < 32) threads = 32;
+  threads += 32;  // the producer warp
   const size_t smem = (size_t)kXStages * 2 * a.d.H;
   auto* kern = smooth_rows_kernel<T, Q>;
   if ((e = prepare_kernel<smooth_rows_kernel<T, Q>>(smem)) != cudaSuccess) return e;
