@@ -140,27 +140,50 @@ class ClockSampler:
 # -------------------------------------------------------- byte accounting ----
 
 def algorithmic_bytes(cfg, rows: int, tokens_active: int, with_scales: bool,
-                      combine_int8: bool = False) -> dict:
+                      combine_int8: bool = False, smooth_bytes: int = 0,
+                      special_tokens: int = 0) -> dict:
     """Bytes each kernel must move per launch (reads + writes of HBM), given
-    the routed row count P and the active token count."""
+    the routed row count P, the active token count, the size of the smooth
+    scales the call reads (once) and the number of tokens with a copy or
+    const slot (their ori_x row is read once; const_v rows once in all)."""
     W, BS, K, H = cfg.ep_world_size, cfg.max_bs, cfg.topk, cfg.hidden
     NS, L = cfg.num_slots, cfg.local_expert_num
     G = cfg.shared_expert_rank_num + cfg.moe_expert_num
     T = W * BS
     mode = cfg.quant_mode
     b_code = 2 if mode == 0 else 1
-    b_scale = {0: 0, 2: 4, 5: cfg.scale_cols}[mode]
+    b_scale = {0: 0, 1: 0, 2: 4, 3: 4 * cfg.group_cols, 4: cfg.scale_cols, 5: cfg.scale_cols}[mode]
     route = 4 * T * K + 4 * T * NS + 3 * 4 * G * W + 4 * W * W * L + 8 * W * L
     permute = (2 * H * tokens_active            # x, read once per active token
                + rows * (H * b_code + b_scale + 16)  # codes, scale, (src, token, slot) record
                + 4 * T * NS * 2 + 4 * T * K     # eidx read, inv write, ids read
-               + (8 * rows if with_scales else 0))  # routing weight read + carried copy
+               + (8 * rows if with_scales else 0)  # routing weight read + carried copy
+               + smooth_bytes)
     ffn_row = (H + 4 * (H // 8)) if combine_int8 else 2 * H  # int8 codes + block scales
-    combine = ffn_row * rows + 2 * H * T + 4 * T * NS + 4 * T * K
+    combine = (ffn_row * rows + 2 * H * T + 4 * T * NS + 4 * T * K
+               + 2 * H * (special_tokens + cfg.const_expert_num))  # ori_x rows, const_v
     out = {"route": route, "permute": permute, "combine": combine}
     if combine_int8:
         out["combine_quant"] = rows * (2 * H + H + 4 * (H // 8))  # bf16 in, codes + scales out
     return out
+
+
+def special_token_count(wl) -> int:
+    """Active tokens with at least one active copy or const slot."""
+    c = wl.cfg
+    lo = c["moe_expert_num"] + c["zero_expert_num"]
+    hi = lo + c["copy_expert_num"] + c["const_expert_num"]
+    if hi == lo:
+        return 0
+    W, BS, K = c["ep_world_size"], c["max_bs"], c["topk"]
+    ids = wl.expert_ids.reshape(W, BS, K)
+    on = np.ones((W, BS, K), bool)
+    if wl.bs_per_rank is not None:
+        on &= (np.arange(BS)[None, :] < wl.bs_per_rank[:, None])[:, :, None]
+    if wl.mask is not None:
+        m = wl.mask.reshape(W, BS, -1).astype(bool)
+        on &= m if m.shape[2] == K else m[:, :, :1]
+    return int((((ids >= lo) & (ids < hi)) & on).any(axis=2).sum())
 
 
 def measured_peaks() -> tuple[float, str]:
@@ -403,6 +426,8 @@ def run_cq(args):
     tokens = wl.tokens
     if wl.mask is not None:
         tokens = int((wl.mask.reshape(cfg.ep_world_size, cfg.max_bs, -1).max(axis=2) > 0).sum())
+    smooth_bytes = int(sm.numel() * 4) if sm is not None else 0
+    special_tokens = special_token_count(wl)
 
     # The launches of a step are captured into CUDA graphs (the whole step, and
     # each kernel alone for the breakdown), so host-side enqueue time never
@@ -533,7 +558,8 @@ def run_cq(args):
             dist.destroy_process_group()
         return 0
 
-    ab = algorithmic_bytes(cfg, rows, tokens, with_scales=True,
+    ab = algorithmic_bytes(cfg, rows, tokens, with_scales=True, smooth_bytes=smooth_bytes,
+                           special_tokens=special_tokens,
                            combine_int8=args.combine == "int8")
     means = {"route": statistics.mean(t_route), "permute": statistics.mean(t_perm),
              "combine": statistics.mean(t_comb)}
