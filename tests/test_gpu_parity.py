@@ -230,3 +230,29 @@ def test_determinism_and_split_entry_points():
     assert torch.equal(out1.expand_x[:R], out3.expand_x[:R])
     assert torch.equal(out1.dynamic_scales[:R], out3.dynamic_scales[:R])
     assert torch.equal(out1.ep_recv_count, out3.ep_recv_count)
+
+
+def test_edge_max_world_size():
+    """W = 768, the largest rank count: more routing CTAs than SMs (the count
+    kernel then lets its dependents launch only when it ends) and the longest
+    rank-base prefix."""
+    _full_check(_cfg_case(11, W=768, M=768, BS=2, K=8, H=1024))
+
+
+def test_edge_max_experts_and_k():
+    """M = 1024 experts (L = 128 per rank) with K = 16."""
+    _full_check(_cfg_case(12, W=8, M=1024, BS=16, K=16, H=1024))
+
+
+def test_edge_max_bs():
+    _full_check(_cfg_case(14, W=4, M=8, BS=512, K=4, H=1024))
+
+
+@pytest.mark.parametrize("mode", [2, 3])
+def test_edge_max_hidden_shared_and_smooth(mode):
+    """H = 8192 with 4 shared experts on 4 ranks and one smooth row per expert:
+    the per-expert-smooth kernel at its largest CTA."""
+    wl = _cfg_case(13, W=8, M=16, BS=32, K=8, H=8192, mode=mode, shared_expert_num=4,
+                   shared_expert_rank_num=4)
+    wl.smooth = np.random.default_rng(13).uniform(0.5, 1.5, (4 + 16, 8192)).astype(np.float32)
+    _full_check(wl)
