@@ -61,6 +61,8 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default="dsv3")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-all-cores", action=argparse.BooleanOptionalAction, default=True,
+                    help="also time the oracle on every host core (spawned processes)")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--quant-mode", type=int, default=None,
                     help="override the workload's quant_mode (0, 2, 5)")
@@ -219,27 +221,30 @@ def ncu_traffic(kernel: str):
 
 # ------------------------------------------------------- oracle baseline ----
 
-def oracle_sample(wl, budget_s: float, max_tokens: int | None = None):
-    """Time the oracle (single-threaded C, as it stands) on a bounded sample of
-    the workload: the full routing scan, then quantisation of the rows of the
-    first n tokens and the combine of those n tokens, n growing until the
-    budget is spent. Returns (tokens/s, description, cores)."""
+def _oracle_prepare(wl):
+    """The whole-batch routing scan (timed) and the inputs of the per-token
+    work: (route, inv remapped into a small expert-output pool, pool, t_route)."""
     import oracle
     from combine_quant_gb300 import workloads
 
     oracle.build()
-    cfg = wl.cfg
-    W, BS, K, H = cfg["ep_world_size"], cfg["max_bs"], cfg["topk"], cfg["hidden"]
-    mode = cfg["quant_mode"]
-    pool = workloads.ffn_standin(wl.seed, 1024, H)
+    pool = workloads.ffn_standin(wl.seed, 1024, wl.cfg["hidden"])
     t0 = time.perf_counter()
-    route = oracle.route(cfg, wl.expert_ids, wl.mask, wl.bs_per_rank)
+    route = oracle.route(wl.cfg, wl.expert_ids, wl.mask, wl.bs_per_rank)
     t_route = time.perf_counter() - t0
     inv_pool = np.where(route.inv >= 0, route.inv.astype(np.int64) % pool.shape[0],
                         route.inv).astype(np.int32)
-    order = [(r, i) for r in range(W) for i in range(BS)]
-    if max_tokens:
-        order = order[:max_tokens]
+    return route, inv_pool, pool, t_route
+
+
+def _oracle_tokens(wl, prep, order, budget_s: float):
+    """Quantise every dispatched row of each token in `order` and combine the
+    token, until the budget is spent. Returns (tokens done, seconds)."""
+    import oracle
+
+    route, inv_pool, pool, _ = prep
+    cfg = wl.cfg
+    K, mode = cfg["topk"], cfg["quant_mode"]
     done = 0
     t0 = time.perf_counter()
     for r, i in order:
@@ -255,13 +260,75 @@ def oracle_sample(wl, budget_s: float, max_tokens: int | None = None):
         done += 1
         if time.perf_counter() - t0 > budget_s:
             break
-    t_tok = time.perf_counter() - t0
+    return done, time.perf_counter() - t0
+
+
+def oracle_sample(wl, budget_s: float, max_tokens: int | None = None):
+    """Time the oracle (single-threaded C, as it stands) on a bounded sample of
+    the workload: the full routing scan, then quantisation of the rows of the
+    first n tokens and the combine of those n tokens, n growing until the
+    budget is spent. Returns (tokens/s, description, cores)."""
+    cfg = wl.cfg
+    W, BS = cfg["ep_world_size"], cfg["max_bs"]
+    prep = _oracle_prepare(wl)
+    order = [(r, i) for r in range(W) for i in range(BS)]
+    if max_tokens:
+        order = order[:max_tokens]
+    done, t_tok = _oracle_tokens(wl, prep, order, budget_s)
+    t_route = prep[3]
     # The routing scan is a whole-batch pass; charge it pro rata.
     per_tok = t_tok / done + t_route / (W * BS)
     desc = (f"oracle route over all {W * BS} tokens ({t_route:.3f} s) + quantise-and-combine of "
             f"the first {done} tokens in rank-major order ({t_tok:.2f} s); value = tokens / "
             f"(per-token time + route time pro rata)")
     return 1.0 / per_tok, desc, 1
+
+
+def _oracle_worker(name, quant_mode, wi, n, budget_s, ready, start, results):
+    """One process of the all-cores oracle baseline: tokens wi, wi + n, ..."""
+    sys.path.insert(0, ROOT)
+    from combine_quant_gb300 import workloads
+
+    wl = workloads.WORKLOADS[name]()
+    if quant_mode is not None:
+        wl = wl.with_mode(quant_mode)
+    prep = _oracle_prepare(wl)
+    W, BS = wl.cfg["ep_world_size"], wl.cfg["max_bs"]
+    order = [(r, i) for r in range(W) for i in range(BS)][wi::n]
+    ready.put(wi)
+    start.wait()
+    done, secs = _oracle_tokens(wl, prep, order, budget_s)
+    results.put((done, secs, prep[3]))
+
+
+def oracle_all_cores(name: str, quant_mode, budget_s: float, n: int | None = None):
+    """The same oracle work on every host core: n spawned processes (started
+    only after all have built their inputs) take interleaved tokens. Returns
+    (tokens/s, cores): all tokens done over the slowest process's time, plus
+    the single-threaded routing scan pro rata."""
+    import multiprocessing as mp
+
+    n = n or os.cpu_count() or 1
+    ctx = mp.get_context("spawn")
+    ready, results, start = ctx.Queue(), ctx.Queue(), ctx.Event()
+    procs = [ctx.Process(target=_oracle_worker,
+                         args=(name, quant_mode, wi, n, budget_s, ready, start, results))
+             for wi in range(n)]
+    for p in procs:
+        p.start()
+    for _ in range(n):
+        ready.get(timeout=600)
+    start.set()
+    out = [results.get(timeout=600 + 4 * budget_s) for _ in range(n)]
+    for p in procs:
+        p.join(timeout=60)
+    done = sum(o[0] for o in out)
+    secs = max(o[1] for o in out)
+    t_route = out[0][2]
+    from combine_quant_gb300 import workloads
+    c = workloads.WORKLOADS[name]().cfg
+    per_tok = secs / done + t_route / (c["ep_world_size"] * c["max_bs"])
+    return 1.0 / per_tok, n
 
 
 # ------------------------------------------------------------- distributed ----
@@ -592,6 +659,11 @@ def run_cq(args):
     if world == 1 and not args.no_cpu_baseline:
         v, desc, cores = oracle_sample(wl, args.cpu_seconds)
         cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+        if args.cpu_all_cores:
+            va, na = oracle_all_cores(args.workload, args.quant_mode, args.cpu_seconds)
+            cpu["all_cores"] = {"value": va, "unit": UNIT, "cores": na,
+                                "sample": f"the same per-token work on {na} spawned processes, "
+                                          "interleaved tokens, each for the same time budget"}
 
     emit({"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
           "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -599,8 +671,9 @@ def run_cq(args):
           "config": {"workload": workload_desc(wl), "tokens_per_step": tokens,
                      "rows_per_step": rows,
                      "io": "bf16 tokens in; dispatch rows " + {
-                         0: "bf16", 2: "int8 + f32 per-row scale",
-                         5: "e4m3 + e8m0 per-32 scales"}[cfg.quant_mode]
+                         0: "bf16", 1: "int8 (static)", 2: "int8 + f32 per-row scale",
+                         3: "fp8 + f32 per-128 scales", 4: "fp8 + e8m0 per-32 scales",
+                         5: "fp8 + e8m0 per-32 scales"}[cfg.quant_mode]
                      + "; combine from " + ("int8 expert outputs + f32 per-8 scales"
                                             if args.combine == "int8" else "bf16 expert outputs")
                      + "; bf16 out",
