@@ -170,6 +170,14 @@ def algorithmic_bytes(cfg, rows: int, tokens_active: int, with_scales: bool,
     return out
 
 
+def kernels_per_step(cfg, smooth_given: bool) -> int:
+    """libcq kernels one step launches: routing (count, offsets), the permute
+    (index + smooth-rows kernels for per-expert smooth scales in modes 1-3,
+    else one kernel) and the combine."""
+    per_expert_smooth = smooth_given and cfg.smooth_kind == 0 and cfg.quant_mode in (1, 2, 3)
+    return 2 + (2 if per_expert_smooth else 1) + 1
+
+
 def special_token_count(wl) -> int:
     """Active tokens with at least one active copy or const slot."""
     c = wl.cfg
@@ -689,7 +697,8 @@ def run_cq(args):
                           "note": "per-kernel figures come from a separate loop of "
                                   f"{n_bd} steps with events between the kernels"},
           "kernels": kernels, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-          "gpu_launches": 3 * args.steps, "clocks": clk, "wall_s": t_wall})
+          "gpu_launches": kernels_per_step(cfg, sm is not None) * args.steps, "clocks": clk,
+          "wall_s": t_wall})
     if dist is not None:
         dist.destroy_process_group()
     return 0
