@@ -466,12 +466,25 @@ __global__ void __launch_bounds__(288) combine_staged_kernel(CombineArgs a, int 
 constexpr int kQThreads = 256;
 constexpr int kQUnits = 4;  // kQThreads * kQUnits * 8 >= the largest H (8192)
 
+// fl(v / s) from y = RN(1 / s) by Markstein's correction step: q0 = RN(v*y),
+// the remainder r = v - s*q0 exact in one fused multiply-add, then
+// RN(q0 + r*y). For a normal s and no overflow this is the correctly rounded
+// quotient (P. Markstein, "Computation of elementary functions on the IBM
+// RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990); the tests
+// compare it with IEEE division on every bf16 mantissa pair at every exponent
+// offset that can round to a non-zero code. A zero or infinite s gives NaN
+// or 0 exactly where v / s does.
+__device__ __forceinline__ float div_by(float v, float s, float y) {
+  const float q0 = __fmul_rn(v, y);
+  return __fmaf_rn(__fmaf_rn(-s, q0, v), y, q0);
+}
+
 // RNE(fl(v / s)) as the low byte of a float, for a block whose scale s is
-// normal or infinite, or whose max is 0: every quotient is then NaN or lies
-// in [-128, 128]. max(q, -256) maps NaN (0/0, inf/inf) to -256; adding
-// 1.5 * 2^23 leaves RNE(q) in the low byte of the sum (-256 -> 0).
-__device__ __forceinline__ uint32_t q8_div_magic(float v, float s) {
-  return __float_as_uint(__fadd_rn(fmaxf(__fdiv_rn(v, s), -256.f), 12582912.f));
+// normal or infinite, or whose max is 0 (y = RN(1 / s)): every quotient is
+// then NaN or lies in [-128, 128]. max(q, -256) maps NaN (0/0, inf/inf) to
+// -256; adding 1.5 * 2^23 leaves RNE(q) in the low byte of the sum (-256 -> 0).
+__device__ __forceinline__ uint32_t q8_div_magic(float v, float s, float y) {
+  return __float_as_uint(__fadd_rn(fmaxf(div_by(v, s, y), -256.f), 12582912.f));
 }
 
 template <class T>
@@ -501,12 +514,14 @@ __global__ void __launch_bounds__(kQThreads) combine_quant_kernel(CombineArgs a)
       const float s = __fmul_rn(m, __fdiv_rn(1.f, 127.f));
       uint32_t w[2];
       if (m == 0.f || s >= 1.17549435e-38f) {
+        const float y = __frcp_rn(s);
 #pragma unroll
         for (int h = 0; h < 2; ++h)
-          w[h] = __byte_perm(
-              __byte_perm(q8_div_magic(f[4 * h], s), q8_div_magic(f[4 * h + 1], s), 0x0040),
-              __byte_perm(q8_div_magic(f[4 * h + 2], s), q8_div_magic(f[4 * h + 3], s), 0x0040),
-              0x5410);
+          w[h] = __byte_perm(__byte_perm(q8_div_magic(f[4 * h], s, y),
+                                         q8_div_magic(f[4 * h + 1], s, y), 0x0040),
+                             __byte_perm(q8_div_magic(f[4 * h + 2], s, y),
+                                         q8_div_magic(f[4 * h + 3], s, y), 0x0040),
+                             0x5410);
       } else {
         // A subnormal or zero scale of a non-zero block: quotients may leave
         // the int8 range and saturate.

@@ -123,3 +123,71 @@ def test_combine_quant_extreme_blocks(x_dtype):
     assert np.array_equal(gh.host(codes[:R]), pc), "int8 codes differ"
     assert np.array_equal(gh.host(scales[:R]).view(np.uint32), ps.view(np.uint32)), \
         "block scales differ"
+
+
+def _division_blocks(x_dtype: int) -> np.ndarray:
+    """Blocks [m, v1..v7] with |v| <= |m| covering the quotients v / s of the
+    block quantiser (s = max * fl(1/127)) that can round to a non-zero code:
+    every mantissa pair of m and v at every exponent offset d = e_m - e_v in
+    0..10 (a larger offset makes |v / s| < 0.5), with m at a few exponents
+    from the bottom to the top of the range; bf16 exhaustively, fp16 with
+    every 3rd m and every 7th v mantissa. The quotient depends only on the mantissas and d
+    while s stays normal, which the bottom exponents leave."""
+    rng = np.random.default_rng(17)
+    if x_dtype == 0:
+        man_m, man_v = range(128), range(128)
+        exps = [1, 2, 5, 6, 7, 8, 9, 12, 127, 200, 254]   # biased binary32 exponents
+        to_f = lambda e, mm: np.float32(np.ldexp(1.0 + mm / 128.0, e - 127))
+    else:
+        man_m, man_v = range(0, 1024, 3), range(0, 1024, 7)
+        exps = [1, 2, 10, 15, 25, 30]                      # biased fp16 exponents
+        to_f = lambda e, mm: np.float32(np.ldexp(1.0 + mm / 1024.0, e - 15))
+    blocks = []
+    for e in exps:
+        for mm in man_m:
+            m = to_f(e, mm)
+            vs = []
+            for d in range(0, 11):
+                if e - d < 1:
+                    break
+                for vm in man_v:
+                    if d == 0 and vm > mm:
+                        continue
+                    v = to_f(e - d, vm)
+                    vs += [v, -v]
+            if x_dtype == 1 and e <= 10:  # fp16 subnormals below m
+                vs += [np.float32(np.ldexp(k, -24)) for k in range(1, 1024, 37)]
+            vs = np.array(vs, np.float32)
+            vs = np.concatenate([vs, np.zeros((-len(vs)) % 7, np.float32)]).reshape(-1, 7)
+            sign = np.where(rng.random(len(vs)) < 0.5, -1.0, 1.0).astype(np.float32)
+            blk = np.concatenate([(m * sign)[:, None], vs], axis=1)
+            blocks.append(blk)
+    return np.concatenate(blocks).reshape(-1)
+
+
+@pytest.mark.parametrize("x_dtype", [0, 1])
+def test_combine_quant_division_exhaustive(x_dtype):
+    """The quantiser's division (a reciprocal and one correction step) against
+    the oracle's IEEE division on the structured block set above: codes and
+    scales bit for bit."""
+    import combine_quant_gb300 as cq
+    wl = workloads.dsv3(seed=40, W=8, BS=128, M=64, K=8, H=1024)
+    if x_dtype:
+        wl = workloads.as_fp16(wl)
+    cfg, out, status, _ = gh.gpu_dispatch(wl)
+    R = int(gh.host(cq.assist_views(cfg, out.assist_info)[2])[-1])
+    vals = _division_blocks(x_dtype)
+    H = cfg.hidden
+    n_rows = (vals.size + H - 1) // H
+    assert n_rows <= R, (n_rows, R)
+    f = np.zeros((cfg.max_rows, H), np.float32)
+    f.reshape(-1)[:vals.size] = vals
+    bits = workloads.to_f16_bits(f) if x_dtype else workloads.to_bf16_bits(f)
+    # every value is exact in the 16-bit type
+    back = workloads.bf16_bits_to_f32(bits) if x_dtype == 0 else bits.view(np.float16).astype(np.float32)
+    assert np.array_equal(back.reshape(-1)[:vals.size], vals)
+    rows = torch.from_numpy(bits).to(gh.DEV).view(cfg.token_dtype)
+    codes, scales = cq.combine_quant(cfg, rows, out.assist_info)
+    pc, ps = oracle.combine_quant_rows(bits[:n_rows], x_dtype)
+    assert np.array_equal(gh.host(codes[:n_rows]), pc), "int8 codes differ"
+    assert np.array_equal(gh.host(scales[:n_rows]).view(np.uint32), ps.view(np.uint32))
