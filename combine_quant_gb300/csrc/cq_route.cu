@@ -89,6 +89,10 @@ __device__ int block_excl_scan(int v, int* buf, int* total) {
 
 // trigger_early: every CTA of this grid is resident at once (W <= SM count),
 // so the dependent kernels may launch right away without starving it.
+// STEPS >= the 32-pair steps of a warp's range: the unrolled loops hold only
+// as many steps as the problem needs (the kernel's code is fetched cold from
+// DRAM when L2 holds other data, so its size shows in the latency).
+template <int STEPS>
 __global__ void __launch_bounds__(kCountThreads) count_kernel(RouteArgs a, int trigger_early) {
   extern __shared__ uint16_t tbl[];  // [kCountWarps][M]: per-warp counts, then bases
   __shared__ int s_tokcnt[kCountWarps];
@@ -111,9 +115,9 @@ __global__ void __launch_bounds__(kCountThreads) count_kernel(RouteArgs a, int t
   // a MoE expert id (>= 0), or a CQ_INV code (none / copy / const c).
   const int64_t Z0 = M, C0 = Z0 + d.Z, Q0 = C0 + d.C, Q1 = Q0 + d.Q;
   bool bad_id = false;
-  int cls[kMaxSteps];
+  int cls[STEPS];
 #pragma unroll
-  for (int s = 0; s < kMaxSteps; ++s) {
+  for (int s = 0; s < STEPS; ++s) {
     const int p = p0 + s * 32 + lane;
     int c = CQ_INV_NONE;
     if (s < nsteps && p < p1) {
@@ -142,9 +146,9 @@ __global__ void __launch_bounds__(kCountThreads) count_kernel(RouteArgs a, int t
 
   // One walk: the ordinal of each pair inside its warp's range, and the
   // warp's count per expert (the group leader adds the group size).
-  int ord[kMaxSteps];
+  int ord[STEPS];
 #pragma unroll
-  for (int s = 0; s < kMaxSteps; ++s) {
+  for (int s = 0; s < STEPS; ++s) {
     ord[s] = 0;
     if (s >= nsteps) continue;
     const int key = cls[s] >= 0 ? cls[s] : -1;
@@ -197,7 +201,7 @@ __global__ void __launch_bounds__(kCountThreads) count_kernel(RouteArgs a, int t
 
   // Final ordinals: the warp's base for the expert plus the in-warp ordinal.
 #pragma unroll
-  for (int s = 0; s < kMaxSteps; ++s) {
+  for (int s = 0; s < STEPS; ++s) {
     if (s >= nsteps) break;
     const int p = p0 + s * 32 + lane;
     if (p < p1) {
@@ -317,7 +321,18 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
   cudaError_t e0 = cudaGetDevice(&dev);
   if (e0 == cudaSuccess) e0 = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e0 != cudaSuccess) return e0;
-  count_kernel<<<a.d.W, kCountThreads, table, s>>>(a, a.d.W <= sms ? 1 : 0);
+  const int tpw = (a.d.BS + kCountWarps - 1) / kCountWarps;
+  const int steps = (tpw * a.d.K + 31) / 32;
+  const int trigger = a.d.W <= sms ? 1 : 0;
+  if (steps <= 2) {
+    count_kernel<2><<<a.d.W, kCountThreads, table, s>>>(a, trigger);
+  } else if (steps <= 4) {
+    count_kernel<4><<<a.d.W, kCountThreads, table, s>>>(a, trigger);
+  } else if (steps <= 8) {
+    count_kernel<8><<<a.d.W, kCountThreads, table, s>>>(a, trigger);
+  } else {
+    count_kernel<kMaxSteps><<<a.d.W, kCountThreads, table, s>>>(a, trigger);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_pdl(offsets_kernel, dim3(a.d.W), dim3(kOffThreads), 0, s, a);
