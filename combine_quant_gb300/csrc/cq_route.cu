@@ -277,15 +277,18 @@ __global__ void __launch_bounds__(kOffThreads) offsets_kernel(RouteArgs a) {
     }
     a.expert_token_nums[(int64_t)rank * d.L + le] = e;
   }
-  if (threadIdx.x == 0) a.ws.rank_tot[rank] = tot;
-
-  // Last CTA: exclusive prefix of the W rank totals gives each rank's first row.
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) s_last = (atomicAdd(a.ws.done, 1u) == (unsigned)(d.W - 1));
+  // Last CTA: exclusive prefix of the W rank totals gives each rank's first
+  // row. Thread 0 publishes this rank's total with a release increment of the
+  // counter; the CTA that completes the count acquires every total, and its
+  // barrier passes them on to its other threads.
+  if (threadIdx.x == 0) {
+    a.ws.rank_tot[rank] = tot;
+    unsigned old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(a.ws.done) : "memory");
+    s_last = old == (unsigned)(d.W - 1);
+  }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
   constexpr int kPerRank = 3;  // W <= 768 = 3 x 256
   const int rb0 = threadIdx.x * kPerRank;
   int rv[kPerRank];
