@@ -69,7 +69,7 @@ def parse_args(argv=None):
     ap.add_argument("--combine", choices=["bf16", "int8"], default="bf16",
                     help="combine from bf16 expert outputs, or from int8 ones quantised on the "
                          "expert side (the quantiser is timed separately, outside the step)")
-    ap.add_argument("--flush", choices=["write+read", "write"], default="write+read",
+    ap.add_argument("--flush", choices=["write+read", "write", "none"], default="write+read",
                     help="L2 flush between steps (outside the timed events)")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch each call directly instead of replaying CUDA graphs")
@@ -469,6 +469,8 @@ def run_cq(args):
 
         @staticmethod
         def zero_():
+            if args.flush == "none":  # hot-L2 figures only: not a contract number
+                return
             flush_w.zero_()
             if args.flush == "write+read":
                 flush_r.amax()
@@ -685,9 +687,11 @@ def run_cq(args):
                      + "; combine from " + ("int8 expert outputs + f32 per-8 scales"
                                             if args.combine == "int8" else "bf16 expert outputs")
                      + "; bf16 out",
-                     "l2": "flushed between steps: 256 MiB write" + (
-                         " then 256 MiB read (no dirty lines left)"
-                         if args.flush == "write+read" else ""),
+                     "l2": ("NOT flushed between steps (--flush none: hot-L2 figures, "
+                            "not a valid headline number)") if args.flush == "none" else
+                           "flushed between steps: 256 MiB write" + (
+                               " then 256 MiB read (no dirty lines left)"
+                               if args.flush == "write+read" else ""),
                      "parallelism": f"{world} independent replica(s), logical ranks on-device",
                      "launch": "CUDA graph replay of the step's three libcq launches"
                                if use_graph else "direct launches"},
