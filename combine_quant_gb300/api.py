@@ -197,6 +197,29 @@ def dispatch(cfg: Config, x: torch.Tensor, expert_ids: torch.Tensor,
     return out
 
 
+def dispatch_noalloc(cfg: Config, x: torch.Tensor, expert_ids: torch.Tensor,
+                     smooth_scales: Optional[torch.Tensor] = None,
+                     x_active_mask: Optional[torch.Tensor] = None,
+                     bs_per_rank: Optional[torch.Tensor] = None,
+                     expert_scales: Optional[torch.Tensor] = None,
+                     out: Optional[DispatchResult] = None) -> DispatchResult:
+    """Dispatch through cq_dispatch_noalloc: no workspace, the library's own
+    fixed scratch instead (for callers that cannot allocate device memory;
+    calls must not overlap on the GPU). `out` may be preallocated."""
+    dev = _check_inputs(cfg, x, expert_ids, smooth_scales, x_active_mask, bs_per_rank,
+                        expert_scales)
+    if out is None:
+        out = alloc_dispatch_outputs(cfg, dev, expert_scales is not None)
+    c = cfg.as_c()
+    rc = _lib.load().cq_dispatch_noalloc(
+        ctypes.byref(c), _ptr(x), _ptr(expert_ids), _ptr(smooth_scales), _ptr(x_active_mask),
+        _ptr(bs_per_rank), _ptr(expert_scales), _ptr(out.expand_x), _ptr(out.dynamic_scales),
+        _ptr(out.assist_info), _ptr(out.ep_recv_count), _ptr(out.expert_token_nums),
+        _ptr(out.expand_scales), _stream(dev))
+    _lib.check(rc, "cq_dispatch_noalloc")
+    return out
+
+
 def dispatch_route(cfg: Config, expert_ids, x_active_mask=None, bs_per_rank=None, *,
                    workspace, out: DispatchResult) -> None:
     """First half of dispatch (scan, counts, prefix sums)."""
@@ -344,3 +367,15 @@ def assist_views(cfg: Config, assist_info: torch.Tensor):
     inv = assist_info[4 * R:4 * R + W * BS * NS].view(W, BS, NS)
     base = assist_info[4 * R + W * BS * NS:]
     return rows, inv, base
+
+
+# The C ABI's names (include/cq.h) for the same calls.
+cq_dispatch = moe_dispatch = dispatch
+cq_dispatch_route = dispatch_route
+cq_dispatch_permute = dispatch_permute
+cq_dispatch_noalloc = dispatch_noalloc
+cq_combine = moe_combine = combine
+cq_combine_quant = combine_quant
+cq_combine_q8 = combine_q8
+cq_read_status = read_status
+cq_read_combine_status = read_combine_status

@@ -41,6 +41,17 @@ def test_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), f"libcq.so does not export {name}"
 
 
+def test_binding_has_every_call_under_its_c_name():
+    """The Python binding offers each data-path entry point of the C ABI under
+    the same name (size queries are Config properties)."""
+    import combine_quant_gb300 as cq
+    calls = [n for n in _declared() if n.startswith(("cq_dispatch", "cq_combine", "cq_read",
+                                                       "moe_"))]
+    assert calls
+    for name in calls:
+        assert callable(getattr(cq, name, None)), f"binding lacks {name}"
+
+
 def _c(cfg):
     return ctypes.byref(_lib.CqConfig(**cfg))
 

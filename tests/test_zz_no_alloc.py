@@ -87,6 +87,17 @@ def test_noalloc_matches_dispatch_on_two_calls_in_a_row():
     _same(cfg, ref, got)
 
 
+def test_python_wrapper_matches_dispatch():
+    """cq.dispatch_noalloc (the binding's wrapper of the same entry point)."""
+    wl = workloads.dsv3(seed=43, W=8, BS=24, M=64, K=8, H=1024)
+    cfg = cq.Config.from_dict(wl.cfg)
+    inp = _inputs(wl)
+    ref = cq.dispatch(cfg, **inp)
+    got = cq.dispatch_noalloc(cfg, **inp)
+    torch.cuda.synchronize()
+    assert _same(cfg, ref, got) > 0
+
+
 def test_noalloc_rejects_problems_beyond_its_scratch():
     cfg = cq.Config(ep_world_size=256, moe_expert_num=512, max_bs=512, topk=16, hidden=4096,
                     quant_mode=2)
