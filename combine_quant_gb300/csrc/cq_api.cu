@@ -4,6 +4,8 @@
 // The ranges follow "CANN ops-transformer 算子解析：MoeDistributeDispatchV3 的
 // EP 域 Token 分发与动态量化通信实现" (约束说明, 参数说明, 前置校验) and
 // "low_latency_dispatch" (shape variables: local_expert_num * W <= 2048).
+// Page tags ([DV3], [DSN], [LLD], [PERF]) name the source pages listed at the
+// top of include/cq.h.
 #include <cuda_runtime.h>
 
 #include "cq_internal.cuh"

@@ -1,18 +1,23 @@
 // cq_combine.cu -- inverse permute + top-K weighted sum, and the combine-side
 // int8 quantisation of the expert outputs.
 //
-// One CTA per (token, 1024-element chunk). The slot table of the token (row
-// of each expert output, or a zero / copy / const code) is read into shared
-// memory; every thread then owns one 8-element unit of the chunk, gathers the
-// expert rows with vector loads (a batch of 8 routed slots issued before the
-// first multiply), and sums in binary32: one fused multiply-add per routed
-// slot in slot order, then the shared-expert rows added unweighted, then one
-// rounding to the output type. This is the weighted sum of
+// The sum for token (r, i) gathers the expert output row of each of its
+// slots and adds them in binary32: one fused multiply-add per routed slot in
+// slot order, then the shared-expert rows added unweighted, then one rounding
+// to the output type. This is the weighted sum of
 // "MoeDistributeDispatch和MoeDistributeCombine算子设计介绍" §3.4.2 and of the
 // combine steps of "CANN MoE Dispatch/Combine 通信算子性能优化实践" (multiply by
 // expert scale, sum in float, add the shared expert output, cast back), with
 // the special experts of "low_latency_dispatch" 特殊专家场景. Token, expert
 // output and result rows are bf16 or fp16 (the T template parameter).
+//
+// Three kernels:
+// - combine_staged_kernel (16-bit expert outputs): persistent CTAs; a
+//   producer warp streams each token's expert rows into a shared-memory ring
+//   with bulk (TMA) loads, consumer warps sum them.
+// - combine_kernel (int8 expert outputs + per-8 scales): one CTA per (token,
+//   1024 values), each thread gathering its 8 values of a batch of slots.
+// - combine_quant_kernel: the expert-side int8 block quantiser.
 #include <mutex>
 
 #include "cq_internal.cuh"
@@ -96,19 +101,6 @@ __device__ __forceinline__ void store8(void* y, int64_t elem, const float (&acc)
                      T::pack2(acc[4], acc[5]), T::pack2(acc[6], acc[7])));
   }
 }
-
-// Expert-output rows as 16-bit values: 8 per 16-byte load.
-template <class T>
-struct Src16 {
-  const uint16_t* ffn;
-  struct Item {
-    uint4 v;
-  };
-  __device__ Item load(int64_t row, int H, int u) const {
-    return {ld_nc_v4(ffn + row * H + 8 * (int64_t)u)};
-  }
-  __device__ void floats(const Item& it, float (&f)[8]) const { unpack8<T>(it.v, f); }
-};
 
 // Expert-output rows as int8 with one scale per 8 values ("CANN MoE
 // Dispatch/Combine 通信算子性能优化实践", Int8DequantProcess): each value is

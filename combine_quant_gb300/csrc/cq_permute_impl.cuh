@@ -2,7 +2,7 @@
 // quantisation), templated on the 16-bit token type; instantiated for bf16
 // and fp16 by cq_permute_bf16.cu / cq_permute_f16.cu.
 //
-// One CTA per source token (r, i). Warp 0 turns each slot's arrival ordinal
+// permute_kernel: one CTA per source token (r, i). Warp 0 turns each slot's arrival ordinal
 // into its global row (rank base + first row of the (expert slot, source)
 // block within the rank + ordinal: the address rule of "MoeDistributeDispatch
 // 和MoeDistributeCombine算子设计介绍" §3.4.2 with the source block folded into the
@@ -16,12 +16,17 @@
 //   mode 0  the 16-bit row travels unchanged
 //   mode 1  static: int8 = RNE(x * scales)
 //   mode 2  per token: s = 127 / max|x*scales|, int8 = RNE(x*scales * s), carry 1/s
-//   mode 3  per 128-group: s = 448 / max|x*scales|, e4m3 = RNE(x*scales * s), carry 1/s
-//   mode 4  mx: per 32-block, e = floor(log2 max|x|) - 8, e4m3 of x / 2^e, e8m0 e+127
-//   mode 5  mx clip: per 32-block, e = ceil(log2(max(max|x|, 1e-4) / 448)), idem
+//   mode 3  per 128-group: s = F / max|x*scales|, fp8 = RNE(x*scales * s), carry 1/s
+//   mode 4  mx: per 32-block, e = floor(log2 max|x|) - emax, fp8 of x / 2^e, e8m0 e+127
+//   mode 5  mx clip: per 32-block, e = ceil(log2(max(max|x|, 1e-4) / F)), idem
+// with fp8 = e4m3fn (F = 448, emax = 8) or e5m2 (F = 57344, emax = 15).
 // "scales" (smooth) is one row per expert, one row for all, or one scalar.
+// With one smooth row per expert the rows are quantised expert by expert
+// instead (index_kernel + smooth_rows_kernel, further down).
 // Arithmetic is single IEEE binary32 operations (explicit _rn intrinsics, no
 // contraction), so codes and scales are reproducible bit for bit.
+// Page tags ([DV3], [DSN], [LLD], [PERF]) name the source pages listed at the
+// top of include/cq.h.
 #pragma once
 
 #include <cuda_bf16.h>

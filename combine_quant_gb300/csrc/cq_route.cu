@@ -16,6 +16,8 @@
 // expert_token_nums[d] and each (slot, source) block's first row counted from
 // the start of rank d. The last of these CTAs (one atomic counter, no spin)
 // prefix-sums the W rank totals into the rank bases.
+// Page tags ([DV3], [DSN], [LLD], [PERF]) name the source pages listed at the
+// top of include/cq.h.
 #include "cq_internal.cuh"
 
 namespace cq {

@@ -11,6 +11,8 @@
  * every float operation below is one IEEE binary32 operation rounded to
  * nearest-even, and fmaf() is the single-rounding fused multiply-add.
  */
+/* Page tags ([DV3], [DSN], [LLD], [PERF]) name the source pages listed at the
+ * top of cq_oracle.h. */
 #include "cq_oracle.h"
 
 #include <math.h>

@@ -1,5 +1,7 @@
 """Pins for the oracle's combine-side int8 block quantisation and the
 dequantising combine ([PERF] Int8QuantProcess / Int8DequantProcess)."""
+# Page tags ([DV3], [DSN], [LLD], [PERF]) name the source pages listed at the
+# top of include/cq.h.
 import json
 import os
 

@@ -4,6 +4,8 @@ Each test checks the oracle against something other than itself: values the
 design page prints, a hand-worked case, a brute-force recount, a sort-based
 re-derivation of the layout, or the page's own position / address formulas.
 """
+# Page tags ([DV3], [DSN], [LLD], [PERF]) name the source pages listed at the
+# top of include/cq.h.
 import json
 import os
 
