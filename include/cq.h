@@ -25,8 +25,10 @@
  *   - Return 0 (CQ_OK) or a negative CQ_ERR_* code. Argument errors are found
  *     on the host before anything is enqueued; nothing is enqueued then.
  *   - Data-dependent problems found on the device (an out-of-range expert
- *     id, a 1-D mask that is not a prefix) never trap: they set sticky bits in
- *     the workspace status word, read with cq_read_status.
+ *     id, a 1-D mask that is not a prefix, a bounded wait that gave up) never
+ *     trap: they set sticky bits in the workspace status word, read with
+ *     cq_read_status (the combine kernels, which take no workspace, in a
+ *     per-device word read with cq_read_combine_status).
  *
  * Notation: W = ep_world_size, M = moe_expert_num, S = shared_expert_num,
  * S_r = shared_expert_rank_num, L = M / (W - S_r) experts per MoE rank,
@@ -56,7 +58,7 @@ typedef struct cq_config {
   int32_t max_bs;                 /* BS in [1, 512], tokens per rank (maximum) */
   int32_t topk;                   /* K in [1, 16], K <= M + Z + C + Q */
   int32_t hidden;                 /* H in [1024, 8192]; this build needs H % 16 == 0
-                                     (H % 32 == 0 for quant_mode 5) */
+                                     (H % 32 == 0 for quant_mode 4 and 5) */
   int32_t global_bs;              /* 0 or BS * W ([DV3] global_bs) */
   int32_t quant_mode;             /* 0 none, 1 static int8, 2 per-token int8, 3 per-128-group
                                      fp8, 4 mx fp8, 5 mx-clip fp8 ([LLD] 计算公式) */
