@@ -7,7 +7,8 @@ C ABI declared in include/cq.h). This package is its thin Python binding:
 synthetic inputs; ``build`` compiles the library in-tree.
 """
 from .api import (Config, DispatchResult, alloc_dispatch_outputs, alloc_workspace,  # noqa: F401
-                  assist_views, combine, combine_q8, combine_quant, cq_combine, cq_combine_q8,
+                  assist_views, check_bounded_wait, combine, combine_q8, combine_quant,
+                  cq_check_bounded_wait, cq_combine, cq_combine_q8,
                   cq_combine_quant, cq_dispatch, cq_dispatch_noalloc, cq_dispatch_permute,
                   cq_dispatch_route, cq_read_combine_status, cq_read_status, dispatch,
                   dispatch_noalloc, dispatch_permute, dispatch_route, moe_combine, moe_dispatch,

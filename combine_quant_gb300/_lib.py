@@ -39,7 +39,7 @@ EXPORTS = (
     "cq_assist_info_size", "cq_workspace_size", "cq_workspace_init", "cq_dispatch",
     "cq_dispatch_route", "cq_dispatch_permute", "cq_combine", "moe_dispatch", "moe_combine",
     "cq_read_status", "cq_strerror", "cq_dispatch_noalloc", "cq_combine_quant", "cq_combine_q8",
-    "cq_read_combine_status",
+    "cq_read_combine_status", "cq_check_bounded_wait",
 )
 
 
@@ -85,6 +85,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "moe_combine": ([cfgp] + [P] * 8 + [i32, P, P], ctypes.c_int),
         "cq_read_status": ([P, P, P], ctypes.c_int),
         "cq_read_combine_status": ([P, P], ctypes.c_int),
+        "cq_check_bounded_wait": ([P, P, P], ctypes.c_int),
         "cq_dispatch_noalloc": ([cfgp] + [P] * 13, ctypes.c_int),
         "cq_combine_quant": ([cfgp] + [P] * 5, ctypes.c_int),
         "cq_combine_q8": ([cfgp] + [P] * 9 + [i32, P, P], ctypes.c_int),

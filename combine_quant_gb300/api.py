@@ -360,6 +360,18 @@ def read_combine_status(device=None) -> int:
     return int(st.value)
 
 
+def check_bounded_wait(device=None) -> tuple[int, float]:
+    """Run the library's bounded wait on a barrier nothing completes
+    (cq_check_bounded_wait): returns (gave_up, seconds)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    gave_up, secs = ctypes.c_uint32(0), ctypes.c_double(0.0)
+    with torch.cuda.device(dev):
+        rc = _lib.load().cq_check_bounded_wait(ctypes.byref(gave_up), ctypes.byref(secs),
+                                               _stream(dev))
+    _lib.check(rc, "cq_check_bounded_wait")
+    return int(gave_up.value), float(secs.value)
+
+
 def assist_views(cfg: Config, assist_info: torch.Tensor):
     """Views into assist_info: rows [R_max, 4], inv [W, BS, NS], rank_row_base [W+1]."""
     R, W, BS, NS = cfg.max_rows, cfg.ep_world_size, cfg.max_bs, cfg.num_slots
@@ -379,3 +391,4 @@ cq_combine_quant = combine_quant
 cq_combine_q8 = combine_q8
 cq_read_status = read_status
 cq_read_combine_status = read_combine_status
+cq_check_bounded_wait = check_bounded_wait

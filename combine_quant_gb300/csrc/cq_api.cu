@@ -8,6 +8,9 @@
 // top of include/cq.h.
 #include <cuda_runtime.h>
 
+#include <chrono>
+
+#include "cq_async.cuh"
 #include "cq_internal.cuh"
 
 using cq::Dims;
@@ -355,6 +358,41 @@ int cq_read_combine_status(uint32_t* status, void* stream) {
   return cq::read_combine_status(status, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? CQ_OK
              : CQ_ERR_CUDA;
+}
+
+namespace {
+// One thread waits, with the limits every kernel of the library uses, on an
+// mbarrier phase that nothing completes, and records whether it gave up.
+__device__ uint32_t g_wait_probe;
+__global__ void bounded_wait_probe() {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  cq::async::mbar_init(&bar, 1);
+  cq::async::mbar_fence_init();
+  g_wait_probe = cq::async::mbar_wait(&bar, 0) ? 0u : 1u;
+}
+}  // namespace
+
+int cq_check_bounded_wait(uint32_t* gave_up, double* seconds, void* stream) {
+  if (!gave_up || !seconds) return CQ_ERR_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const uint32_t zero = 0;
+  if (cudaMemcpyToSymbolAsync(g_wait_probe, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, s) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return CQ_ERR_CUDA;
+  const auto t0 = std::chrono::steady_clock::now();
+  bounded_wait_probe<<<1, 32, 0, s>>>();
+  if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
+    return CQ_ERR_CUDA;
+  *seconds = std::chrono::duration<double>(std::chrono::steady_clock::now() - t0).count();
+  uint32_t v = 0;
+  if (cudaMemcpyFromSymbolAsync(&v, g_wait_probe, sizeof v, 0, cudaMemcpyDeviceToHost, s) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return CQ_ERR_CUDA;
+  *gave_up = v;
+  return CQ_OK;
 }
 
 const char* cq_strerror(int code) {

@@ -295,6 +295,15 @@ int cq_read_status(void* workspace, uint32_t* status, void* stream);
  * error. */
 int cq_read_combine_status(uint32_t* status, void* stream);
 
+/* Diagnostic (no counterpart in the pages): every wait of a kernel in this
+ * library on its own bulk copies gives up after about one second (or a cap on
+ * polls), sets CQ_ST_TIMEOUT and lets the kernel end, instead of hanging the
+ * device. This call runs that same wait on a barrier phase that nothing
+ * completes, on `stream`, and synchronises: *gave_up = 1 when the wait ended
+ * by its limit, *seconds = the host-measured duration of the launch. The
+ * device stays usable afterwards. CQ_ERR_ARG for NULL outputs. */
+int cq_check_bounded_wait(uint32_t* gave_up, double* seconds, void* stream);
+
 /* Static description of an error code. */
 const char* cq_strerror(int code);
 

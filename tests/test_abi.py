@@ -154,6 +154,7 @@ def test_host_errors_before_any_device_work(lib):
     assert lib.cq_combine(_c(cfg), *([fake] * 8), 2, fake, None) == _lib.CQ_ERR_ARG
     assert lib.cq_read_status(None, None, None) == _lib.CQ_ERR_ARG
     assert lib.cq_read_combine_status(None, None) == _lib.CQ_ERR_ARG
+    assert lib.cq_check_bounded_wait(None, None, None) == _lib.CQ_ERR_ARG
     assert lib.cq_workspace_init(None, 0, None) == _lib.CQ_ERR_ARG
     for code in (0, -1, -2, -3, -4, -99):
         assert isinstance(lib.cq_strerror(code), bytes)
