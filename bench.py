@@ -43,12 +43,12 @@ L2_FLUSH_BYTES = 256 << 20
 # the SHA-256 of the kernel's source file when it was captured; reported only
 # while the source is unchanged.
 NCU_TRAFFIC = {
-    # profiles/dsv3_kernels_ncu_full.md: read 470.089984 MB + write 47.944192 MB
-    "combine": {"bytes_per_launch": 518034176,
-                "src_sha": "cd4cf4163580efe2916382351b2735207d97f845ee81463e77dd3ec2cffd0db7"},
-    # read 59.22944 MB + write 175.434752 MB
-    "permute": {"bytes_per_launch": 234664192,
-                "src_sha": "a63756706a4883852c57624dbc8ca85756979d75c86f436a9d4a7af20b2223b3"},
+    # profiles/dsv3_kernels_ncu_full.md: read 470.070528 MB + write 48.177664 MB
+    "combine": {"bytes_per_launch": 518248192,
+                "src_sha": "702576bc1f87fe0463459c6f192f59f691affa006a6f3a7a979ad03ad61fa7d7"},
+    # read 59.218432 MB + write 175.693056 MB
+    "permute": {"bytes_per_launch": 234911488,
+                "src_sha": "f6199a28a51fd66527fb3db692d8b5429730b1b7e8b5d9a358727364ae79f42c"},
 }
 
 
@@ -206,8 +206,8 @@ def measured_peaks() -> tuple[float, str]:
 
 
 KERNEL_SOURCES = {
-    "permute": ["cq_permute_impl.cuh", "cq_permute_bf16.cu", "cq_internal.cuh"],
-    "combine": ["cq_combine.cu", "cq_internal.cuh"],
+    "permute": ["cq_permute_impl.cuh", "cq_permute_bf16.cu", "cq_internal.cuh", "cq_async.cuh"],
+    "combine": ["cq_combine.cu", "cq_internal.cuh", "cq_async.cuh"],
 }
 
 
