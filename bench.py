@@ -374,6 +374,8 @@ def run_reference(args):
     from combine_quant_gb300 import workloads
 
     wl = workloads.WORKLOADS[args.workload]()
+    if args.quant_mode is not None:
+        wl = wl.with_mode(args.quant_mode)
     W, BS = wl.cfg["ep_world_size"], wl.cfg["max_bs"]
     # Each step is a bounded sample: enough tokens that K + W steps take about
     # a minute of host time in total.
