@@ -379,14 +379,14 @@ __device__ __forceinline__ float quantise(const float (&f)[2][16], const Units& 
 // Slot k of token tok (source rank r): its global row = first row of the
 // destination rank + first row of the (expert slot, source) block inside the
 // rank + arrival ordinal. Writes the inverse-map entry and, for a dispatched
-// slot, the (src, token, slot) row record and the carried weight. Returns the
-// row (-1 if none) and the slot's smooth-table row in `srow`.
-__device__ __forceinline__ int map_slot(const PermuteArgs& a, int64_t tok, int r, int k,
+// slot, the (src, token, slot) row record and the carried weight. `e` is the
+// slot's arrival ordinal (eidx), loaded by the caller. Returns the row (-1 if
+// none) and the slot's smooth-table row in `srow`.
+__device__ __forceinline__ int map_slot(const PermuteArgs& a, int64_t tok, int r, int k, int e,
                                         int& srow) {
   const Dims& d = a.d;
   srow = 0;
   if (k >= d.NS) return -1;
-  const int e = a.ws.eidx[tok * d.NS + k];
   int code = e, row = -1;
   if (e >= 0) {
     int g, dst;  // global expert slot, destination rank
@@ -465,10 +465,60 @@ __global__ void __launch_bounds__(256) permute_kernel(PermuteArgs a) {
   }
   if (prefetched) load_row();
   griddep_wait();  // routing outputs (ordinals, offsets) are read from here on
+  // Warp 0 starts loading the slots' ordinals; the mapping finishes after the
+  // row is staged, so its latency overlaps the quantisation.
+  const int e_slot = threadIdx.x < 32 && lane < d.NS ? a.ws.eidx[tok * d.NS + lane] : CQ_INV_NONE;
 
+  // Staged row layout: code row (2H bytes in mode 0, else H), then the scale
+  // row padded to 16 bytes.
+  const int code_bytes = MODE == 0 ? 2 * H : H;
+  const int scale_bytes = MODE == 3 ? 4 * d.G3 : ((MODE == 4 || MODE == 5) ? d.SC : 0);
+  char* const dyn = static_cast<char*>(a.dynamic_scales);
+  char* const out = static_cast<char*>(a.expand_x);
+
+  // The code row (and scale row) every routed row gets, into s_stage; mode 2
+  // returns the carried scale in warp 0. All threads take part.
+  auto stage = [&]() -> float {
+    float carried = 0.f;
+    if (MODE == 0) {
+      // The 16-bit row itself travels ([DV3] 情形 1).
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int u = threadIdx.x + q * blockDim.x;
+        if (U.ok[q]) {
+          st_shared_v4(s_stage + 32 * u, U.v[q][0]);
+          st_shared_v4(s_stage + 32 * u + 16, U.v[q][1]);
+        }
+      }
+    } else {
+      // One quantisation per token: every routed row gets the same codes.
+      const float* srow = SM == kSharedRow ? a.smooth : nullptr;
+      const float scalar = SM == kScalar ? a.smooth[0] : 0.f;
+      float f[2][16];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int u = threadIdx.x + q * blockDim.x;
+        if (U.ok[q]) {
+          unit_values<T, SM>(U.v[q], srow, scalar, u, f[q]);
+        } else {
+#pragma unroll
+          for (int t = 0; t < 16; ++t) f[q][t] = 0.f;
+        }
+      }
+      carried = quantise<Q>(f, U, s_stage, s_stage + code_bytes, s_red[0], blockDim.x);
+      if (MODE == 5 || MODE == 4) {
+        if (threadIdx.x == 0 && d.SC > (units >> 1)) s_stage[code_bytes + (units >> 1)] = 0;
+      }
+    }
+    fence_proxy_async_smem();  // staging writes before the bulk copies read them
+    return carried;
+  };
+
+  float carried = 0.f;
+  if (prefetched) carried = stage();
   if (threadIdx.x < 32) {
     int srow;
-    const int row = map_slot(a, tok, r, lane, srow);
+    const int row = map_slot(a, tok, r, lane, e_slot, srow);
     const unsigned bal = __ballot_sync(kFull, row >= 0);
     if (row >= 0) {
       const int pos = __popc(bal & ((1u << lane) - 1u));
@@ -480,65 +530,22 @@ __global__ void __launch_bounds__(256) permute_kernel(PermuteArgs a) {
   __syncthreads();
   const int nrows = s_nrows;
   if (nrows == 0) return;
-  if (!prefetched) load_row();  // routing found rows the inputs did not predict
-
-  // Staged row layout: code row (2H bytes in mode 0, else H), then the scale
-  // row padded to 16 bytes.
-  const int code_bytes = MODE == 0 ? 2 * H : H;
-  const int scale_bytes = MODE == 3 ? 4 * d.G3 : ((MODE == 4 || MODE == 5) ? d.SC : 0);
-  const int stride = code_bytes + ((scale_bytes + 15) & ~15);
-  char* const dyn = static_cast<char*>(a.dynamic_scales);
-  char* const out = static_cast<char*>(a.expand_x);
-
-  if (MODE == 0) {
-    // The 16-bit row itself travels ([DV3] 情形 1): stage it once.
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int u = threadIdx.x + q * blockDim.x;
-      if (U.ok[q]) {
-        st_shared_v4(s_stage + 32 * u, U.v[q][0]);
-        st_shared_v4(s_stage + 32 * u + 16, U.v[q][1]);
-      }
-    }
-    fence_proxy_async_smem();
+  if (!prefetched) {  // routing found rows the inputs did not predict
+    load_row();
+    carried = stage();
     __syncthreads();
-    if (threadIdx.x == 0) {
-      for (int n = 0; n < nrows; ++n)
-        bulk_store(out + (int64_t)s_row[n] * code_bytes, s_stage, (uint32_t)code_bytes);
-      bulk_commit();
-      bulk_wait_read<0>();
+  }
+  if (threadIdx.x == 0) {
+    for (int n = 0; n < nrows; ++n) {
+      const int64_t row = s_row[n];
+      bulk_store(out + row * code_bytes, s_stage, (uint32_t)code_bytes);
+      if (scale_bytes && a.scale_rows_bulk)
+        bulk_store(dyn + row * scale_bytes, s_stage + code_bytes, (uint32_t)scale_bytes);
     }
-  } else {
-    // One quantisation per token: every routed row gets the same codes.
-    const float* srow = SM == kSharedRow ? a.smooth : nullptr;
-    const float scalar = SM == kScalar ? a.smooth[0] : 0.f;
-    float f[2][16];
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int u = threadIdx.x + q * blockDim.x;
-      if (U.ok[q]) {
-        unit_values<T, SM>(U.v[q], srow, scalar, u, f[q]);
-      } else {
-#pragma unroll
-        for (int t = 0; t < 16; ++t) f[q][t] = 0.f;
-      }
-    }
-    const float carried = quantise<Q>(f, U, s_stage, s_stage + code_bytes, s_red[0], blockDim.x);
-    if (MODE == 5 || MODE == 4) {
-      if (threadIdx.x == 0 && d.SC > (units >> 1)) s_stage[code_bytes + (units >> 1)] = 0;
-    }
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      for (int n = 0; n < nrows; ++n) {
-        const int64_t row = s_row[n];
-        bulk_store(out + row * code_bytes, s_stage, (uint32_t)code_bytes);
-        if (scale_bytes && a.scale_rows_bulk)
-          bulk_store(dyn + row * scale_bytes, s_stage + code_bytes, (uint32_t)scale_bytes);
-      }
-      bulk_commit();
-      bulk_wait_read<0>();
-    }
+    bulk_commit();
+    bulk_wait_read<0>();
+  }
+  if (MODE != 0) {
     if (MODE == 2 && threadIdx.x < nrows)
       reinterpret_cast<float*>(dyn)[s_row[threadIdx.x]] = carried;
     if (scale_bytes && !a.scale_rows_bulk) {  // scale rows not 16-byte sized / aligned
@@ -577,7 +584,9 @@ __global__ void __launch_bounds__(256) index_kernel(PermuteArgs a) {
   if (tok < (int64_t)a.d.W * a.d.BS) {
     const int r = (int)(tok / a.d.BS);
     int srow;
-    const int row = map_slot(a, tok, r, threadIdx.x & 31, srow);
+    const int k = threadIdx.x & 31;
+    const int e = k < a.d.NS ? a.ws.eidx[tok * a.d.NS + k] : CQ_INV_NONE;
+    const int row = map_slot(a, tok, r, k, e, srow);
     if (row >= 0) a.ws.row_src[row] = make_int2((int)tok, srow);
   }
   griddep_launch_dependents();
