@@ -185,8 +185,10 @@ __device__ __forceinline__ uint4 q8_16_direct(const float (&v)[16]) {
 
 // Two binary32 products in one packed instruction, each lane rounded to
 // nearest even on its own (the same results as two scalar _rn products). Use
-// only where no add follows the product: ptxas may fuse a packed multiply
-// and a packed add into one multiply-add with a single rounding.
+// only where no packed add follows the product: ptxas may fuse a packed
+// multiply and a packed add into one multiply-add with a single rounding
+// (scalar _rn adds after it are not fused; a GPU test on rounding ties checks
+// that).
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
   float2 r;
   asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
@@ -196,27 +198,28 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
   return r;
 }
 
-// Four int8 codes RNE(fl(v * m)) for products that lie in [-128, 128]:
+// Sixteen int8 codes RNE(fl(v * m)) for products that lie in [-128, 128]:
 // adding 1.5 * 2^23 gives a sum whose ulp is 1, so its low mantissa bits
 // hold the nearest-even integer n, and the low byte of its bit pattern is n
-// in two's complement. Three byte permutes pack the four codes.
-// The product and the add are scalar _rn operations, which are never fused:
-// a fused multiply-add would round x * m once, straight to an integer, and
-// differ from RNE(fl(x * m)) where fl(x * m) is an exact tie (ptxas does
-// contract the packed f32x2 forms).
-__device__ __forceinline__ uint32_t q8_magic(float v, float m) {
-  return __float_as_uint(__fadd_rn(__fmul_rn(v, m), 12582912.f));  // + 1.5 * 2^23
-}
-
-__device__ __forceinline__ uint32_t q8x4_magic(float a, float b, float c, float d, float m) {
-  return __byte_perm(__byte_perm(q8_magic(a, m), q8_magic(b, m), 0x0040),
-                     __byte_perm(q8_magic(c, m), q8_magic(d, m), 0x0040), 0x5410);
-}
-
+// in two's complement. Three byte permutes pack four codes.
+// The products are packed f32x2 multiplies, each lane rounded on its own;
+// the adds are scalar _rn operations, and that mixed pair is not fused. A
+// fused multiply-add would round v * m once, straight to an integer, and
+// differ from RNE(fl(v * m)) where fl(v * m) is a tie that the exact product
+// is not (a packed multiply followed by a packed add does get contracted).
 __device__ __forceinline__ uint4 q8_16_magic(const float (&v)[16], float m) {
-  return make_uint4(q8x4_magic(v[0], v[1], v[2], v[3], m), q8x4_magic(v[4], v[5], v[6], v[7], m),
-                    q8x4_magic(v[8], v[9], v[10], v[11], m),
-                    q8x4_magic(v[12], v[13], v[14], v[15], m));
+  uint32_t o[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const float2 p0 = mul2(make_float2(v[4 * t], v[4 * t + 1]), make_float2(m, m));
+    const float2 p1 = mul2(make_float2(v[4 * t + 2], v[4 * t + 3]), make_float2(m, m));
+    const uint32_t c0 = __float_as_uint(__fadd_rn(p0.x, 12582912.f));  // + 1.5 * 2^23
+    const uint32_t c1 = __float_as_uint(__fadd_rn(p0.y, 12582912.f));
+    const uint32_t c2 = __float_as_uint(__fadd_rn(p1.x, 12582912.f));
+    const uint32_t c3 = __float_as_uint(__fadd_rn(p1.y, 12582912.f));
+    o[t] = __byte_perm(__byte_perm(c0, c1, 0x0040), __byte_perm(c2, c3, 0x0040), 0x5410);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 template <bool E5>
@@ -234,15 +237,28 @@ __device__ __forceinline__ uint4 fp8_16(const float (&v)[16], float mult) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// Max of one float per thread over the first nt threads of the block
-// (NaN-propagating when NAN_OUT); nt is a multiple of 32, at most 256 (8
-// warps). The threads meet at __syncthreads, or (NAMED, when other warps of
-// the block do not take part) at named barrier 1. `buf` holds >= 8 floats and
-// must not be reused by another block_max until the next such barrier.
+// Max over the 32 lanes of a warp of non-negative (or NaN) values: NaN
+// propagated (NAN_OUT) or ignored, as in max3.
+template <bool NAN_OUT = false>
+__device__ __forceinline__ float warp_max(float v) {
+  float r;
+  if (NAN_OUT) {
+    asm volatile("redux.sync.max.NaN.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  } else {
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  }
+  return r;
+}
+
+// Max of one non-negative (or NaN) float per thread over the first nt
+// threads of the block (NaN-propagating when NAN_OUT); nt is a multiple of
+// 32, at most 256 (8 warps). The threads meet at __syncthreads, or (NAMED,
+// when other warps of the block do not take part) at named barrier 1. `buf`
+// holds >= 8 floats and must not be reused by another block_max until the
+// next such barrier.
 template <bool NAN_OUT = false, bool NAMED = false>
 __device__ __forceinline__ float block_max(float v, float* buf, int nt) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = max3<NAN_OUT>(v, __shfl_xor_sync(kFull, v, o), v);
+  v = warp_max<NAN_OUT>(v);
   const int lane = threadIdx.x & 31;
   if (lane == 0) buf[threadIdx.x >> 5] = v;
   if (NAMED) {
@@ -250,11 +266,7 @@ __device__ __forceinline__ float block_max(float v, float* buf, int nt) {
   } else {
     __syncthreads();
   }
-  // Every group of 8 lanes reduces the same (up to) 8 warp maxima.
-  float m = (lane & 7) < (nt >> 5) ? buf[lane & 7] : 0.f;
-#pragma unroll
-  for (int o = 4; o > 0; o >>= 1) m = max3<NAN_OUT>(m, __shfl_xor_sync(kFull, m, o), m);
-  return m;
+  return warp_max<NAN_OUT>(lane < (nt >> 5) ? buf[lane] : 0.f);
 }
 
 // Thread-owned part of the token row: two 16-element units (32 bytes each).

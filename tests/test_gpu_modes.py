@@ -154,3 +154,61 @@ def test_e5m2_extremes_and_fp16(mode):
     wl.x = workloads.to_bf16_bits(x)
     gh.full_parity(wl)
     gh.full_parity(workloads.as_fp16(_e5(_base("tiny"), mode)))
+
+
+def _tie_maxima():
+    """Row maxima A (bf16, in [1, 127]) for which the product of A/2 with the
+    binary32 scale s = 127/A rounds onto the tie 63.5 without being 63.5
+    exactly: a single-rounding multiply-add would round that product to 63 or
+    64 by its exact value, the two-step rounding of the method gives 64."""
+    bits = np.arange(1, 0x7f80, dtype=np.uint32) << 16
+    vals = bits.view(np.float32)
+    out = []
+    for A in vals[(vals >= 1.0) & (vals <= 127.0)]:
+        s = np.float32(127.0) / A
+        h = np.float32(A / 2)
+        p = np.float32(h * s)
+        if p == np.float32(63.5) and np.float64(h) * np.float64(s) != 63.5:
+            out.append(float(A))
+    return np.array(out, np.float32)
+
+
+@pytest.mark.parametrize("kind", [None, 0, 1, 2])
+def test_mode2_rounding_ties(kind):
+    """Per-token int8 codes on products that sit on .5 ties: rows whose max A
+    makes fl(A/2 * fl(127/A)) a tie reached by rounding (about 600 such A), and
+    rows with max 127 (scale 1) holding every k + 0.5. Smooth scales are all
+    ones, so every smooth shape (kind 0: the per-expert-smooth kernel) meets
+    the same products; the codes must be the round-to-nearest-even of the
+    rounded product, bit for bit with the oracle."""
+    wl = _base("dsv3_small")
+    x = workloads.bf16_bits_to_f32(wl.x).copy()
+    W, BS, H = x.shape
+    maxima = _tie_maxima()
+    assert maxima.size > 500
+    rng = np.random.default_rng(7)
+    halves = (np.arange(127, dtype=np.float32) + np.float32(0.5))  # 0.5 .. 126.5, exact in bf16
+    n = 0
+    for r in range(W):
+        for i in range(BS):
+            if n % 4 == 3:
+                row = np.resize(np.concatenate([halves, -halves]), H).astype(np.float32)
+                row[H - 1] = 127.0
+                rng.shuffle(row)
+            else:
+                A = maxima[n % maxima.size]
+                h = np.float32(A / 2)
+                row = np.where(np.arange(H) % 2 == 0, h, -h).astype(np.float32)
+                # a third of the row: random values below the max
+                fill = rng.integers(0, H, H // 3)
+                row[fill] = (rng.uniform(-1, 1, fill.size) * A).astype(np.float32)
+                row[rng.integers(0, H)] = A if n % 2 == 0 else -A
+            x[r, i] = row
+            n += 1
+    wl.x = workloads.to_bf16_bits(x)
+    if kind is None:
+        gh.full_parity(_with(wl, 2))
+    else:
+        sm = _smooth(wl, kind)
+        sm[...] = 1.0
+        gh.full_parity(_with(wl, 2, sm, kind))

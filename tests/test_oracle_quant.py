@@ -197,3 +197,36 @@ def test_mode0_is_copy(oracle_lib):
     xb = np.random.default_rng(5).integers(0, 65535, 1024).astype(np.uint16)
     codes, scale = oracle.quant_row(0, xb)
     assert np.array_equal(codes, xb) and scale is None
+
+
+def test_int8_two_step_rounding_on_ties(oracle_lib):
+    """The method rounds the product to binary32 first and then to an
+    integer, nearest even ("low_latency_dispatch" 计算公式, quant_mode 2). For
+    rows with max A the code of A/2 is RNE(fl(A/2 * fl(127/A))); wherever
+    that rounded product is the tie 63.5 (exact value off by less than an
+    ulp), the code is 64, while rounding the exact product once would give 63
+    where it lies below 63.5. Exact ties k + 0.5 at scale 1 go to even."""
+    bits = np.arange(1, 0x7f80, dtype=np.uint32) << 16
+    vals = bits.view(np.float32)
+    below = above = 0
+    for A in vals[(vals >= 1.0) & (vals <= 127.0)]:
+        s = np.float32(127.0) / A
+        h = np.float32(A / 2)
+        exact = np.float64(h) * np.float64(s)
+        if np.float32(h * s) != np.float32(63.5) or exact == 63.5:
+            continue
+        row = np.zeros(256, np.float32)
+        row[0], row[1], row[2] = A, h, -h
+        codes, scale = oracle.quant_row(2, to_bf16_bits(row))
+        assert codes[0] == 127 and codes[1] == 64 and codes[2] == -64, A
+        below += exact < 63.5
+        above += exact > 63.5
+    assert below > 100 and above > 100  # both sides of the tie are exercised
+    halves = np.arange(127, dtype=np.float32) + np.float32(0.5)
+    row = np.zeros(256, np.float32)
+    row[:127] = halves
+    row[127] = 127.0
+    codes, _ = oracle.quant_row(2, to_bf16_bits(row))
+    k = np.arange(127)
+    assert np.array_equal(codes[:127], np.where(k % 2 == 0, k, k + 1))  # k + 0.5 -> even
+    assert codes[127] == 127
