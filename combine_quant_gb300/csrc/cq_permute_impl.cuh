@@ -187,8 +187,8 @@ __device__ __forceinline__ uint4 q8_16_direct(const float (&v)[16]) {
 // nearest even on its own (the same results as two scalar _rn products). Use
 // only where no packed add follows the product: ptxas may fuse a packed
 // multiply and a packed add into one multiply-add with a single rounding
-// (scalar _rn adds after it are not fused; a GPU test on rounding ties checks
-// that).
+// (a packed fma by 1.0 after it is not merged; a GPU test on rounding ties
+// checks that).
 __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
   float2 r;
   asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
@@ -198,25 +198,36 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
   return r;
 }
 
+// p + 1.5 * 2^23 for both lanes, as a packed fma by 1.0: p * 1 is exact, so
+// each lane is the one rounding of the sum, as an add would give.
+__device__ __forceinline__ float2 addmagic2(float2 p) {
+  float2 r;
+  asm("{\n .reg .b64 rp, rm, ro, rd;\n mov.b64 rp, {%2, %3};\n mov.b64 rm, {%4, %4};\n"
+      " mov.b64 ro, {%5, %5};\n fma.rn.f32x2 rd, rp, ro, rm;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(r.x), "=f"(r.y)
+      : "f"(p.x), "f"(p.y), "f"(12582912.f), "f"(1.0f));
+  return r;
+}
+
 // Sixteen int8 codes RNE(fl(v * m)) for products that lie in [-128, 128]:
 // adding 1.5 * 2^23 gives a sum whose ulp is 1, so its low mantissa bits
 // hold the nearest-even integer n, and the low byte of its bit pattern is n
 // in two's complement. Three byte permutes pack four codes.
 // The products are packed f32x2 multiplies, each lane rounded on its own;
-// the adds are scalar _rn operations, and that mixed pair is not fused. A
-// fused multiply-add would round v * m once, straight to an integer, and
-// differ from RNE(fl(v * m)) where fl(v * m) is a tie that the exact product
-// is not (a packed multiply followed by a packed add does get contracted).
+// the adds are packed fmas by 1.0, which ptxas keeps apart from the products.
+// A multiply-add fused from the two would round v * m once, straight to an
+// integer, and differ from RNE(fl(v * m)) where fl(v * m) is a tie that the
+// exact product is not (a packed multiply followed by a packed add does get
+// contracted; a GPU test on rounding ties checks these codes).
 __device__ __forceinline__ uint4 q8_16_magic(const float (&v)[16], float m) {
   uint32_t o[4];
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
     const float2 p0 = mul2(make_float2(v[4 * t], v[4 * t + 1]), make_float2(m, m));
     const float2 p1 = mul2(make_float2(v[4 * t + 2], v[4 * t + 3]), make_float2(m, m));
-    const uint32_t c0 = __float_as_uint(__fadd_rn(p0.x, 12582912.f));  // + 1.5 * 2^23
-    const uint32_t c1 = __float_as_uint(__fadd_rn(p0.y, 12582912.f));
-    const uint32_t c2 = __float_as_uint(__fadd_rn(p1.x, 12582912.f));
-    const uint32_t c3 = __float_as_uint(__fadd_rn(p1.y, 12582912.f));
+    const float2 s0 = addmagic2(p0), s1 = addmagic2(p1);
+    const uint32_t c0 = __float_as_uint(s0.x), c1 = __float_as_uint(s0.y);
+    const uint32_t c2 = __float_as_uint(s1.x), c3 = __float_as_uint(s1.y);
     o[t] = __byte_perm(__byte_perm(c0, c1, 0x0040), __byte_perm(c2, c3, 0x0040), 0x5410);
   }
   return make_uint4(o[0], o[1], o[2], o[3]);
