@@ -65,7 +65,7 @@ def parse_args(argv=None):
                     help="also time the oracle on every host core (spawned processes)")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--quant-mode", type=int, default=None,
-                    help="override the workload's quant_mode (0, 2, 5)")
+                    help="override the workload's quant_mode (0-5)")
     ap.add_argument("--combine", choices=["bf16", "int8"], default="bf16",
                     help="combine from bf16 expert outputs, or from int8 ones quantised on the "
                          "expert side (the quantiser is timed separately, outside the step)")
@@ -245,6 +245,23 @@ def _oracle_prepare(wl):
     return route, inv_pool, pool, t_route
 
 
+def _smooth_of(wl, r, i, k):
+    """(row, scalar) smooth arguments of the oracle's quantisation for slot k
+    of token (r, i): the expert's row (shared experts first), the one shared
+    row, or the scalar, as smooth_kind says; none outside modes 1-3."""
+    cfg = wl.cfg
+    if wl.smooth is None or cfg["quant_mode"] not in (1, 2, 3):
+        return None, None
+    kind = cfg.get("smooth_kind", 0)
+    if kind == 2:
+        return None, float(wl.smooth.reshape(-1)[0])
+    if kind == 1:
+        return wl.smooth.reshape(-1), None
+    K = cfg["topk"]
+    s_eff = cfg["shared_expert_num"] if cfg["shared_expert_rank_num"] > 0 else 0
+    return (wl.smooth[s_eff + wl.expert_ids[r, i, k]] if k < K else wl.smooth[k - K]), None
+
+
 def _oracle_tokens(wl, prep, order, budget_s: float):
     """Quantise every dispatched row of each token in `order` and combine the
     token, until the budget is spent. Returns (tokens done, seconds)."""
@@ -259,10 +276,9 @@ def _oracle_tokens(wl, prep, order, budget_s: float):
         for k in range(route.inv.shape[2]):
             row = route.inv[r, i, k]
             if row >= 0:
-                sm = None
-                if wl.smooth is not None and mode == 2:
-                    sm = wl.smooth[wl.expert_ids[r, i, k]] if k < K else wl.smooth[k - K]
-                oracle.quant_row(mode, wl.x[r, i], sm)
+                sm_row, sm_scalar = _smooth_of(wl, r, i, k)
+                oracle.quant_row(mode, wl.x[r, i], sm_row, cfg.get("x_dtype", 0), sm_scalar,
+                                 cfg.get("y_dtype", 0))
         oracle.combine_tokens(cfg, [(r, i)], pool, inv_pool, wl.expert_scales, wl.x,
                               wl.const_alpha1, wl.const_alpha2, wl.const_v)
         done += 1
@@ -434,7 +450,7 @@ def run_cq(args):
     x = tdev(wl.x, torch.bfloat16)
     ids = tdev(wl.expert_ids, torch.int32)
     w = tdev(wl.expert_scales, torch.float32)
-    sm = tdev(wl.smooth, torch.float32) if cfg.quant_mode == 2 else None
+    sm = tdev(wl.smooth, torch.float32) if cfg.quant_mode in (1, 2, 3) else None
     mask = tdev(wl.mask, torch.uint8)
     bpr = tdev(wl.bs_per_rank, torch.int32)
     ws = cq.alloc_workspace(cfg, dev)

@@ -233,6 +233,20 @@ __device__ __forceinline__ uint4 q8_16_magic(const float (&v)[16], float m) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// Sixteen int8 codes RNE(v) for values of magnitude below 127.5 (codes in
+// [-127, 127]), by the same add-and-pack.
+__device__ __forceinline__ uint4 q8_16_add(const float (&v)[16]) {
+  uint32_t o[4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const float2 s0 = addmagic2(make_float2(v[4 * t], v[4 * t + 1]));
+    const float2 s1 = addmagic2(make_float2(v[4 * t + 2], v[4 * t + 3]));
+    o[t] = __byte_perm(__byte_perm(__float_as_uint(s0.x), __float_as_uint(s0.y), 0x0040),
+                       __byte_perm(__float_as_uint(s1.x), __float_as_uint(s1.y), 0x0040), 0x5410);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 template <bool E5>
 __device__ __forceinline__ uint32_t fp8x2(float lo, float hi) {
   return E5 ? e5m2x2(lo, hi) : e4m3x2(lo, hi);
@@ -242,9 +256,11 @@ template <bool E5>
 __device__ __forceinline__ uint4 fp8_16(const float (&v)[16], float mult) {
   uint32_t o[4];
 #pragma unroll
-  for (int t = 0; t < 4; ++t)
-    o[t] = fp8x2<E5>(__fmul_rn(v[4 * t], mult), __fmul_rn(v[4 * t + 1], mult)) |
-           (fp8x2<E5>(__fmul_rn(v[4 * t + 2], mult), __fmul_rn(v[4 * t + 3], mult)) << 16);
+  for (int t = 0; t < 4; ++t) {
+    const float2 p0 = mul2(make_float2(v[4 * t], v[4 * t + 1]), make_float2(mult, mult));
+    const float2 p1 = mul2(make_float2(v[4 * t + 2], v[4 * t + 3]), make_float2(mult, mult));
+    o[t] = fp8x2<E5>(p0.x, p0.y) | (fp8x2<E5>(p1.x, p1.y) << 16);
+  }
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
@@ -337,9 +353,15 @@ __device__ __forceinline__ float quantise(const float (&f)[2][16], const Units& 
   constexpr int kEmax = E5 ? 15 : 8;
   float carried = 0.f;
   if (MODE == 1) {
+    // A thread whose values all lie below 127.5 in magnitude has codes in
+    // [-127, 127]: add-and-pack. Any other value (large, infinite, NaN) sends
+    // the thread to convert-and-saturate.
+    const bool small = max3<true>(max16<true>(f[0]), max16<true>(f[1]), 0.f) < 127.5f;
 #pragma unroll
     for (int q = 0; q < 2; ++q)
-      if (U.ok[q]) put16<GLOBAL>(codes + 16 * (threadIdx.x + q * nt), q8_16_direct(f[q]));
+      if (U.ok[q])
+        put16<GLOBAL>(codes + 16 * (threadIdx.x + q * nt),
+                      small ? q8_16_add(f[q]) : q8_16_direct(f[q]));
   } else if (MODE == 2) {
     // The row max with NaN propagated. A row with neither NaN nor infinity
     // whose 127/max is finite (or whose max is 0) has every product x * s in

@@ -63,9 +63,15 @@ class Workload:
     notes: dict = field(default_factory=dict)
 
     def with_mode(self, mode: int) -> "Workload":
+        """The same inputs under another quant_mode. Modes 1-3 keep the smooth
+        scales; mode 1 (static scales) without any takes one (H,) row of 32.0,
+        which spreads N(0, 1) tokens over the int8 range."""
         cfg = dict(self.cfg)
         cfg["quant_mode"] = int(mode)
-        smooth = self.smooth if mode == 2 else None
+        smooth = self.smooth if mode in (1, 2, 3) else None
+        if mode == 1 and smooth is None:
+            smooth = np.full(cfg["hidden"], 32.0, np.float32)
+            cfg["smooth_kind"] = 1
         return Workload(self.name + f"_m{mode}", cfg, self.x, self.expert_ids,
                         self.expert_scales, smooth, self.mask, self.bs_per_rank,
                         self.const_alpha1, self.const_alpha2, self.const_v, self.seed,

@@ -212,3 +212,33 @@ def test_mode2_rounding_ties(kind):
         sm = _smooth(wl, kind)
         sm[...] = 1.0
         gh.full_parity(_with(wl, 2, sm, kind))
+
+
+@pytest.mark.parametrize("kind,scale", [(0, 1.0), (1, 1.0), (2, 1.0), (2, 37.0), (0, 37.0)])
+def test_mode1_extremes(kind, scale):
+    """Static int8 on values that leave the ordinary range: every tie k + 0.5
+    up to 127.5, the saturation boundary (+-127.5, +-128 and beyond),
+    infinities, NaN and huge values, next to ordinary rows. Smooth scales are
+    all `scale`, so x * scale is exact for scale 1; scale 37 pushes about a
+    quarter of the values past the int8 range, mixing threads whose values
+    all round into [-127, 127] with threads that saturate."""
+    wl = _base("dsv3_small")
+    x = workloads.bf16_bits_to_f32(wl.x).copy()
+    H = x.shape[2]
+    halves = np.arange(-128, 128, dtype=np.float32) + np.float32(0.5)  # -127.5 .. 127.5
+    x[0, 0] = np.resize(halves, H)
+    edge = np.array([127.0, 127.5, -127.5, 128.0, -128.0, 129.0, -130.0, 126.5, -126.5, 255.0],
+                    np.float32)
+    x[0, 1] = np.resize(edge, H)
+    x[0, 2, 3] = np.inf
+    x[0, 3, 5] = -np.inf
+    x[0, 4, 7] = np.nan
+    x[0, 5, ::17] = 1e30
+    x[0, 6, ::5] = -3e38
+    x[1, 0, :] = 127.5
+    x[1, 1, :] = -127.5
+    x[1, 2, H // 2] = 127.5  # one thread's values reach the boundary, the rest are ordinary
+    wl.x = workloads.to_bf16_bits(x)
+    sm = _smooth(wl, kind)
+    sm[...] = scale
+    gh.full_parity(_with(wl, 1, sm, kind))
