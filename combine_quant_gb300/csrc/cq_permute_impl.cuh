@@ -637,7 +637,9 @@ __global__ void __launch_bounds__(256) index_kernel(PermuteArgs a) {
   griddep_launch_dependents();
 }
 
-template <class T, int Q>
+// FULL: the consumer threads hold exactly two units each (H a multiple of
+// 1024), so no unit needs a bounds check.
+template <class T, int Q, bool FULL>
 __global__ void __launch_bounds__(288, 2) smooth_rows_kernel(PermuteArgs a) {
   constexpr int MODE = q_mode(Q);
   __shared__ uint64_t s_full[kXStages];
@@ -727,7 +729,7 @@ __global__ void __launch_bounds__(288, 2) smooth_rows_kernel(PermuteArgs a) {
   // Consumer warps: each row is quantised by all of them together.
   Units U;
 #pragma unroll
-  for (int q = 0; q < 2; ++q) U.ok[q] = (int)threadIdx.x + q * ncons < units;
+  for (int q = 0; q < 2; ++q) U.ok[q] = FULL || (int)threadIdx.x + q * ncons < units;
   float sm[2][16];
   int cur = -1;
   for (int j = 0; j < n_rows; ++j) {
@@ -815,24 +817,28 @@ cudaError_t launch_smooth_rows(const PermuteArgs& a, cudaStream_t s) {
   const int units = a.d.H >> 4;
   int threads = ((units + 1) / 2 + 31) / 32 * 32;
   if (threads < 32) threads = 32;
+  const bool full = units == 2 * threads;
   threads += 32;  // the producer warp
   const size_t smem = (size_t)kXStages * 2 * a.d.H;
-  auto* kern = smooth_rows_kernel<T, Q>;
-  if ((e = prepare_kernel<smooth_rows_kernel<T, Q>>(smem)) != cudaSuccess) return e;
-  // The last occupancy query of this instantiation.
+  auto* kern = full ? smooth_rows_kernel<T, Q, true> : smooth_rows_kernel<T, Q, false>;
+  if ((e = full ? prepare_kernel<smooth_rows_kernel<T, Q, true>>(smem)
+                : prepare_kernel<smooth_rows_kernel<T, Q, false>>(smem)) != cudaSuccess)
+    return e;
+  // The last occupancy query of each instantiation.
   static std::mutex mu;
-  static size_t occ_smem = 0;
-  static int occ_threads = 0, occ_blocks = 0;
+  static size_t occ_smem[2] = {0, 0};
+  static int occ_threads[2] = {0, 0}, occ_blocks[2] = {0, 0};
   int blocks;
   {
     std::lock_guard<std::mutex> lock(mu);
-    if (occ_threads != threads || occ_smem != smem) {
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_blocks, kern, threads, smem);
+    const int f = full ? 1 : 0;
+    if (occ_threads[f] != threads || occ_smem[f] != smem) {
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_blocks[f], kern, threads, smem);
       if (e != cudaSuccess) return e;
-      occ_threads = threads;
-      occ_smem = smem;
+      occ_threads[f] = threads;
+      occ_smem[f] = smem;
     }
-    blocks = occ_blocks;
+    blocks = occ_blocks[f];
   }
   if (blocks < 1) return cudaErrorInvalidConfiguration;
   int64_t grid = (int64_t)sm_count() * blocks;

@@ -242,3 +242,12 @@ def test_mode1_extremes(kind, scale):
     sm = _smooth(wl, kind)
     sm[...] = scale
     gh.full_parity(_with(wl, 1, sm, kind))
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_per_expert_smooth_ragged_hidden(mode):
+    """One smooth row per expert with H = 1040 (65 units of 16): the
+    per-expert-smooth kernel's variant whose last consumer threads hold one
+    unit or none (H = 1024 k takes the variant without bounds checks)."""
+    wl = _base("h1040")
+    gh.full_parity(_with(wl, mode, _smooth(wl, 0), 0))
