@@ -43,12 +43,12 @@ L2_FLUSH_BYTES = 256 << 20
 # the SHA-256 of the kernel's source file when it was captured; reported only
 # while the source is unchanged.
 NCU_TRAFFIC = {
-    # profiles/dsv3_kernels_ncu_full.md: read 470.070528 MB + write 48.177664 MB
-    "combine": {"bytes_per_launch": 518248192,
+    # profiles/dsv3_kernels_ncu_full.md: read 470.116608 MB + write 47.918080 MB
+    "combine": {"bytes_per_launch": 518034688,
                 "src_sha": "702576bc1f87fe0463459c6f192f59f691affa006a6f3a7a979ad03ad61fa7d7"},
-    # read 59.218432 MB + write 175.693056 MB
-    "permute": {"bytes_per_launch": 234911488,
-                "src_sha": "f6199a28a51fd66527fb3db692d8b5429730b1b7e8b5d9a358727364ae79f42c"},
+    # read 59.236096 MB + write 175.429376 MB
+    "permute": {"bytes_per_launch": 234665472,
+                "src_sha": "aadb9854cea32da9defc98c33dcab36a81e64e2bd929c316962b493af63c0dd9"},
 }
 
 
