@@ -473,14 +473,6 @@ __global__ void __launch_bounds__(kQThreads) combine_quant_kernel(CombineArgs a)
   }
 }
 
-// Number of SMs of the current device.
-int sm_count() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  return n;
-}
-
 // Column chunks of at most kChunkCols elements; a ring of at most
 // kRingBytes (several CTAs per SM), 2..kRingMax chunks; one CTA per item
 // (kPersistent false) or one wave of CTAs looping over the items.
@@ -504,21 +496,10 @@ cudaError_t launch_staged(const CombineArgs& a, cudaStream_t s) {
   auto* kern = combine_staged_kernel<T, OUT_F32>;
   cudaError_t e = prepare_kernel<combine_staged_kernel<T, OUT_F32>>(smem);
   if (e != cudaSuccess) return e;
-  // The last occupancy query of this instantiation.
-  static std::mutex mu;
-  static size_t occ_smem = 0;
-  static int occ_threads = 0, occ_blocks = 0;
-  int blocks;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (occ_threads != threads || occ_smem != smem) {
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_blocks, kern, threads, smem);
-      if (e != cudaSuccess) return e;
-      occ_threads = threads;
-      occ_smem = smem;
-    }
-    blocks = occ_blocks;
-  }
+  int blocks = 0;
+  if ((e = occupancy_blocks<combine_staged_kernel<T, OUT_F32>>(threads, smem, &blocks)) !=
+      cudaSuccess)
+    return e;
   const int n_sm = sm_count();
   if (blocks < 1 || n_sm < 1) return cudaErrorInvalidConfiguration;
   const int64_t items = (int64_t)a.d.W * a.d.BS * nchunk;
@@ -566,12 +547,10 @@ cudaError_t launch_combine_q8(const CombineArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_combine_quant(const CombineArgs& a, cudaStream_t s) {
-  static int blocks_per_sm = 0;  // the kernels' occupancy (the same for both types)
-  if (blocks_per_sm == 0) {
-    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &blocks_per_sm, combine_quant_kernel<BF16>, kQThreads, 0);
-    if (e != cudaSuccess) return e;
-  }
+  int blocks_per_sm = 0;  // the kernels' occupancy (the same for both types)
+  const cudaError_t e = occupancy_blocks<combine_quant_kernel<BF16>>(kQThreads, 0, &blocks_per_sm);
+  if (e != cudaSuccess) return e;
+  if (blocks_per_sm < 1) return cudaErrorInvalidConfiguration;
   int64_t grid = (int64_t)sm_count() * blocks_per_sm;
   if (grid > a.d.R_max) grid = a.d.R_max;
   if (grid < 1) grid = 1;

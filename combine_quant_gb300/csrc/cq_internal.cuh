@@ -6,6 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "cq.h"
@@ -204,6 +205,47 @@ cudaError_t prepare_kernel(size_t smem) {
     if (e != cudaSuccess) return e;
     allowed[dev] = smem;
   }
+  return cudaSuccess;
+}
+
+// Number of SMs of the current device (cached per device; 0 on error).
+inline int sm_count() {
+  static std::atomic<int> cached[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
+// Resident CTAs per SM of `Kernel` at `threads` threads and `smem` bytes of
+// dynamic shared memory on the current device. The last query of each
+// device is cached (the launchers ask with the same sizes call after call).
+template <auto Kernel>
+cudaError_t occupancy_blocks(int threads, size_t smem, int* blocks) {
+  struct Entry {
+    int threads;
+    size_t smem;
+    int blocks;
+  };
+  static std::mutex mu;
+  static Entry cache[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  Entry& c = cache[dev];
+  if (c.threads != threads || c.smem != smem || c.blocks <= 0) {
+    int b = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, Kernel, threads, smem);
+    if (e != cudaSuccess) return e;
+    c = Entry{threads, smem, b};
+  }
+  *blocks = c.blocks;
   return cudaSuccess;
 }
 

@@ -791,20 +791,6 @@ __global__ void __launch_bounds__(288, 2) smooth_rows_kernel(PermuteArgs a) {
   griddep_launch_dependents();
 }
 
-// Number of SMs of the current device (cached per device).
-inline int sm_count() {
-  static std::atomic<int> cached[64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  std::atomic<int>& c = cached[dev & 63];
-  int n = c.load(std::memory_order_relaxed);
-  if (n <= 0) {
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    c.store(n, std::memory_order_relaxed);
-  }
-  return n;
-}
-
 // The per-expert-smooth path: index_kernel, then smooth_rows_kernel with one
 // wave of CTAs (SMs x resident CTAs per SM).
 template <class T, int Q>
@@ -824,22 +810,10 @@ cudaError_t launch_smooth_rows(const PermuteArgs& a, cudaStream_t s) {
   if ((e = full ? prepare_kernel<smooth_rows_kernel<T, Q, true>>(smem)
                 : prepare_kernel<smooth_rows_kernel<T, Q, false>>(smem)) != cudaSuccess)
     return e;
-  // The last occupancy query of each instantiation.
-  static std::mutex mu;
-  static size_t occ_smem[2] = {0, 0};
-  static int occ_threads[2] = {0, 0}, occ_blocks[2] = {0, 0};
-  int blocks;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    const int f = full ? 1 : 0;
-    if (occ_threads[f] != threads || occ_smem[f] != smem) {
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_blocks[f], kern, threads, smem);
-      if (e != cudaSuccess) return e;
-      occ_threads[f] = threads;
-      occ_smem[f] = smem;
-    }
-    blocks = occ_blocks[f];
-  }
+  int blocks = 0;
+  e = full ? occupancy_blocks<smooth_rows_kernel<T, Q, true>>(threads, smem, &blocks)
+           : occupancy_blocks<smooth_rows_kernel<T, Q, false>>(threads, smem, &blocks);
+  if (e != cudaSuccess) return e;
   if (blocks < 1) return cudaErrorInvalidConfiguration;
   int64_t grid = (int64_t)sm_count() * blocks;
   if (grid > a.d.R_max) grid = a.d.R_max;

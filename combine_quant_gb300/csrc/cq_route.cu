@@ -322,10 +322,8 @@ __global__ void __launch_bounds__(kOffThreads) offsets_kernel(RouteArgs a) {
 
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
   const size_t table = sizeof(uint16_t) * kCountWarps * (size_t)a.d.M;  // <= 32 KB
-  int dev = 0, sms = 0;
-  cudaError_t e0 = cudaGetDevice(&dev);
-  if (e0 == cudaSuccess) e0 = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e0 != cudaSuccess) return e0;
+  const int sms = sm_count();
+  if (sms < 1) return cudaErrorInvalidDevice;
   const int tpw = (a.d.BS + kCountWarps - 1) / kCountWarps;
   const int steps = (tpw * a.d.K + 31) / 32;
   const int trigger = a.d.W <= sms ? 1 : 0;
