@@ -68,9 +68,27 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
   }
 }
 
+// Two binary32 fused multiply-adds (a * b + c, one rounding each) in one
+// packed instruction: each lane is exactly __fmaf_rn of its operands.
+__device__ __forceinline__ void fma2(float& c0, float& c1, float a0, float a1, float b0, float b1) {
+  asm("{\n .reg .b64 ra, rb, rc;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mov.b64 rc, {%0, %1};\n fma.rn.f32x2 rc, ra, rb, rc;\n mov.b64 {%0, %1}, rc;\n}"
+      : "+f"(c0), "+f"(c1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+// Two binary32 products in one packed instruction, each lane rounded to
+// nearest even on its own (as two __fmul_rn).
+__device__ __forceinline__ void mul2(float& r0, float& r1, float a0, float a1, float b0, float b1) {
+  asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mul.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(r0), "=f"(r1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 __device__ __forceinline__ void fma8f(float (&acc)[8], float w, const float (&v)[8]) {
 #pragma unroll
-  for (int t = 0; t < 8; ++t) acc[t] = __fmaf_rn(w, v[t], acc[t]);
+  for (int t = 0; t < 8; t += 2) fma2(acc[t], acc[t + 1], w, w, v[t], v[t + 1]);
 }
 
 __device__ __forceinline__ void add8f(float (&acc)[8], const float (&v)[8]) {
@@ -119,12 +137,14 @@ struct SrcQ8 {
     return {ld_nc_v2(codes + row * H + 8 * (int64_t)u), ld_nc_f32(scales + row * (H >> 3) + u)};
   }
   __device__ void floats(const Item& it, float (&f)[8]) const {
+    float c[8];
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
       const uint32_t word = t < 4 ? it.q.x : it.q.y;
-      const int c = (int)(int8_t)(word >> (8 * (t & 3)));
-      f[t] = __fmul_rn((float)c, it.s);
+      c[t] = (float)(int)(int8_t)(word >> (8 * (t & 3)));
     }
+#pragma unroll
+    for (int t = 0; t < 8; t += 2) mul2(f[t], f[t + 1], c[t], c[t + 1], it.s, it.s);
   }
 };
 
