@@ -238,7 +238,7 @@ int cq_combine_q8(const cq_config* cfg, const int8_t* ffn_codes, const float* ff
                   const float* const_alpha2, const void* const_v, int32_t out_dtype, void* y,
                   void* stream);
 
-/* The spec names of the two operators: identical to cq_dispatch / cq_combine. */
+/* The operators under their MoE names: identical to cq_dispatch / cq_combine. */
 int moe_dispatch(const cq_config* cfg, const void* x, const int32_t* expert_ids,
                  const float* smooth_scales, const uint8_t* x_active_mask,
                  const int32_t* bs_per_rank, const float* expert_scales, void* expand_x,
