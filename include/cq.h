@@ -57,7 +57,7 @@ typedef struct cq_config {
   int32_t const_expert_num;       /* Q >= 0: ids [M+Z+C, M+Z+C+Q) give a1*x + a2*v */
   int32_t max_bs;                 /* BS in [1, 512], tokens per rank (maximum) */
   int32_t topk;                   /* K in [1, 16], K <= M + Z + C + Q */
-  int32_t hidden;                 /* H in [1024, 8192]; this build needs H % 16 == 0
+  int32_t hidden;                 /* H in [1024, 8192]; the library needs H % 16 == 0
                                      (H % 32 == 0 for quant_mode 4 and 5) */
   int32_t global_bs;              /* 0 or BS * W ([DV3] global_bs) */
   int32_t quant_mode;             /* 0 none, 1 static int8, 2 per-token int8, 3 per-128-group

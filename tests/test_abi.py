@@ -127,7 +127,7 @@ def test_host_errors_before_any_device_work(lib):
     bad = dict(cfg, topk=0)
     assert lib.cq_dispatch(_c(bad), *args, 1 << 20, None) == _lib.CQ_ERR_ARG
     assert lib.cq_dispatch(_c(dict(cfg, quant_mode=5, hidden=1040)), *args, 1 << 20, None) == \
-        _lib.CQ_ERR_UNSUPPORTED  # mx blocks need H % 32 == 0 in this build
+        _lib.CQ_ERR_UNSUPPORTED  # mx blocks need H % 32 == 0 in this library
     assert lib.cq_dispatch(_c(dict(cfg, quant_mode=6)), *args, 1 << 20, None) == _lib.CQ_ERR_ARG
     a_nos = list(args)
     a_nos[2] = None  # static quantisation without scales
