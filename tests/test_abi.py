@@ -69,7 +69,8 @@ def _random_cfg(rng):
         topk=int(rng.choice([1, 8, 16, 17])), hidden=int(rng.choice([1024, 7168, 8192, 1000, 8320])),
         global_bs=int(rng.choice([0, 0, 5])), quant_mode=int(rng.choice([0, 1, 2, 3, 4, 5, 6])),
         expert_token_nums_type=int(rng.choice([0, 1, 2])), mask_ndim=int(rng.choice([0, 1, 2, 3])),
-        x_dtype=int(rng.choice([0, 1, 2])), smooth_kind=int(rng.choice([0, 1, 2, 3])))
+        x_dtype=int(rng.choice([0, 1, 2])), smooth_kind=int(rng.choice([0, 1, 2, 3])),
+        y_dtype=int(rng.choice([0, 0, 1, 2])))
 
 
 def test_validation_agrees_with_oracle(lib, oracle_lib):
