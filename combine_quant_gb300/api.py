@@ -154,6 +154,38 @@ def alloc_dispatch_outputs(cfg: Config, device, with_expand_scales: bool = True)
         torch.empty(R, dtype=torch.float32, device=device) if with_expand_scales else None)
 
 
+def _check_outputs(cfg: Config, out: DispatchResult, dev, rows: bool = True,
+                   route: bool = True) -> None:
+    """The caller's output buffers must have the config's shapes and types:
+    the kernels write through raw pointers and cannot check sizes. `rows`:
+    the permute outputs are written; `route`: the routing outputs are."""
+    W, H, R = cfg.ep_world_size, cfg.hidden, cfg.max_rows
+    L = cfg.local_expert_num
+    if out.assist_info is None:
+        raise ValueError("assist_info is required")
+    _need(out.assist_info, "assist_info", torch.int32, (cfg.assist_info_size,), dev)
+    if route:
+        if out.ep_recv_count is None or out.expert_token_nums is None:
+            raise ValueError("ep_recv_count and expert_token_nums are required")
+        _need(out.ep_recv_count, "ep_recv_count", torch.int32, (W, W * L), dev)
+        _need(out.expert_token_nums, "expert_token_nums", torch.int64, (W, L), dev)
+    if rows:
+        if out.expand_x is None:
+            raise ValueError("expand_x is required")
+        _need(out.expand_x, "expand_x", cfg.code_dtype(), (R, H), dev)
+        if cfg.quant_mode == 2:
+            _need(out.dynamic_scales, "dynamic_scales", torch.float32, (R,), dev)
+        elif cfg.quant_mode == 3:
+            _need(out.dynamic_scales, "dynamic_scales", torch.float32, (R, cfg.group_cols), dev)
+        elif cfg.quant_mode in (4, 5):
+            _need(out.dynamic_scales, "dynamic_scales", torch.uint8, (R, cfg.scale_cols), dev)
+        _need(out.expand_scales, "expand_scales", torch.float32, (R,), dev)
+
+
+def _check_workspace(workspace: torch.Tensor, dev) -> None:
+    _need(workspace, "workspace", torch.uint8, None, dev)
+
+
 def _check_inputs(cfg, x, expert_ids, smooth_scales, x_active_mask, bs_per_rank, expert_scales):
     W, BS, K, H = cfg.ep_world_size, cfg.max_bs, cfg.topk, cfg.hidden
     dev = expert_ids.device
@@ -185,8 +217,10 @@ def dispatch(cfg: Config, x: torch.Tensor, expert_ids: torch.Tensor,
                         expert_scales)
     if workspace is None:
         workspace = alloc_workspace(cfg, dev)
+    _check_workspace(workspace, dev)
     if out is None:
         out = alloc_dispatch_outputs(cfg, dev, expert_scales is not None)
+    _check_outputs(cfg, out, dev)
     c = cfg.as_c()
     rc = _lib.load().cq_dispatch(
         ctypes.byref(c), _ptr(x), _ptr(expert_ids), _ptr(smooth_scales), _ptr(x_active_mask),
@@ -210,6 +244,7 @@ def dispatch_noalloc(cfg: Config, x: torch.Tensor, expert_ids: torch.Tensor,
                         expert_scales)
     if out is None:
         out = alloc_dispatch_outputs(cfg, dev, expert_scales is not None)
+    _check_outputs(cfg, out, dev)
     c = cfg.as_c()
     rc = _lib.load().cq_dispatch_noalloc(
         ctypes.byref(c), _ptr(x), _ptr(expert_ids), _ptr(smooth_scales), _ptr(x_active_mask),
@@ -224,6 +259,8 @@ def dispatch_route(cfg: Config, expert_ids, x_active_mask=None, bs_per_rank=None
                    workspace, out: DispatchResult) -> None:
     """First half of dispatch (scan, counts, prefix sums)."""
     dev = _check_inputs(cfg, None, expert_ids, None, x_active_mask, bs_per_rank, None)
+    _check_workspace(workspace, dev)
+    _check_outputs(cfg, out, dev, rows=False)
     c = cfg.as_c()
     rc = _lib.load().cq_dispatch_route(
         ctypes.byref(c), _ptr(expert_ids), _ptr(x_active_mask), _ptr(bs_per_rank),
@@ -240,6 +277,8 @@ def dispatch_permute(cfg: Config, x, expert_ids, smooth_scales=None, expert_scal
     prefetching rows of inactive tokens."""
     dev = _check_inputs(cfg, x, expert_ids, smooth_scales, x_active_mask, bs_per_rank,
                         expert_scales)
+    _check_workspace(workspace, dev)
+    _check_outputs(cfg, out, dev, route=False)
     c = cfg.as_c()
     rc = _lib.load().cq_dispatch_permute(
         ctypes.byref(c), _ptr(x), _ptr(expert_ids), _ptr(smooth_scales), _ptr(x_active_mask),
@@ -263,6 +302,8 @@ def combine(cfg: Config, expand_x_ffn: torch.Tensor, assist_info: torch.Tensor,
     _need(expand_x_ffn, "expand_x_ffn", cfg.token_dtype, (cfg.max_rows, H), dev)
     _need(assist_info, "assist_info", torch.int32, (cfg.assist_info_size,), dev)
     _need(expert_scales, "expert_scales", torch.float32, (W, BS, K), dev)
+    _need(ep_recv_count, "ep_recv_count", torch.int32,
+          (W, W * cfg.local_expert_num), dev)
     _need(ori_x, "ori_x", cfg.token_dtype, (W, BS, H), dev)
     Q = cfg.const_expert_num
     _need(const_alpha1, "const_alpha1", torch.float32, (Q,), dev)
@@ -320,6 +361,8 @@ def combine_q8(cfg: Config, codes: torch.Tensor, scales: torch.Tensor, assist_in
     _need(scales, "scales", torch.float32, (cfg.max_rows, H // 8), dev)
     _need(assist_info, "assist_info", torch.int32, (cfg.assist_info_size,), dev)
     _need(expert_scales, "expert_scales", torch.float32, (W, BS, K), dev)
+    _need(ep_recv_count, "ep_recv_count", torch.int32,
+          (W, W * cfg.local_expert_num), dev)
     _need(ori_x, "ori_x", cfg.token_dtype, (W, BS, H), dev)
     Q = cfg.const_expert_num
     _need(const_alpha1, "const_alpha1", torch.float32, (Q,), dev)
