@@ -118,10 +118,10 @@ int cq_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
  * cq_dispatch -- routing scan + permute + pre-communication quantisation.
  * [DSN] §2.2 (sendStatus scan, expandIdx, MoePermute), §2.4 (ep_recv_count as
  * the transposed received-count matrix prefix-summed row-major, expert token
- * numbers), [DV3] 功能说明 情形 1 / 情形 2 and [LLD] 计算公式 quant_mode 0, 2, 5.
+ * numbers), [DV3] 功能说明 情形 1 / 情形 2 and [LLD] 计算公式 quant_mode 0-5.
  *
- * Inputs:
- *   x              bf16 [W, BS, H]  tokens of every logical rank
+ * Inputs ("the token type" is bf16, or fp16 when x_dtype is 1):
+ *   x              token type [W, BS, H]  tokens of every logical rank
  *   expert_ids     int32 [W, BS, K] routed expert ids (MoE, zero, copy, const ranges)
  *   smooth_scales  the "scales" of [LLD]: required in mode 1, optional in
  *                  modes 2 and 3, NULL in modes 0, 4, 5. Shape by
@@ -199,14 +199,14 @@ int cq_dispatch_permute(const cq_config* cfg, const void* x, const int32_t* expe
  * alpha1[c]*ori_x + alpha2[c]*const_v[c] (products then sum, each rounded)
  * for const expert c. Inactive tokens give 0.
  *
- *   expand_x_ffn   bf16 [R_max, H] expert outputs, row-aligned with expand_x
+ *   expand_x_ffn   token type [R_max, H] expert outputs, row-aligned with expand_x
  *   assist_info    as written by cq_dispatch
  *   ep_recv_count  as written by cq_dispatch, or NULL (the row map inside
  *                  assist_info already locates every row)
  *   expert_scales  f32 [W, BS, K]
- *   ori_x          bf16 [W, BS, H]; required when C + Q > 0, else may be NULL
- *   const_alpha1, const_alpha2  f32 [Q]; const_v bf16 [Q, H]; required when Q > 0
- *   out_dtype      0: y is bf16 [W, BS, H]; 1: y is f32 [W, BS, H]
+ *   ori_x          token type [W, BS, H]; required when C + Q > 0, else may be NULL
+ *   const_alpha1, const_alpha2  f32 [Q]; const_v token type [Q, H]; required when Q > 0
+ *   out_dtype      0: y is the token type [W, BS, H]; 1: y is f32 [W, BS, H]
  */
 int cq_combine(const cq_config* cfg, const void* expand_x_ffn, const int32_t* assist_info,
                const int32_t* ep_recv_count, const float* expert_scales, const void* ori_x,
@@ -223,12 +223,12 @@ int cq_combine(const cq_config* cfg, const void* expand_x_ffn, const int32_t* as
  * each value (code * scale, one binary32 rounding) and then forms exactly the
  * sum of cq_combine.
  *
- * cq_combine_quant: expand_x_ffn bf16 [R_max, H] -> ffn_codes int8 [R_max, H]
+ * cq_combine_quant: expand_x_ffn token type [R_max, H] -> ffn_codes int8 [R_max, H]
  *   and ffn_scales f32 [R_max, H/8]; only the dispatched rows (the total in
  *   assist_info) are written. A producer that fuses this quantisation into
  *   its own epilogue can skip this call.
  * cq_combine_q8: as cq_combine, reading ffn_codes / ffn_scales instead of
- *   bf16 rows (0.5 fewer bytes per value).
+ *   16-bit rows (0.5 fewer bytes per value).
  */
 int cq_combine_quant(const cq_config* cfg, const void* expand_x_ffn, const int32_t* assist_info,
                      int8_t* ffn_codes, float* ffn_scales, void* stream);
