@@ -60,3 +60,32 @@ def test_single_process_throughput():
 
     value, slowest = bench.job_throughput(50.0, 100, 4)
     assert slowest == 50.0 and value == pytest.approx(100 * 4 / 0.05)
+
+
+def test_reference_arm_json_line(capsys):
+    """The reference arm (the oracle on host cores) prints one JSON line with
+    the contract's keys, its own cpu_baseline and a zero-copy e2e."""
+    import json
+
+    sys.path.insert(0, ROOT)
+    import bench
+
+    rc = bench.run_reference(bench.parse_args(["--impl", "reference", "--workload", "tiny",
+                                               "--steps", "2", "--warmup", "3"]))
+    assert rc == 0
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["steps"] == 2 and d["warmup"] == 3
+    assert d["value"] > 0 and d["higher_is_better"] is True
+    assert "workload" in d["config"]
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
+    assert cb["sample"]
+    e2e = d["e2e"]
+    assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
