@@ -23,10 +23,14 @@
 namespace cq {
 namespace {
 
-constexpr int kCountThreads = 512;
-constexpr int kCountWarps = kCountThreads / 32;
+// The count kernel runs kCountWarps warps per source rank, or kCountWarpsWide
+// for batches of at least kWideBS tokens per rank (shorter per-warp ranges;
+// measured faster from BS = 256 on, slower for small batches).
+constexpr int kCountWarps = 16;
+constexpr int kCountWarpsWide = 32;
+constexpr int kWideBS = 256;
 // Pairs per warp are at most ceil(512 / 16) tokens x 16 slots = 512, i.e. 16
-// per lane, so each lane keeps its pairs in 16 registers.
+// per lane, so each lane keeps its pairs in 16 registers (8 with 32 warps).
 constexpr int kMaxSteps = 16;
 constexpr int kOffThreads = 256;
 constexpr int kOffWarps = kOffThreads / 32;
@@ -94,11 +98,12 @@ __device__ int block_excl_scan(int v, int* buf, int* total) {
 // STEPS >= the 32-pair steps of a warp's range: the unrolled loops hold only
 // as many steps as the problem needs (the kernel's code is fetched cold from
 // DRAM when L2 holds other data, so its size shows in the latency).
-template <int STEPS>
-__global__ void __launch_bounds__(kCountThreads) count_kernel(RouteArgs a, int trigger_early) {
-  extern __shared__ uint16_t tbl[];  // [kCountWarps][M]: per-warp counts, then bases
-  __shared__ int s_tokcnt[kCountWarps];
-  __shared__ int s_tokbase[kCountWarps + 1];
+template <int STEPS, int NW>
+__global__ void __launch_bounds__(NW * 32) count_kernel(RouteArgs a, int trigger_early) {
+  constexpr int kThreads = NW * 32;
+  extern __shared__ uint16_t tbl[];  // [NW][M]: per-warp counts, then bases
+  __shared__ int s_tokcnt[NW];
+  __shared__ int s_tokbase[NW + 1];
 
   if (trigger_early) griddep_launch_dependents();
   const Dims& d = a.d;
@@ -107,7 +112,7 @@ __global__ void __launch_bounds__(kCountThreads) count_kernel(RouteArgs a, int t
   const int M = d.M, K = d.K, BS = d.BS, NS = d.NS;
   int n_r = BS;
   if (a.bs_per_rank) n_r = min(max(a.bs_per_rank[r], 0), BS);
-  const int tpw = (BS + kCountWarps - 1) / kCountWarps;
+  const int tpw = (BS + NW - 1) / NW;
   const int t0 = min(warp * tpw, BS), t1 = min(t0 + tpw, BS);
   const int p0 = t0 * K, p1 = t1 * K;
   const int nsteps = (p1 - p0 + 31) >> 5;
@@ -136,10 +141,10 @@ __global__ void __launch_bounds__(kCountThreads) count_kernel(RouteArgs a, int t
     }
     cls[s] = c;
   }
-  for (int t = threadIdx.x; t < kCountWarps * M; t += kCountThreads) tbl[t] = 0;
+  for (int t = threadIdx.x; t < NW * M; t += kThreads) tbl[t] = 0;
   // [DV3] x_active_mask: in 1-D form every true entry precedes every false one.
   if (d.mask_ndim == 1 && a.mask) {
-    for (int i = threadIdx.x + 1; i < n_r; i += kCountThreads) {
+    for (int i = threadIdx.x + 1; i < n_r; i += kThreads) {
       const int64_t tok = (int64_t)r * BS + i;
       if (a.mask[tok] && !a.mask[tok - 1]) atomicOr(a.ws.status, (uint32_t)CQ_ST_BAD_MASK);
     }
@@ -175,9 +180,9 @@ __global__ void __launch_bounds__(kCountThreads) count_kernel(RouteArgs a, int t
 
   // Per expert: exclusive scan over the warps (warp bases); the total is
   // this source's count for the expert.
-  for (int e = threadIdx.x; e < M; e += kCountThreads) {
+  for (int e = threadIdx.x; e < M; e += kThreads) {
     int run = 0;
-    for (int w = 0; w < kCountWarps; ++w) {
+    for (int w = 0; w < NW; ++w) {
       const int c = tbl[w * M + e];
       tbl[w * M + e] = (uint16_t)run;
       run += c;
@@ -186,17 +191,17 @@ __global__ void __launch_bounds__(kCountThreads) count_kernel(RouteArgs a, int t
   }
   if (threadIdx.x == 0) {
     int run = 0;
-    for (int w = 0; w < kCountWarps; ++w) {
+    for (int w = 0; w < NW; ++w) {
       s_tokbase[w] = run;
       run += s_tokcnt[w];
     }
-    s_tokbase[kCountWarps] = run;  // active tokens of this source
+    s_tokbase[NW] = run;  // active tokens of this source
   }
   __syncthreads();
   // Shared-expert rank g hosts replica g % R of shared expert g / R; source r
   // sends every active token to replica r % R of each shared expert.
-  const int n_act = s_tokbase[kCountWarps];
-  for (int g = threadIdx.x; g < d.S_r; g += kCountThreads) {
+  const int n_act = s_tokbase[NW];
+  for (int g = threadIdx.x; g < d.S_r; g += kThreads) {
     const bool mine = d.S_eff > 0 && (g % d.R_rep) == (r % d.R_rep);
     a.ws.counts_t[(int64_t)g * d.W + r] = mine ? n_act : 0;
   }
@@ -318,25 +323,40 @@ __global__ void __launch_bounds__(kOffThreads) offsets_kernel(RouteArgs a) {
   }
 }
 
+// One count-kernel instantiation; the wide one first raises its dynamic
+// shared-memory limit (its table reaches 64 KB at M = 1024).
+template <int STEPS, int NW>
+cudaError_t launch_count(const RouteArgs& a, size_t table, int trigger, cudaStream_t s) {
+  if (NW == kCountWarpsWide) {
+    const cudaError_t e = prepare_kernel<count_kernel<STEPS, NW>>(table);
+    if (e != cudaSuccess) return e;
+  }
+  count_kernel<STEPS, NW><<<a.d.W, NW * 32, table, s>>>(a, trigger);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
-  const size_t table = sizeof(uint16_t) * kCountWarps * (size_t)a.d.M;  // <= 32 KB
+  const bool wide = a.d.BS >= kWideBS;
+  const int nw = wide ? kCountWarpsWide : kCountWarps;
+  const size_t table = sizeof(uint16_t) * nw * (size_t)a.d.M;  // <= 64 KB
   const int sms = sm_count();
   if (sms < 1) return cudaErrorInvalidDevice;
-  const int tpw = (a.d.BS + kCountWarps - 1) / kCountWarps;
+  const int tpw = (a.d.BS + nw - 1) / nw;
   const int steps = (tpw * a.d.K + 31) / 32;
   const int trigger = a.d.W <= sms ? 1 : 0;
-  if (steps <= 2) {
-    count_kernel<2><<<a.d.W, kCountThreads, table, s>>>(a, trigger);
-  } else if (steps <= 4) {
-    count_kernel<4><<<a.d.W, kCountThreads, table, s>>>(a, trigger);
-  } else if (steps <= 8) {
-    count_kernel<8><<<a.d.W, kCountThreads, table, s>>>(a, trigger);
+  cudaError_t e;
+  if (wide) {
+    e = steps <= 2   ? launch_count<2, kCountWarpsWide>(a, table, trigger, s)
+        : steps <= 4 ? launch_count<4, kCountWarpsWide>(a, table, trigger, s)
+                     : launch_count<8, kCountWarpsWide>(a, table, trigger, s);
   } else {
-    count_kernel<kMaxSteps><<<a.d.W, kCountThreads, table, s>>>(a, trigger);
+    e = steps <= 2   ? launch_count<2, kCountWarps>(a, table, trigger, s)
+        : steps <= 4 ? launch_count<4, kCountWarps>(a, table, trigger, s)
+        : steps <= 8 ? launch_count<8, kCountWarps>(a, table, trigger, s)
+                     : launch_count<kMaxSteps, kCountWarps>(a, table, trigger, s);
   }
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_pdl(offsets_kernel, dim3(a.d.W), dim3(kOffThreads), 0, s, a);
 }
