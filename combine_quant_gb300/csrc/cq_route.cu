@@ -29,6 +29,8 @@ namespace {
 constexpr int kCountWarps = 16;
 constexpr int kCountWarpsWide = 32;
 constexpr int kWideBS = 256;
+constexpr int kCountWarpsSmall = 4;
+constexpr int kSmallBS = 32;
 // Pairs per warp are at most ceil(512 / 16) tokens x 16 slots = 512, i.e. 16
 // per lane, so each lane keeps its pairs in 16 registers (8 with 32 warps).
 constexpr int kMaxSteps = 16;
@@ -338,8 +340,8 @@ cudaError_t launch_count(const RouteArgs& a, size_t table, int trigger, cudaStre
 }  // namespace
 
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
-  const bool wide = a.d.BS >= kWideBS;
-  const int nw = wide ? kCountWarpsWide : kCountWarps;
+  const bool wide = a.d.BS >= kWideBS, small = a.d.BS <= kSmallBS;
+  const int nw = wide ? kCountWarpsWide : small ? kCountWarpsSmall : kCountWarps;
   const size_t table = sizeof(uint16_t) * nw * (size_t)a.d.M;  // <= 64 KB
   const int sms = sm_count();
   if (sms < 1) return cudaErrorInvalidDevice;
@@ -347,7 +349,10 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
   const int steps = (tpw * a.d.K + 31) / 32;
   const int trigger = a.d.W <= sms ? 1 : 0;
   cudaError_t e;
-  if (wide) {
+  if (small) {  // at most 8 tokens x 16 slots per warp: 4 steps
+    e = steps <= 2 ? launch_count<2, kCountWarpsSmall>(a, table, trigger, s)
+                   : launch_count<4, kCountWarpsSmall>(a, table, trigger, s);
+  } else if (wide) {
     e = steps <= 2   ? launch_count<2, kCountWarpsWide>(a, table, trigger, s)
         : steps <= 4 ? launch_count<4, kCountWarpsWide>(a, table, trigger, s)
                      : launch_count<8, kCountWarpsWide>(a, table, trigger, s);
