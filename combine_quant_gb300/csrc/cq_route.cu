@@ -5,10 +5,11 @@
 // expert ("expandIdx", the sendStatus counter of "MoeDistributeDispatch和
 // MoeDistributeCombine算子设计介绍" §2.2.2) and every active token its ordinal
 // among active tokens (the shared-expert slots). The tokens of a source are
-// split into 16 contiguous per-warp ranges; one walk with warp match_any
-// (equal ids grouped, ranked by lane) gives each pair its ordinal inside its
-// warp's range and per-warp counts; a per-expert scan over the 16 warps then
-// turns those into the serial scan's ordinals and this source's counts.
+// split into contiguous per-warp ranges (4, 16 or 32 warps by batch size);
+// one walk with warp match_any (equal ids grouped, ranked by lane) gives
+// each pair its ordinal inside its warp's range and per-warp counts; a
+// per-expert scan over the warps then turns those into the serial scan's
+// ordinals and this source's counts.
 //
 // offsets_kernel (one CTA per destination rank d) prefix-sums rank d's
 // received-count matrix, transposed to (local expert, source) order and summed
