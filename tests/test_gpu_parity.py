@@ -248,6 +248,14 @@ def test_edge_max_bs():
     _full_check(_cfg_case(14, W=4, M=8, BS=512, K=4, H=1024))
 
 
+def test_edge_count_kernel_widths():
+    """The routing scan runs 32 warps per source from 256 tokens per rank on
+    (with M = 1024 its per-warp table is 64 KB of shared memory) and 4 warps
+    up to 32 tokens per rank; both against the oracle at those edges."""
+    _full_check(_cfg_case(15, W=8, M=1024, BS=256, K=16, H=1024))
+    _full_check(_cfg_case(16, W=4, M=16, BS=32, K=16, H=1024))
+
+
 @pytest.mark.parametrize("mode", [2, 3])
 def test_edge_max_hidden_shared_and_smooth(mode):
     """H = 8192 with 4 shared experts on 4 ranks and one smooth row per expert:
