@@ -72,6 +72,8 @@ def parse_args(argv=None):
                          "expert side (the quantiser is timed separately, outside the step)")
     ap.add_argument("--flush", choices=["write+read", "write", "none"], default="write+read",
                     help="L2 flush between steps (outside the timed events)")
+    ap.add_argument("--e2e-sets", type=int, default=2,
+                    help="input/output buffer sets of the end-to-end leg (pipeline depth)")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch each call directly instead of replaying CUDA graphs")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -598,7 +600,7 @@ def run_cq(args):
         hids = torch.from_numpy(np.ascontiguousarray(wl.expert_ids)).pin_memory()
         hw = torch.from_numpy(np.ascontiguousarray(wl.expert_scales)).pin_memory()
         n_e2e = max(10, min(args.steps, 500))
-        # Two buffer sets: step k uploads into set k % 2 on the upload stream,
+        # args.e2e_sets buffer sets: step k uploads into set k % n on the upload stream,
         # computes on the main stream, downloads y on the download stream; the
         # events keep each set's reuse ordered, so copies of neighbouring
         # steps overlap the compute of this one.
@@ -607,13 +609,13 @@ def run_cq(args):
                      y=torch.empty_like(y),
                      hy=torch.empty(y.shape, dtype=torch.bfloat16).pin_memory(),
                      up=torch.cuda.Event(), done=torch.cuda.Event(), down=torch.cuda.Event())
-                for _ in range(2)]
+                for _ in range(args.e2e_sets)]
         for b in sets:
             b["done"].record(stream)
             b["down"].record(stream)
 
         def e2e_step(k):
-            b = sets[k % 2]
+            b = sets[k % len(sets)]
             with torch.cuda.stream(s_up):
                 s_up.wait_event(b["done"])  # the set's inputs are free once its last compute ended
                 b["x"].copy_(hx, non_blocking=True)
@@ -638,7 +640,7 @@ def run_cq(args):
         e0.record(s_up)
         for k in range(n_e2e):
             e2e_step(k)
-        s_down.wait_event(sets[(n_e2e - 1) % 2]["down"])
+        s_down.wait_event(sets[(n_e2e - 1) % len(sets)]["down"])
         e1.record(s_down)
         barrier()
         e_value, _ = job_throughput(e0.elapsed_time(e1), tokens, n_e2e, dist, dev)
@@ -646,8 +648,8 @@ def run_cq(args):
                "h2d_bytes_per_step": hx.nbytes + hids.nbytes + hw.nbytes,
                "d2h_bytes_per_step": sets[0]["hy"].nbytes, "steps": n_e2e,
                "api": "cq_dispatch + cq_combine (libcq C ABI via ctypes)",
-               "pipelining": "two buffer sets; upload, compute and download on three "
-                             "streams, so neighbouring steps' copies overlap"}
+               "pipelining": f"{len(sets)} buffer sets; upload, compute and download on "
+                             "three streams, so neighbouring steps' copies overlap"}
 
     if rank != 0:
         if dist is not None:
