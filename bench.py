@@ -53,6 +53,13 @@ NCU_TRAFFIC = {
 }
 
 
+def _positive_int(text: str) -> int:
+    v = int(text)
+    if v < 1:
+        raise argparse.ArgumentTypeError(f"must be >= 1, got {v}")
+    return v
+
+
 def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -72,8 +79,8 @@ def parse_args(argv=None):
                          "expert side (the quantiser is timed separately, outside the step)")
     ap.add_argument("--flush", choices=["write+read", "write", "none"], default="write+read",
                     help="L2 flush between steps (outside the timed events)")
-    ap.add_argument("--e2e-sets", type=int, default=2,
-                    help="input/output buffer sets of the end-to-end leg (pipeline depth)")
+    ap.add_argument("--e2e-sets", type=_positive_int, default=2,
+                    help="input/output buffer sets of the end-to-end leg (pipeline depth, >= 1)")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch each call directly instead of replaying CUDA graphs")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,

@@ -222,11 +222,12 @@ def dispatch(cfg: Config, x: torch.Tensor, expert_ids: torch.Tensor,
         out = alloc_dispatch_outputs(cfg, dev, expert_scales is not None)
     _check_outputs(cfg, out, dev)
     c = cfg.as_c()
-    rc = _lib.load().cq_dispatch(
-        ctypes.byref(c), _ptr(x), _ptr(expert_ids), _ptr(smooth_scales), _ptr(x_active_mask),
-        _ptr(bs_per_rank), _ptr(expert_scales), _ptr(out.expand_x), _ptr(out.dynamic_scales),
-        _ptr(out.assist_info), _ptr(out.ep_recv_count), _ptr(out.expert_token_nums),
-        _ptr(out.expand_scales), _ptr(workspace), workspace.numel(), _stream(dev))
+    with torch.cuda.device(dev):  # the library looks up the current device
+        rc = _lib.load().cq_dispatch(
+            ctypes.byref(c), _ptr(x), _ptr(expert_ids), _ptr(smooth_scales), _ptr(x_active_mask),
+            _ptr(bs_per_rank), _ptr(expert_scales), _ptr(out.expand_x), _ptr(out.dynamic_scales),
+            _ptr(out.assist_info), _ptr(out.ep_recv_count), _ptr(out.expert_token_nums),
+            _ptr(out.expand_scales), _ptr(workspace), workspace.numel(), _stream(dev))
     _lib.check(rc, "cq_dispatch")
     return out
 
@@ -246,11 +247,12 @@ def dispatch_noalloc(cfg: Config, x: torch.Tensor, expert_ids: torch.Tensor,
         out = alloc_dispatch_outputs(cfg, dev, expert_scales is not None)
     _check_outputs(cfg, out, dev)
     c = cfg.as_c()
-    rc = _lib.load().cq_dispatch_noalloc(
-        ctypes.byref(c), _ptr(x), _ptr(expert_ids), _ptr(smooth_scales), _ptr(x_active_mask),
-        _ptr(bs_per_rank), _ptr(expert_scales), _ptr(out.expand_x), _ptr(out.dynamic_scales),
-        _ptr(out.assist_info), _ptr(out.ep_recv_count), _ptr(out.expert_token_nums),
-        _ptr(out.expand_scales), _stream(dev))
+    with torch.cuda.device(dev):  # the library looks up the current device
+        rc = _lib.load().cq_dispatch_noalloc(
+            ctypes.byref(c), _ptr(x), _ptr(expert_ids), _ptr(smooth_scales), _ptr(x_active_mask),
+            _ptr(bs_per_rank), _ptr(expert_scales), _ptr(out.expand_x), _ptr(out.dynamic_scales),
+            _ptr(out.assist_info), _ptr(out.ep_recv_count), _ptr(out.expert_token_nums),
+            _ptr(out.expand_scales), _stream(dev))
     _lib.check(rc, "cq_dispatch_noalloc")
     return out
 
@@ -262,10 +264,11 @@ def dispatch_route(cfg: Config, expert_ids, x_active_mask=None, bs_per_rank=None
     _check_workspace(workspace, dev)
     _check_outputs(cfg, out, dev, rows=False)
     c = cfg.as_c()
-    rc = _lib.load().cq_dispatch_route(
-        ctypes.byref(c), _ptr(expert_ids), _ptr(x_active_mask), _ptr(bs_per_rank),
-        _ptr(out.assist_info), _ptr(out.ep_recv_count), _ptr(out.expert_token_nums),
-        _ptr(workspace), workspace.numel(), _stream(dev))
+    with torch.cuda.device(dev):  # the library looks up the current device
+        rc = _lib.load().cq_dispatch_route(
+            ctypes.byref(c), _ptr(expert_ids), _ptr(x_active_mask), _ptr(bs_per_rank),
+            _ptr(out.assist_info), _ptr(out.ep_recv_count), _ptr(out.expert_token_nums),
+            _ptr(workspace), workspace.numel(), _stream(dev))
     _lib.check(rc, "cq_dispatch_route")
 
 
@@ -280,11 +283,12 @@ def dispatch_permute(cfg: Config, x, expert_ids, smooth_scales=None, expert_scal
     _check_workspace(workspace, dev)
     _check_outputs(cfg, out, dev, route=False)
     c = cfg.as_c()
-    rc = _lib.load().cq_dispatch_permute(
-        ctypes.byref(c), _ptr(x), _ptr(expert_ids), _ptr(smooth_scales), _ptr(x_active_mask),
-        _ptr(bs_per_rank), _ptr(expert_scales), _ptr(out.expand_x), _ptr(out.dynamic_scales),
-        _ptr(out.assist_info), _ptr(out.expand_scales), _ptr(workspace), workspace.numel(),
-        _stream(dev))
+    with torch.cuda.device(dev):  # the library looks up the current device
+        rc = _lib.load().cq_dispatch_permute(
+            ctypes.byref(c), _ptr(x), _ptr(expert_ids), _ptr(smooth_scales), _ptr(x_active_mask),
+            _ptr(bs_per_rank), _ptr(expert_scales), _ptr(out.expand_x), _ptr(out.dynamic_scales),
+            _ptr(out.assist_info), _ptr(out.expand_scales), _ptr(workspace), workspace.numel(),
+            _stream(dev))
     _lib.check(rc, "cq_dispatch_permute")
 
 
@@ -317,10 +321,11 @@ def combine(cfg: Config, expand_x_ffn: torch.Tensor, assist_info: torch.Tensor,
         y = torch.empty(W, BS, H, dtype=out_dtype, device=dev)
     _need(y, "y", out_dtype, (W, BS, H), dev)
     c = cfg.as_c()
-    rc = _lib.load().cq_combine(
-        ctypes.byref(c), _ptr(expand_x_ffn), _ptr(assist_info), _ptr(ep_recv_count),
-        _ptr(expert_scales), _ptr(ori_x), _ptr(const_alpha1), _ptr(const_alpha2), _ptr(const_v),
-        0 if out_dtype != torch.float32 else 1, _ptr(y), _stream(dev))
+    with torch.cuda.device(dev):  # the library looks up the current device
+        rc = _lib.load().cq_combine(
+            ctypes.byref(c), _ptr(expand_x_ffn), _ptr(assist_info), _ptr(ep_recv_count),
+            _ptr(expert_scales), _ptr(ori_x), _ptr(const_alpha1), _ptr(const_alpha2), _ptr(const_v),
+            0 if out_dtype != torch.float32 else 1, _ptr(y), _stream(dev))
     _lib.check(rc, "cq_combine")
     return y
 
@@ -340,8 +345,9 @@ def combine_quant(cfg: Config, expand_x_ffn: torch.Tensor, assist_info: torch.Te
     _need(codes, "codes", torch.int8, (R, H), dev)
     _need(scales, "scales", torch.float32, (R, H // 8), dev)
     c = cfg.as_c()
-    rc = _lib.load().cq_combine_quant(ctypes.byref(c), _ptr(expand_x_ffn), _ptr(assist_info),
-                                      _ptr(codes), _ptr(scales), _stream(dev))
+    with torch.cuda.device(dev):  # the library looks up the current device
+        rc = _lib.load().cq_combine_quant(ctypes.byref(c), _ptr(expand_x_ffn), _ptr(assist_info),
+                                          _ptr(codes), _ptr(scales), _stream(dev))
     _lib.check(rc, "cq_combine_quant")
     return codes, scales
 
@@ -376,10 +382,11 @@ def combine_q8(cfg: Config, codes: torch.Tensor, scales: torch.Tensor, assist_in
         y = torch.empty(W, BS, H, dtype=out_dtype, device=dev)
     _need(y, "y", out_dtype, (W, BS, H), dev)
     c = cfg.as_c()
-    rc = _lib.load().cq_combine_q8(
-        ctypes.byref(c), _ptr(codes), _ptr(scales), _ptr(assist_info), _ptr(ep_recv_count),
-        _ptr(expert_scales), _ptr(ori_x), _ptr(const_alpha1), _ptr(const_alpha2), _ptr(const_v),
-        0 if out_dtype != torch.float32 else 1, _ptr(y), _stream(dev))
+    with torch.cuda.device(dev):  # the library looks up the current device
+        rc = _lib.load().cq_combine_q8(
+            ctypes.byref(c), _ptr(codes), _ptr(scales), _ptr(assist_info), _ptr(ep_recv_count),
+            _ptr(expert_scales), _ptr(ori_x), _ptr(const_alpha1), _ptr(const_alpha2), _ptr(const_v),
+            0 if out_dtype != torch.float32 else 1, _ptr(y), _stream(dev))
     _lib.check(rc, "cq_combine_q8")
     return y
 
@@ -387,7 +394,9 @@ def combine_q8(cfg: Config, codes: torch.Tensor, scales: torch.Tensor, assist_in
 def read_status(workspace: torch.Tensor) -> int:
     """Synchronise the current stream, return and clear the sticky status bits."""
     st = ctypes.c_uint32(0)
-    rc = _lib.load().cq_read_status(_ptr(workspace), ctypes.byref(st), _stream(workspace.device))
+    with torch.cuda.device(workspace.device):
+        rc = _lib.load().cq_read_status(_ptr(workspace), ctypes.byref(st),
+                                        _stream(workspace.device))
     _lib.check(rc, "cq_read_status")
     return int(st.value)
 

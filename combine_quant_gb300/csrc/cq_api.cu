@@ -88,16 +88,47 @@ int check_ws(const Dims& d, const void* ws, size_t bytes) {
   return CQ_OK;
 }
 
-int route_impl(const cq_config* cfg, const int32_t* expert_ids, const uint8_t* mask,
-               const int32_t* bs_per_rank, int32_t* assist_info, int32_t* ep_recv_count,
-               int64_t* expert_token_nums, void* workspace, size_t workspace_bytes,
-               void* stream) {
+// Host-only checks of the route half's arguments (nothing is enqueued).
+int check_route(const cq_config* cfg, const int32_t* expert_ids, const uint8_t* mask,
+                const int32_t* assist_info, const int32_t* ep_recv_count,
+                const int64_t* expert_token_nums, const void* workspace,
+                size_t workspace_bytes) {
   int rc = validate(cfg);
   if (rc != CQ_OK) return rc;
   const Dims d = dims_of(cfg);
   if (!expert_ids || !assist_info || !ep_recv_count || !expert_token_nums) return CQ_ERR_ARG;
   if (d.mask_ndim != 0 && !mask) return CQ_ERR_ARG;
-  if ((rc = check_ws(d, workspace, workspace_bytes)) != CQ_OK) return rc;
+  return check_ws(d, workspace, workspace_bytes);
+}
+
+// Host-only checks of the permute half's arguments (nothing is enqueued).
+int check_permute(const cq_config* cfg, const void* x, const int32_t* expert_ids,
+                  const float* smooth, const void* expand_x, const void* dynamic_scales,
+                  const int32_t* assist_info, const void* workspace, size_t workspace_bytes) {
+  int rc = validate(cfg);
+  if (rc != CQ_OK) return rc;
+  const Dims d = dims_of(cfg);
+  if (!x || !expert_ids || !expand_x || !assist_info) return CQ_ERR_ARG;
+  if (d.mode >= 2 && !dynamic_scales) return CQ_ERR_ARG;
+  // [LLD] quant_mode 相关约束: mx modes take no scales; static quantisation needs them.
+  if (smooth && (d.mode == 0 || d.mode == 4 || d.mode == 5)) return CQ_ERR_ARG;
+  if (!smooth && d.mode == 1) return CQ_ERR_ARG;
+  if (!aligned(x, 16) || !aligned(expand_x, 16) ||
+      (smooth && cfg->smooth_kind != 2 && !aligned(smooth, 16)) || !aligned(assist_info, 16) ||
+      (smooth && !aligned(smooth, 4)) ||
+      ((d.mode == 2 || d.mode == 3) && !aligned(dynamic_scales, 4)))
+    return CQ_ERR_ARG;
+  return check_ws(d, workspace, workspace_bytes);
+}
+
+int route_impl(const cq_config* cfg, const int32_t* expert_ids, const uint8_t* mask,
+               const int32_t* bs_per_rank, int32_t* assist_info, int32_t* ep_recv_count,
+               int64_t* expert_token_nums, void* workspace, size_t workspace_bytes,
+               void* stream) {
+  const int rc = check_route(cfg, expert_ids, mask, assist_info, ep_recv_count,
+                             expert_token_nums, workspace, workspace_bytes);
+  if (rc != CQ_OK) return rc;
+  const Dims d = dims_of(cfg);
   cq::RouteArgs a;
   a.d = d;
   a.expert_ids = expert_ids;
@@ -116,20 +147,10 @@ int permute_impl(const cq_config* cfg, const void* x, const int32_t* expert_ids,
                  const float* expert_scales, void* expand_x, void* dynamic_scales,
                  int32_t* assist_info, float* expand_scales, void* workspace,
                  size_t workspace_bytes, void* stream) {
-  int rc = validate(cfg);
+  const int rc = check_permute(cfg, x, expert_ids, smooth, expand_x, dynamic_scales,
+                               assist_info, workspace, workspace_bytes);
   if (rc != CQ_OK) return rc;
   const Dims d = dims_of(cfg);
-  if (!x || !expert_ids || !expand_x || !assist_info) return CQ_ERR_ARG;
-  if (d.mode >= 2 && !dynamic_scales) return CQ_ERR_ARG;
-  // [LLD] quant_mode 相关约束: mx modes take no scales; static quantisation needs them.
-  if (smooth && (d.mode == 0 || d.mode == 4 || d.mode == 5)) return CQ_ERR_ARG;
-  if (!smooth && d.mode == 1) return CQ_ERR_ARG;
-  if (!aligned(x, 16) || !aligned(expand_x, 16) ||
-      (smooth && cfg->smooth_kind != 2 && !aligned(smooth, 16)) || !aligned(assist_info, 16) ||
-      (smooth && !aligned(smooth, 4)) ||
-      ((d.mode == 2 || d.mode == 3) && !aligned(dynamic_scales, 4)))
-    return CQ_ERR_ARG;
-  if ((rc = check_ws(d, workspace, workspace_bytes)) != CQ_OK) return rc;
   cq::PermuteArgs a;
   a.d = d;
   a.x = static_cast<const uint16_t*>(x);
@@ -152,6 +173,22 @@ int permute_impl(const cq_config* cfg, const void* x, const int32_t* expert_ids,
 }
 
 }  // namespace
+
+namespace cq {
+
+int dispatch_check(const cq_config* cfg, const void* x, const int32_t* expert_ids,
+                   const float* smooth_scales, const uint8_t* x_active_mask, const void* expand_x,
+                   const void* dynamic_scales, const int32_t* assist_info,
+                   const int32_t* ep_recv_count, const int64_t* expert_token_nums,
+                   const void* workspace, size_t workspace_bytes) {
+  const int rc = check_route(cfg, expert_ids, x_active_mask, assist_info, ep_recv_count,
+                             expert_token_nums, workspace, workspace_bytes);
+  if (rc != CQ_OK) return rc;
+  return check_permute(cfg, x, expert_ids, smooth_scales, expand_x, dynamic_scales, assist_info,
+                       workspace, workspace_bytes);
+}
+
+}  // namespace cq
 
 extern "C" {
 
@@ -220,13 +257,12 @@ int cq_dispatch(const cq_config* cfg, const void* x, const int32_t* expert_ids,
                 void* dynamic_scales, int32_t* assist_info, int32_t* ep_recv_count,
                 int64_t* expert_token_nums, float* expand_scales, void* workspace,
                 size_t workspace_bytes, void* stream) {
-  // Check the permute half's arguments too before enqueueing the route half.
-  int rc = validate(cfg);
+  // Every argument of both halves is checked before the route half is
+  // enqueued, so an argument error leaves the outputs untouched.
+  int rc = cq::dispatch_check(cfg, x, expert_ids, smooth_scales, x_active_mask, expand_x,
+                             dynamic_scales, assist_info, ep_recv_count, expert_token_nums,
+                             workspace, workspace_bytes);
   if (rc != CQ_OK) return rc;
-  const int m = cfg->quant_mode;
-  if (!x || !expand_x || (m >= 2 && !dynamic_scales)) return CQ_ERR_ARG;
-  if (smooth_scales && (m == 0 || m == 4 || m == 5)) return CQ_ERR_ARG;
-  if (!smooth_scales && m == 1) return CQ_ERR_ARG;
   rc = route_impl(cfg, expert_ids, x_active_mask, bs_per_rank, assist_info, ep_recv_count,
                   expert_token_nums, workspace, workspace_bytes, stream);
   if (rc != CQ_OK) return rc;

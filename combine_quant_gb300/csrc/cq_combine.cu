@@ -412,7 +412,9 @@ __global__ void __launch_bounds__(288) combine_staged_kernel(CombineArgs a, int 
 
 // Combine-side int8 quantisation of the expert outputs before they are sent
 // back ("CANN MoE Dispatch/Combine 通信算子性能优化实践", Int8QuantProcess):
-// per block of 8 values, scale = max|v| * fl(1/127), code = RNE(v / scale).
+// per block of 8 values, scale = max|v| * fl(1/127), and the quotient
+// v / scale cast float -> fp16 -> int8, each cast to nearest even, the int8
+// one saturating.
 // One wave of CTAs; CTA b takes rows b, b + gridDim.x, ... below the
 // dispatched total, each thread up to kQUnits 8-element units of the row with
 // all its loads issued before the first division.
@@ -432,12 +434,24 @@ __device__ __forceinline__ float div_by(float v, float s, float y) {
   return __fmaf_rn(__fmaf_rn(-s, q0, v), y, q0);
 }
 
-// RNE(fl(v / s)) as the low byte of a float, for a block whose scale s is
-// normal or infinite, or whose max is 0 (y = RN(1 / s)): every quotient is
-// then NaN or lies in [-128, 128]. max(q, -256) maps NaN (0/0, inf/inf) to
-// -256; adding 1.5 * 2^23 leaves RNE(q) in the low byte of the sum (-256 -> 0).
-__device__ __forceinline__ uint32_t q8_div_magic(float v, float s, float y) {
-  return __float_as_uint(__fadd_rn(fmaxf(div_by(v, s, y), -256.f), 12582912.f));
+// fl(v / s) for a block whose scale s is normal or infinite, or whose max is
+// 0 (y = RN(1 / s)): every quotient is then NaN or lies in [-128, 128], and
+// max(q, -256) maps NaN (0/0, inf/inf) to -256.
+__device__ __forceinline__ float q_div(float v, float s, float y) {
+  return fmaxf(div_by(v, s, y), -256.f);
+}
+
+// The page's cast chain float -> fp16 -> int8 for two quotients in
+// [-256, 128]: cvt.rn.f16x2.f32 rounds each to the nearest binary16 (ties to
+// even); adding 1536 = 1.5 * 2^10 in binary16 rounds the sum to an integer
+// (the spacing is 1 in [1024, 2048)), so the low byte of each 16-bit sum is
+// the nearest-even integer of the binary16 value in two's complement (-256
+// gives 0). Byte 0 holds lo's code, byte 2 hi's.
+__device__ __forceinline__ uint32_t q8x2_via_f16(float lo, float hi) {
+  uint32_t h, r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(h) : "f"(hi), "f"(lo));
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0x66006600u));
+  return r;
 }
 
 template <class T>
@@ -470,18 +484,17 @@ __global__ void __launch_bounds__(kQThreads) combine_quant_kernel(CombineArgs a)
         const float y = __frcp_rn(s);
 #pragma unroll
         for (int h = 0; h < 2; ++h)
-          w[h] = __byte_perm(__byte_perm(q8_div_magic(f[4 * h], s, y),
-                                         q8_div_magic(f[4 * h + 1], s, y), 0x0040),
-                             __byte_perm(q8_div_magic(f[4 * h + 2], s, y),
-                                         q8_div_magic(f[4 * h + 3], s, y), 0x0040),
-                             0x5410);
+          w[h] = __byte_perm(
+              q8x2_via_f16(q_div(f[4 * h], s, y), q_div(f[4 * h + 1], s, y)),
+              q8x2_via_f16(q_div(f[4 * h + 2], s, y), q_div(f[4 * h + 3], s, y)), 0x6420);
       } else {
         // A subnormal or zero scale of a non-zero block: quotients may leave
-        // the int8 range and saturate.
+        // the int8 range (beyond 65504 the fp16 value is infinite) and
+        // saturate.
         w[0] = w[1] = 0u;
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
-          int c = __float2int_rn(__fdiv_rn(f[t], s));
+          int c = __float2int_rn(__half2float(__float2half_rn(__fdiv_rn(f[t], s))));
           c = max(-128, min(127, c));
           w[t >> 2] |= ((uint32_t)c & 0xffu) << (8 * (t & 3));
         }

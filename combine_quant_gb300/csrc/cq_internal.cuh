@@ -254,6 +254,14 @@ __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Every host-side check of cq_dispatch's arguments (both halves), with
+// nothing enqueued: CQ_OK or the error code cq_dispatch would return.
+int dispatch_check(const cq_config* cfg, const void* x, const int32_t* expert_ids,
+                   const float* smooth_scales, const uint8_t* x_active_mask, const void* expand_x,
+                   const void* dynamic_scales, const int32_t* assist_info,
+                   const int32_t* ep_recv_count, const int64_t* expert_token_nums,
+                   const void* workspace, size_t workspace_bytes);
+
 // Launchers (each returns the cudaError_t of its launch).
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
 cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t s);

@@ -59,6 +59,12 @@ extern "C" int cq_dispatch_noalloc(const cq_config* cfg, const void* x, const in
   void* scratch = nullptr;
   const int arc = scratch_address(&scratch);
   if (arc != CQ_OK) return arc;
+  // Every argument check of cq_dispatch runs before the header is cleared,
+  // so an argument error returns with nothing enqueued.
+  const int crc = cq::dispatch_check(cfg, x, expert_ids, smooth_scales, x_active_mask, expand_x,
+                                     dynamic_scales, assist_info, ep_recv_count,
+                                     expert_token_nums, scratch, CQ_NOALLOC_SCRATCH_BYTES);
+  if (crc != CQ_OK) return crc;
   // The array keeps whatever the previous call left. Only the header (status
   // word and the routing kernel's completion counter) has to start at zero;
   // every other byte the kernels read is written earlier in the same call.

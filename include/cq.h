@@ -19,9 +19,12 @@
  * Conventions for every entry point:
  *   - All tensor pointers are DEVICE pointers, row-major, contiguous, owned
  *     by the caller. The library never allocates or frees memory.
- *   - `stream` is a cudaStream_t passed as void*. Work is enqueued on it and
- *     the call returns without synchronising (except cq_read_status and
- *     cq_read_combine_status).
+ *   - `stream` is a cudaStream_t passed as void*, created on the device that
+ *     is current when the call is made (the library sizes launches, caches
+ *     per-device state and finds its built-in arrays by the current device),
+ *     and every pointer refers to that device's memory. Work is enqueued on
+ *     it and the call returns without synchronising (except cq_read_status
+ *     and cq_read_combine_status).
  *   - Return 0 (CQ_OK) or a negative CQ_ERR_* code. Argument errors are found
  *     on the host before anything is enqueued; nothing is enqueued then.
  *   - Data-dependent problems found on the device (an out-of-range expert
@@ -218,10 +221,11 @@ int cq_combine(const cq_config* cfg, const void* expand_x_ffn, const int32_t* as
  * 优化实践", 通信前量化: Combine 发送前按 block 量化为 int8, Int8QuantProcess /
  * Int8DequantProcess). The expert side quantises each output row before it is
  * sent back, in blocks of 8 values (32 bytes of fp32): scale = max|v| times
- * fl(1/127), code = round-to-nearest-even(v / scale) saturated to int8 (an
- * all-zero block has scale 0 and codes 0). The receiving side dequantises
- * each value (code * scale, one binary32 rounding) and then forms exactly the
- * sum of cq_combine.
+ * fl(1/127), and the binary32 quotient v / scale is cast float -> fp16 ->
+ * int8 as the page writes it, each cast rounding to nearest even, the int8
+ * one saturating (an all-zero block has scale 0 and codes 0). The receiving
+ * side casts int8 -> fp16 -> float (exact), multiplies by the scale (one
+ * binary32 rounding) and then forms exactly the sum of cq_combine.
  *
  * cq_combine_quant: expand_x_ffn token type [R_max, H] -> ffn_codes int8 [R_max, H]
  *   and ffn_scales f32 [R_max, H/8]; only the dispatched rows (the total in

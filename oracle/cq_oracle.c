@@ -672,7 +672,10 @@ int cqo_combine(const cqo_config* c, const uint16_t* ffn, const int32_t* inv,
 /* Int8DequantProcess: before an expert output row is sent back it is cut     */
 /* into 32-byte blocks of 8 float values; per block the scale is the largest  */
 /* magnitude times 1/SCALE_PARAM (SCALE_PARAM = 127), each value is divided by */
-/* the scale and cast to int8; the receiver multiplies back by the scale.     */
+/* the scale and the quotient is cast float -> fp16 -> int8; the receiver     */
+/* casts int8 -> fp16 -> float (exact) and multiplies back by the scale.      */
+/* The page names the two casts but not their rounding: both are taken as     */
+/* round-to-nearest-even, the second one saturating to [-128, 127].           */
 /* ------------------------------------------------------------------------ */
 
 int cqo_combine_quant_row(int32_t H, int32_t dt, const uint16_t* row, int8_t* codes,
@@ -687,8 +690,12 @@ int cqo_combine_quant_row(int32_t H, int32_t dt, const uint16_t* row, int8_t* co
     }
     const float scale = m * inv_param; /* Muls(1/SCALE_PARAM) */
     for (int32_t t = 0; t < 8; ++t) {
-      /* Div, then one round-to-nearest-even cast (0/0 = NaN gives 0) */
-      codes[b * 8 + t] = sat_rne_int8(in16(dt, row[b * 8 + t]) / scale);
+      /* Div, then Cast(float -> fp16 -> int8): the binary32 quotient rounded
+       * to binary16 (nearest even; beyond 65504 it becomes infinity), that
+       * value rounded to an integer (nearest even) and saturated. 0/0 = NaN
+       * stays NaN in fp16 and gives 0. */
+      const float q = in16(dt, row[b * 8 + t]) / scale;
+      codes[b * 8 + t] = sat_rne_int8(cqo_f16_to_f32(cqo_f16_from_f32(q)));
     }
     scales[b] = scale;
   }

@@ -134,9 +134,10 @@ int cqo_combine(const cqo_config* c, const uint16_t* ffn, const int32_t* inv,
                 const float* expert_scales, const uint16_t* ori_x, const float* const_alpha1,
                 const float* const_alpha2, const uint16_t* const_v, int32_t out_f32, void* y);
 
-/* Combine-side int8 block quantisation of one expert-output row of H bf16
- * values: blocks of 8 elements, scale = max|v| * fl(1/127), codes =
- * RNE(v / scale) saturated to int8. codes [H], scales [H/8] (H % 8 == 0). */
+/* Combine-side int8 block quantisation of one expert-output row of H 16-bit
+ * values: blocks of 8 elements, scale = max|v| * fl(1/127), codes = the
+ * quotient v / scale cast float -> fp16 -> int8 (each cast round-to-nearest-
+ * even, the int8 one saturating). codes [H], scales [H/8] (H % 8 == 0). */
 int cqo_combine_quant_row(int32_t hidden, int32_t x_dtype, const uint16_t* row, int8_t* codes,
                           float* scales);
 

@@ -118,13 +118,54 @@ def test_derived_sizes(lib, oracle_lib, name):
     assert lib.cq_workspace_size(c) > 0
 
 
+def _no_gpu_visible():
+    """The rejection tests below hand the library pointers into host memory;
+    they run only where no GPU is visible, so that even a check that stopped
+    working could not launch a kernel on them."""
+    import torch
+    return not torch.cuda.is_available()
+
+
+needs_no_gpu = pytest.mark.skipif(not _no_gpu_visible(),
+                                  reason="host-pointer rejection tests run without a GPU")
+
+
+class _HostBufs:
+    """Real, 256-byte aligned host buffers, one per pointer argument of
+    cq_dispatch / cq_combine, each large enough for the config."""
+
+    def __init__(self, cfg):
+        W, BS, K, H = cfg["ep_world_size"], cfg["max_bs"], cfg["topk"], cfg["hidden"]
+        R = oracle.max_rows(cfg)
+        NS = oracle.num_slots(cfg)
+        sizes = dict(x=2 * W * BS * H, ids=4 * W * BS * K, smooth=4 * (cfg["moe_expert_num"] + 4) * H,
+                     mask=W * BS * K, bpr=4 * W, w=4 * W * BS * K, expand_x=2 * R * H + 16,
+                     dyn=4 * R * H, assist=4 * (4 * R + W * BS * NS + W + 1), erc=4 * W * 2048,
+                     etn=8 * W * 2048, es=4 * R, ws=4 << 20, ffn=2 * R * H, y=4 * W * BS * H,
+                     a=64, v=2 * 16 * H)
+        self._mem = {k: np.zeros(n + 256, np.uint8) for k, n in sizes.items()}
+
+    def __getitem__(self, name):
+        a = self._mem[name]
+        return ctypes.c_void_p(a.ctypes.data + (-a.ctypes.data) % 256)
+
+    def dispatch_args(self):
+        return [self[k] for k in ("x", "ids", "smooth", "mask", "bpr", "w", "expand_x", "dyn",
+                                  "assist", "erc", "etn", "es", "ws")]
+
+    def combine_args(self):
+        return [self[k] for k in ("ffn", "assist", "erc", "w", "x", "a", "a", "v")]
+
+
+@needs_no_gpu
 def test_host_errors_before_any_device_work(lib):
-    """Invalid arguments are rejected on the host (these calls would fault if
-    they reached the device: the pointers are fake)."""
+    """Invalid arguments are rejected on the host before anything is
+    enqueued. With no GPU present, a call that got as far as a launch would
+    return CQ_ERR_CUDA instead of the argument error checked here."""
     cfg = make_config(ep_world_size=4, moe_expert_num=8, max_bs=8, topk=2, hidden=1024,
                       quant_mode=2)
-    fake = ctypes.c_void_p(0x10000)
-    args = [fake] * 13
+    hb = _HostBufs(cfg)
+    args = hb.dispatch_args()
     bad = dict(cfg, topk=0)
     assert lib.cq_dispatch(_c(bad), *args, 1 << 20, None) == _lib.CQ_ERR_ARG
     assert lib.cq_dispatch(_c(dict(cfg, quant_mode=5, hidden=1040)), *args, 1 << 20, None) == \
@@ -148,17 +189,35 @@ def test_host_errors_before_any_device_work(lib):
     a3[3] = None
     assert lib.cq_dispatch(_c(dict(cfg, mask_ndim=1)), *a3, 1 << 20, None) == _lib.CQ_ERR_ARG
     # combine: copy experts need ori_x
-    cargs = [fake] * 8
+    cargs = hb.combine_args()
     cargs[4] = None
-    assert lib.cq_combine(_c(dict(cfg, copy_expert_num=1)), *cargs, 0, fake, None) == \
+    assert lib.cq_combine(_c(dict(cfg, copy_expert_num=1)), *cargs, 0, hb["y"], None) == \
         _lib.CQ_ERR_ARG
-    assert lib.cq_combine(_c(cfg), *([fake] * 8), 2, fake, None) == _lib.CQ_ERR_ARG
+    assert lib.cq_combine(_c(cfg), *hb.combine_args(), 2, hb["y"], None) == _lib.CQ_ERR_ARG
     assert lib.cq_read_status(None, None, None) == _lib.CQ_ERR_ARG
     assert lib.cq_read_combine_status(None, None) == _lib.CQ_ERR_ARG
     assert lib.cq_check_bounded_wait(None, None, None) == _lib.CQ_ERR_ARG
     assert lib.cq_workspace_init(None, 0, None) == _lib.CQ_ERR_ARG
-    for code in (0, -1, -2, -3, -4, -99):
+    for code in (0, -1, -2, -3, -4, -5, -99):
         assert isinstance(lib.cq_strerror(code), bytes)
+
+
+@needs_no_gpu
+@pytest.mark.parametrize("which", ["x", "expand_x", "assist", "dyn", "smooth"])
+def test_permute_half_errors_before_the_route_half(lib, which):
+    """An argument only the permute half uses (a misaligned token row, code
+    row, assist_info, scale row or smooth table) is rejected before the route
+    half is enqueued: the call returns CQ_ERR_ARG, not the CQ_ERR_CUDA that a
+    route launch attempted without a GPU would give."""
+    cfg = make_config(ep_world_size=4, moe_expert_num=8, max_bs=8, topk=2, hidden=1024,
+                      quant_mode=2)
+    hb = _HostBufs(cfg)
+    args = hb.dispatch_args()
+    pos = {"x": 0, "smooth": 2, "expand_x": 6, "dyn": 7, "assist": 8}[which]
+    args[pos] = ctypes.c_void_p(args[pos].value + (2 if which == "dyn" else 1))
+    assert lib.cq_dispatch(_c(cfg), *args, 4 << 20, None) == _lib.CQ_ERR_ARG
+    assert lib.cq_dispatch_noalloc(_c(cfg), *args[:12], None) in (_lib.CQ_ERR_ARG,
+                                                                  _lib.CQ_ERR_CUDA)
 
 
 def test_python_config_roundtrip(lib):

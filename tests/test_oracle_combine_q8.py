@@ -23,10 +23,28 @@ def test_golden_block(oracle_lib):
     assert np.all(codes[8:] == 0) and np.all(scales[1:] == 0)  # zero blocks
 
 
+def test_golden_block_fp16_hop(oracle_lib):
+    """[PERF] casts the quotient float -> fp16 -> int8: a hand-worked block whose
+    quotients all sit within half an fp16 spacing of a .5 tie, so the two-step
+    cast and a single rounding disagree on every value but the block max."""
+    g = json.load(open(os.path.join(GOLD, "combine_int8_fp16_hop.json")))
+    row = np.zeros(1024, np.float32)
+    row[:8] = g["block"]
+    bits = to_bf16_bits(row)
+    assert np.array_equal(bf16_bits_to_f32(bits)[:8], np.float32(g["block"]))  # exact in bf16
+    codes, scales = oracle.combine_quant_row(bits)
+    assert hex(int(np.float32(scales[0]).view(np.uint32))) == g["scale_hex"]
+    assert codes[:8].tolist() == g["codes"]
+    assert codes[:8].tolist() != g["codes_one_rounding"]
+
+
 def test_matches_torch_composition_and_bound(oracle_lib):
+    """The chain Div -> fp16 -> int8 composed from torch's own casts (binary32
+    division, .half() rounds to nearest even, torch.round is half-to-even)."""
     rng = np.random.default_rng(0)
     H = 2048
     inv_param = torch.tensor(1.0, dtype=torch.float32) / torch.tensor(127.0, dtype=torch.float32)
+    n_hop = 0
     for t in range(10):
         v = (rng.standard_normal(H) * np.exp(rng.normal(0, 3))).astype(np.float32)
         v[rng.integers(0, H, 30)] = 0.0
@@ -34,12 +52,18 @@ def test_matches_torch_composition_and_bound(oracle_lib):
         codes, scales = oracle.combine_quant_row(bits)
         x = torch.from_numpy(bf16_bits_to_f32(bits)).view(-1, 8)
         s = x.abs().amax(dim=1) * inv_param
-        q = torch.nan_to_num(torch.round(x / s[:, None]), nan=0.0).clamp(-128, 127)
+        quot = x / s[:, None]
+        q = torch.nan_to_num(torch.round(quot.half().float()), nan=0.0).clamp(-128, 127)
+        one = torch.nan_to_num(torch.round(quot), nan=0.0).clamp(-128, 127)
+        n_hop += int((q != one).sum())
         assert np.array_equal(scales, s.numpy())
         assert np.array_equal(codes.reshape(-1, 8), q.to(torch.int8).numpy())
+        # the fp16 step moves a quotient by at most half an fp16 spacing
+        # (2^-5 for |q| < 128), so a code is within 0.5 + 2^-5 steps of v
         deq = codes.astype(np.float64).reshape(-1, 8) * scales[:, None].astype(np.float64)
         err = np.abs(deq - x.numpy().astype(np.float64))
-        assert np.all(err <= 0.5 * scales[:, None] * (1 + 1e-5) + 1e-38)
+        assert np.all(err <= (0.5 + 2.0 ** -5) * scales[:, None] * (1 + 1e-5) + 1e-38)
+    assert n_hop > 0  # the inputs reach quotients where the fp16 step matters
 
 
 def test_dequantising_combine_float64_bound(oracle_lib):

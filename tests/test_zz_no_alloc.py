@@ -24,7 +24,7 @@ DEV = torch.device("cuda:0")
 def _inputs(wl):
     t = lambda a, dt: None if a is None else torch.from_numpy(  # noqa: E731
         np.ascontiguousarray(a)).to(DEV).view(dt)
-    sm = t(wl.smooth, torch.float32) if wl.cfg["quant_mode"] == 2 else None
+    sm = t(wl.smooth, torch.float32) if wl.cfg["quant_mode"] in (1, 2, 3) else None
     return dict(x=t(wl.x, torch.bfloat16), expert_ids=t(wl.expert_ids, torch.int32),
                 smooth_scales=sm, x_active_mask=t(wl.mask, torch.uint8),
                 bs_per_rank=t(wl.bs_per_rank, torch.int32),
@@ -65,26 +65,35 @@ def _same(cfg, a, b):
     return R
 
 
+def _check_case(wl):
+    cfg = cq.Config.from_dict(wl.cfg)
+    inp = _inputs(wl)
+    ref = cq.dispatch(cfg, **inp)  # the existing entry point, with its own workspace
+    got = cq.alloc_dispatch_outputs(cfg, DEV)
+    assert _noalloc(cfg, inp, got) == _lib.CQ_OK
+    torch.cuda.synchronize()
+    return _same(cfg, ref, got)
+
+
 def test_noalloc_matches_dispatch_on_two_calls_in_a_row():
     cases = [workloads.dsv3(seed=41, W=8, BS=40, M=64, K=8, H=2048),
              workloads.special(seed=42, W=8, BS=24, H=1024, M=48)]
     for wl in cases:  # two different problems back to back share the scratch array
-        cfg = cq.Config.from_dict(wl.cfg)
-        inp = _inputs(wl)
-        ref = cq.dispatch(cfg, **inp)  # the existing entry point, with its own workspace
-        got = cq.alloc_dispatch_outputs(cfg, DEV)
-        assert _noalloc(cfg, inp, got) == _lib.CQ_OK
-        torch.cuda.synchronize()
-        assert _same(cfg, ref, got) > 0
+        assert _check_case(wl) > 0
     # and the first problem once more, after the second left its data behind
-    wl = cases[0]
-    cfg = cq.Config.from_dict(wl.cfg)
-    inp = _inputs(wl)
-    ref = cq.dispatch(cfg, **inp)
-    got = cq.alloc_dispatch_outputs(cfg, DEV)
-    assert _noalloc(cfg, inp, got) == _lib.CQ_OK
-    torch.cuda.synchronize()
-    _same(cfg, ref, got)
+    _check_case(cases[0])
+
+
+def test_noalloc_per_expert_smooth_and_mx_after_a_larger_problem():
+    """The per-expert-smooth path (its row table is the largest part of the
+    scratch) and mode 5, each right after a larger problem has filled more of
+    the array, so that any byte read before this call writes it would show."""
+    big = workloads.skew(seed=44, W=16, BS=64, M=64, K=16, H=1024)   # mode 2, per-expert smooth
+    assert cq.Config.from_dict(big.cfg).workspace_size <= _lib.NOALLOC_SCRATCH_BYTES
+    smooth_small = workloads.skew(seed=45, W=4, BS=24, M=16, K=8, H=2048)
+    mx_small = workloads.mxfp8(seed=46, W=4, BS=20, M=16, K=4, H=1024)
+    for wl in (big, smooth_small, big, mx_small, smooth_small):
+        assert _check_case(wl) > 0
 
 
 def test_python_wrapper_matches_dispatch():
@@ -99,15 +108,14 @@ def test_python_wrapper_matches_dispatch():
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
+    """A problem whose workspace exceeds the built-in array is refused with
+    CQ_ERR_TOO_LARGE on the host. Every pointer is NULL: the size check comes
+    first, and were it ever skipped, the NULL token rows would be refused too
+    (CQ_ERR_ARG) before anything is enqueued."""
     cfg = cq.Config(ep_world_size=256, moe_expert_num=512, max_bs=512, topk=16, hidden=4096,
                     quant_mode=2)
     assert cfg.check() == 0 and cfg.workspace_size > _lib.NOALLOC_SCRATCH_BYTES
-
-    class _T:  # stand-ins: the call must fail before touching any pointer
-        def data_ptr(self):
-            return 0x10000
-
-    inp = dict(x=_T(), expert_ids=_T(), smooth_scales=None, x_active_mask=None,
+    inp = dict(x=None, expert_ids=None, smooth_scales=None, x_active_mask=None,
                bs_per_rank=None, expert_scales=None)
-    fake = cq.DispatchResult(_T(), _T(), _T(), _T(), _T(), None)
-    assert _noalloc(cfg, inp, fake) == _lib.CQ_ERR_TOO_LARGE
+    none = cq.DispatchResult(None, None, None, None, None, None)
+    assert _noalloc(cfg, inp, none) == _lib.CQ_ERR_TOO_LARGE
