@@ -8,9 +8,10 @@ synthetic inputs; ``build`` compiles the library in-tree.
 """
 from .api import (Config, DispatchResult, alloc_dispatch_outputs, alloc_workspace,  # noqa: F401
                   assist_views, check_bounded_wait, combine, combine_q8, combine_quant,
-                  cq_check_bounded_wait, cq_combine, cq_combine_q8,
-                  cq_combine_quant, cq_dispatch, cq_dispatch_noalloc, cq_dispatch_permute,
+                  combine_ws, cq_check_bounded_wait, cq_combine, cq_combine_q8,
+                  cq_combine_quant, cq_combine_ws, cq_dispatch, cq_dispatch_noalloc, cq_dispatch_permute,
                   cq_dispatch_route, cq_read_combine_status, cq_read_status, dispatch,
                   dispatch_noalloc, dispatch_permute, dispatch_route, moe_combine, moe_dispatch,
                   read_combine_status, read_status)
-from ._lib import CqError  # noqa: F401
+from ._lib import (CQ_ST_BAD_ID, CQ_ST_BAD_MASK, CQ_ST_INTERNAL, CQ_ST_TIMEOUT,  # noqa: F401
+                   CqError)

@@ -39,7 +39,7 @@ EXPORTS = (
     "cq_assist_info_size", "cq_workspace_size", "cq_workspace_init", "cq_dispatch",
     "cq_dispatch_route", "cq_dispatch_permute", "cq_combine", "moe_dispatch", "moe_combine",
     "cq_read_status", "cq_strerror", "cq_dispatch_noalloc", "cq_combine_quant", "cq_combine_q8",
-    "cq_read_combine_status", "cq_check_bounded_wait",
+    "cq_read_combine_status", "cq_check_bounded_wait", "cq_combine_ws",
 )
 
 
@@ -83,6 +83,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "cq_dispatch_permute": ([cfgp] + [P] * 11 + [sz, P], ctypes.c_int),
         "cq_combine": ([cfgp] + [P] * 8 + [i32, P, P], ctypes.c_int),
         "moe_combine": ([cfgp] + [P] * 8 + [i32, P, P], ctypes.c_int),
+        "cq_combine_ws": ([cfgp] + [P] * 8 + [i32, P, P, sz, P], ctypes.c_int),
         "cq_read_status": ([P, P, P], ctypes.c_int),
         "cq_read_combine_status": ([P, P], ctypes.c_int),
         "cq_check_bounded_wait": ([P, P, P], ctypes.c_int),

@@ -299,10 +299,15 @@ def combine(cfg: Config, expand_x_ffn: torch.Tensor, assist_info: torch.Tensor,
             const_alpha2: Optional[torch.Tensor] = None,
             const_v: Optional[torch.Tensor] = None,
             out_dtype: Optional[torch.dtype] = None,
-            y: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """MoE combine (cq_combine): y [W, BS, H] in the token dtype (default) or float32."""
+            y: Optional[torch.Tensor] = None,
+            workspace: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """MoE combine (cq_combine): y [W, BS, H] in the token dtype (default) or
+    float32. With `workspace` (the dispatch workspace of the same config) the
+    call is cq_combine_ws: its status goes to that workspace (read_status)."""
     W, BS, K, H = cfg.ep_world_size, cfg.max_bs, cfg.topk, cfg.hidden
     dev = assist_info.device
+    if workspace is not None:
+        _check_workspace(workspace, dev)
     _need(expand_x_ffn, "expand_x_ffn", cfg.token_dtype, (cfg.max_rows, H), dev)
     _need(assist_info, "assist_info", torch.int32, (cfg.assist_info_size,), dev)
     _need(expert_scales, "expert_scales", torch.float32, (W, BS, K), dev)
@@ -321,13 +326,22 @@ def combine(cfg: Config, expand_x_ffn: torch.Tensor, assist_info: torch.Tensor,
         y = torch.empty(W, BS, H, dtype=out_dtype, device=dev)
     _need(y, "y", out_dtype, (W, BS, H), dev)
     c = cfg.as_c()
+    args = (ctypes.byref(c), _ptr(expand_x_ffn), _ptr(assist_info), _ptr(ep_recv_count),
+            _ptr(expert_scales), _ptr(ori_x), _ptr(const_alpha1), _ptr(const_alpha2),
+            _ptr(const_v), 0 if out_dtype != torch.float32 else 1, _ptr(y))
     with torch.cuda.device(dev):  # the library looks up the current device
-        rc = _lib.load().cq_combine(
-            ctypes.byref(c), _ptr(expand_x_ffn), _ptr(assist_info), _ptr(ep_recv_count),
-            _ptr(expert_scales), _ptr(ori_x), _ptr(const_alpha1), _ptr(const_alpha2), _ptr(const_v),
-            0 if out_dtype != torch.float32 else 1, _ptr(y), _stream(dev))
-    _lib.check(rc, "cq_combine")
+        if workspace is None:
+            rc = _lib.load().cq_combine(*args, _stream(dev))
+        else:
+            rc = _lib.load().cq_combine_ws(*args, _ptr(workspace), workspace.numel(), _stream(dev))
+    _lib.check(rc, "cq_combine" if workspace is None else "cq_combine_ws")
     return y
+
+
+def combine_ws(cfg: Config, expand_x_ffn: torch.Tensor, assist_info: torch.Tensor,
+               expert_scales: torch.Tensor, workspace: torch.Tensor, **kw) -> torch.Tensor:
+    """cq_combine_ws: combine whose status goes to `workspace` (read_status)."""
+    return combine(cfg, expand_x_ffn, assist_info, expert_scales, workspace=workspace, **kw)
 
 
 def combine_quant(cfg: Config, expand_x_ffn: torch.Tensor, assist_info: torch.Tensor,
@@ -439,6 +453,7 @@ cq_dispatch_route = dispatch_route
 cq_dispatch_permute = dispatch_permute
 cq_dispatch_noalloc = dispatch_noalloc
 cq_combine = moe_combine = combine
+cq_combine_ws = combine_ws
 cq_combine_quant = combine_quant
 cq_combine_q8 = combine_q8
 cq_read_status = read_status

@@ -320,6 +320,24 @@ int cq_combine(const cq_config* cfg, const void* expand_x_ffn, const int32_t* as
                                                                                    : CQ_ERR_CUDA;
 }
 
+int cq_combine_ws(const cq_config* cfg, const void* expand_x_ffn, const int32_t* assist_info,
+                  const int32_t* ep_recv_count, const float* expert_scales, const void* ori_x,
+                  const float* const_alpha1, const float* const_alpha2, const void* const_v,
+                  int32_t out_dtype, void* y, void* workspace, size_t workspace_bytes,
+                  void* stream) {
+  (void)ep_recv_count;
+  cq::CombineArgs a;
+  int rc = combine_args(cfg, assist_info, expert_scales, ori_x, const_alpha1, const_alpha2,
+                        const_v, out_dtype, y, &a);
+  if (rc != CQ_OK) return rc;
+  if (!expand_x_ffn || !aligned(expand_x_ffn, 16)) return CQ_ERR_ARG;
+  if ((rc = check_ws(a.d, workspace, workspace_bytes)) != CQ_OK) return rc;
+  a.ffn = static_cast<const uint16_t*>(expand_x_ffn);
+  a.status = cq::carve(workspace, a.d).status;
+  return cq::launch_combine(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? CQ_OK
+                                                                                   : CQ_ERR_CUDA;
+}
+
 int cq_combine_quant(const cq_config* cfg, const void* expand_x_ffn, const int32_t* assist_info,
                      int8_t* ffn_codes, float* ffn_scales, void* stream) {
   int rc = validate(cfg);

@@ -241,7 +241,8 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(CombineArgs a, Src sr
 constexpr int kRingMax = 16;
 
 // Sticky status of the combine kernels of this device (CQ_ST_* bits), read
-// and cleared by cq_read_combine_status.
+// and cleared by cq_read_combine_status; a call given a workspace reports to
+// that workspace's status word instead.
 __device__ uint32_t g_combine_status;
 
 constexpr int kUnitsPerThread = 4;  // 8-element units per consumer thread
@@ -276,6 +277,7 @@ __global__ void __launch_bounds__(288) combine_staged_kernel(CombineArgs a, int 
   const Dims& d = a.d;
   const int H = d.H;
   const uint32_t slot_bytes = 2u * (uint32_t)cw;
+  uint32_t* const st_word = a.status ? a.status : &g_combine_status;
   const int ncons = (int)blockDim.x - 32;  // consumer threads
   const int nwc = ncons >> 5;              // consumer warps
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -312,7 +314,7 @@ __global__ void __launch_bounds__(288) combine_staged_kernel(CombineArgs a, int 
           if (issued >= nslots &&
               !mbar_wait(&s_empty[s], (uint32_t)((issued / nslots) - 1) & 1u)) {
             s_fail = 1;
-            atomicOr(&g_combine_status, (uint32_t)CQ_ST_TIMEOUT);
+            atomicOr(st_word, (uint32_t)CQ_ST_TIMEOUT);
           }
           if (!s_fail) {
             mbar_arrive_expect_tx(&s_full[s], bytes);
@@ -362,7 +364,7 @@ __global__ void __launch_bounds__(288) combine_staged_kernel(CombineArgs a, int 
         // The whole warp leaves together if any lane gave up.
         if (!__all_sync(0xffffffffu, mbar_wait(&s_full[s], (uint32_t)(consumed / nslots) & 1u))) {
           s_fail = 1;
-          if (lane == 0) atomicOr(&g_combine_status, (uint32_t)CQ_ST_TIMEOUT);
+          if (lane == 0) atomicOr(st_word, (uint32_t)CQ_ST_TIMEOUT);
           return;
         }
         const uint8_t* rowp = s_ring + (size_t)s * slot_bytes;

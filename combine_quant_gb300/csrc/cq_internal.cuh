@@ -131,6 +131,7 @@ struct CombineArgs {
   const uint16_t* const_v;
   void* y;
   int32_t out_f32;
+  uint32_t* status;  // CQ_ST_* word of this call (a workspace's), or NULL: the device's own
 };
 
 // The two 16-bit token types. In a packed 32-bit word element 2t is the low

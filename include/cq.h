@@ -30,7 +30,7 @@
  *   - Data-dependent problems found on the device (an out-of-range expert
  *     id, a 1-D mask that is not a prefix, a bounded wait that gave up) never
  *     trap: they set sticky bits in the workspace status word, read with
- *     cq_read_status (the combine kernels, which take no workspace, in a
+ *     cq_read_status (the combine calls that take no workspace, in a
  *     per-device word read with cq_read_combine_status).
  *
  * Notation: W = ep_world_size, M = moe_expert_num, S = shared_expert_num,
@@ -216,6 +216,19 @@ int cq_combine(const cq_config* cfg, const void* expand_x_ffn, const int32_t* as
                const float* const_alpha1, const float* const_alpha2, const void* const_v,
                int32_t out_dtype, void* y, void* stream);
 
+/* cq_combine reporting to a workspace: the same operation and arguments, plus
+ * the dispatch workspace of the same config (>= cq_workspace_size() bytes,
+ * 256-byte aligned; CQ_ERR_WORKSPACE otherwise). A bounded wait that gave up
+ * sets CQ_ST_TIMEOUT in that workspace's status word, read and cleared with
+ * cq_read_status, instead of the per-device word of cq_read_combine_status;
+ * so pipelines on different streams, each with its own workspace, see only
+ * their own status. Only the status word of the workspace is touched. */
+int cq_combine_ws(const cq_config* cfg, const void* expand_x_ffn, const int32_t* assist_info,
+                  const int32_t* ep_recv_count, const float* expert_scales, const void* ori_x,
+                  const float* const_alpha1, const float* const_alpha2, const void* const_v,
+                  int32_t out_dtype, void* y, void* workspace, size_t workspace_bytes,
+                  void* stream);
+
 /*
  * Combine with int8 expert outputs ("CANN MoE Dispatch/Combine 通信算子性能
  * 优化实践", 通信前量化: Combine 发送前按 block 量化为 int8, Int8QuantProcess /
@@ -291,9 +304,10 @@ int cq_dispatch_noalloc(const cq_config* cfg, const void* x, const int32_t* expe
  * it. One of the two calls in this library that wait for the device. */
 int cq_read_status(void* workspace, uint32_t* status, void* stream);
 
-/* The combine kernels take no workspace; their status word (CQ_ST_TIMEOUT
- * only: a bounded wait for the kernel's own bulk loads gave up) is one word
- * per device inside the library, shared by all combine calls on that device.
+/* cq_combine and cq_combine_q8 take no workspace; their status word
+ * (CQ_ST_TIMEOUT only: a bounded wait for the kernel's own bulk loads gave
+ * up) is one word per device inside the library, shared by all such combine
+ * calls on that device (cq_combine_ws reports to its workspace instead).
  * Synchronise `stream`, copy the word of the current device into *status and
  * clear it. Returns CQ_ERR_ARG if status is NULL, CQ_ERR_CUDA on a CUDA
  * error. */

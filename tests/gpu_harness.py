@@ -2,6 +2,9 @@
 compare it with the oracle on the same seeded inputs."""
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import torch
 
@@ -69,47 +72,6 @@ def smooth_args(wl, src, tok, k):
     K = wl.cfg["topk"]
     s_eff = wl.cfg["shared_expert_num"] if wl.cfg["shared_expert_rank_num"] > 0 else 0
     return (wl.smooth[s_eff + wl.expert_ids[src, tok, k]] if k < K else wl.smooth[k - K]), None
-
-
-def compare_rows(wl, out, ref_route, sample):
-    """expand_x / dynamic_scales / expand_scales of the sampled rows against
-    the oracle's quantisation of their source tokens."""
-    mode = wl.cfg["quant_mode"]
-    K = wl.cfg["topk"]
-    sample = np.asarray(sorted(set(int(s) for s in sample)), np.int64)
-    if sample.size == 0:
-        return 0
-    idx = torch.from_numpy(sample).to(DEV)
-    ex = host(out.expand_x.index_select(0, idx))
-    dyn = host(out.dynamic_scales.index_select(0, idx)) if out.dynamic_scales is not None else None
-    es = host(out.expand_scales.index_select(0, idx)) if out.expand_scales is not None else None
-    for n, row in enumerate(sample):
-        src, tok, k = ref_route.assist[row, :3]
-        sm_row, sm_scalar = smooth_args(wl, src, tok, k)
-        codes, scale = oracle.quant_row(mode, wl.x[src, tok], sm_row, wl.cfg.get("x_dtype", 0),
-                                        sm_scalar, wl.cfg.get("y_dtype", 0))
-        assert np.array_equal(ex[n].view(codes.dtype), codes), f"expand_x row {row}"
-        if mode == 2:
-            assert dyn[n] == scale, f"dynamic_scales row {row}"
-        elif mode == 3:
-            assert np.array_equal(dyn[n].view(np.uint32), scale.view(np.uint32)), f"row {row}"
-        elif mode in (4, 5):
-            assert np.array_equal(dyn[n], scale), f"mx scales row {row}"
-        if es is not None:
-            want = wl.expert_scales[src, tok, k] if k < K else np.float32(1.0)
-            assert es[n] == want, f"expand_scales row {row}"
-    return sample.size
-
-
-def sample_rows(ref_route, rng, n_random=256):
-    R = ref_route.rows
-    if R == 0:
-        return []
-    base = ref_route.rank_row_base
-    picks = list(range(min(32, R))) + list(range(max(0, R - 32), R))
-    picks += [int(b) for b in base[:-1] if b < R] + [int(b) - 1 for b in base[1:] if b > 0]
-    picks += list(rng.integers(0, R, n_random))
-    return picks
 
 
 class FfnStandin:
@@ -188,3 +150,108 @@ def bf16_ulp_diff(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:
         b = b.astype(np.int32)
         return np.where(b & 0x8000, -(b & 0x7fff), b & 0x7fff)
     return np.abs(key(a_bits) - key(b_bits))
+
+
+# ---------------------------------------------------------------------------
+# Element-complete comparison at full size. The oracle works token by token
+# (its C calls release the GIL, so a thread pool spreads them over the host
+# cores); the GPU outputs are copied back in chunks of tokens, so host memory
+# stays bounded whatever the workload's size.
+
+_POOL = None
+
+
+def pool() -> ThreadPoolExecutor:
+    global _POOL
+    if _POOL is None:
+        _POOL = ThreadPoolExecutor(max_workers=max(1, min(32, os.cpu_count() or 1)))
+    return _POOL
+
+
+def _quant_expect(wl, src, tok, k):
+    sm_row, sm_scalar = smooth_args(wl, src, tok, k)
+    return oracle.quant_row(wl.cfg["quant_mode"], wl.x[src, tok], sm_row,
+                            wl.cfg.get("x_dtype", 0), sm_scalar, wl.cfg.get("y_dtype", 0))
+
+
+def compare_rows_complete(wl, out, ref_route, tok_chunk: int = 512) -> int:
+    """Every dispatched row against the oracle's quantisation of its source
+    token (per routed slot when the smooth scales differ per expert, else once
+    per token): codes, carried scales and routing weights bit for bit. The
+    rows are reached through the inverse map, which compare_route has already
+    matched with the oracle's; returns the number of rows checked (all R)."""
+    cfg = wl.cfg
+    mode, K = cfg["quant_mode"], cfg["topk"]
+    W, BS = cfg["ep_world_size"], cfg["max_bs"]
+    NS = ref_route.inv.shape[2]
+    per_slot = uses_smooth(wl) and cfg.get("smooth_kind", 0) == 0
+    inv = ref_route.inv.reshape(W * BS, NS)
+    checked = 0
+    for t0 in range(0, W * BS, tok_chunk):
+        sub = inv[t0:t0 + tok_chunk]
+        tt, kk = np.nonzero(sub >= 0)
+        if tt.size == 0:
+            continue
+        rows = sub[tt, kk].astype(np.int64)
+        idx = torch.from_numpy(rows).to(DEV)
+        ex = host(out.expand_x.index_select(0, idx))
+        dyn = host(out.dynamic_scales.index_select(0, idx)) if out.dynamic_scales is not None \
+            else None
+        es = host(out.expand_scales.index_select(0, idx)) if out.expand_scales is not None \
+            else None
+        toks = t0 + tt
+        keys = list(zip(toks.tolist(), kk.tolist())) if per_slot else \
+            sorted(set((t, 0) for t in toks.tolist()))
+        exp = dict(zip(keys, pool().map(
+            lambda key: _quant_expect(wl, key[0] // BS, key[0] % BS, key[1]), keys)))
+        for n in range(rows.size):
+            t, k = int(toks[n]), int(kk[n])
+            codes, scale = exp[(t, k) if per_slot else (t, 0)]
+            assert np.array_equal(ex[n].view(codes.dtype), codes), f"expand_x row {rows[n]}"
+            if mode == 2:
+                assert dyn[n].view(np.uint32) == np.float32(scale).view(np.uint32), \
+                    f"dynamic_scales row {rows[n]}"
+            elif mode == 3:
+                assert np.array_equal(dyn[n].view(np.uint32), scale.view(np.uint32)), \
+                    f"group scales row {rows[n]}"
+            elif mode in (4, 5):
+                assert np.array_equal(dyn[n], scale), f"mx scales row {rows[n]}"
+            if es is not None:
+                src, tok = divmod(t, BS)
+                want = wl.expert_scales[src, tok, k] if k < K else np.float32(1.0)
+                assert es[n] == want, f"expand_scales row {rows[n]}"
+        checked += rows.size
+    assert checked == ref_route.rows
+    return checked
+
+
+def _oracle_combine_chunk(fn, toks, n_parts):
+    parts = [toks[i::n_parts] for i in range(n_parts)]  # some may be empty
+    res = list(pool().map(fn, parts))
+    out = np.empty((len(toks),) + res[0].shape[1:], res[0].dtype)
+    for i, r in enumerate(res):
+        out[i::n_parts][:len(r)] = r
+    return out
+
+
+def compare_combine_complete(wl, y32: torch.Tensor, y16: torch.Tensor, oracle_tokens,
+                             tok_chunk: int = 1024) -> int:
+    """Every token of y (fp32 and the token type) against the oracle:
+    within 1e-5 and 1 ulp, and exactly equal (the same operation order).
+    oracle_tokens(tokens, out_f32) -> [len(tokens), H]."""
+    W, BS = wl.cfg["ep_world_size"], wl.cfg["max_bs"]
+    g32v = y32.view(W * BS, -1)
+    g16v = y16.view(W * BS, -1)
+    n = max(1, min(32, os.cpu_count() or 1))
+    for t0 in range(0, W * BS, tok_chunk):
+        t1 = min(W * BS, t0 + tok_chunk)
+        toks = [divmod(t, BS) for t in range(t0, t1)]
+        g32 = host(g32v[t0:t1])
+        g16 = host(g16v[t0:t1])
+        r32 = _oracle_combine_chunk(lambda p: oracle_tokens(p, True), toks, n)
+        r16 = _oracle_combine_chunk(lambda p: oracle_tokens(p, False), toks, n)
+        assert np.max(np.abs(g32 - r32)) <= 1e-5, f"tokens {t0}..{t1}"
+        assert np.max(bf16_ulp_diff(g16, r16)) <= 1, f"tokens {t0}..{t1}"
+        assert np.array_equal(g32.view(np.uint32), r32.view(np.uint32)), f"tokens {t0}..{t1}"
+        assert np.array_equal(g16, r16), f"tokens {t0}..{t1}"
+    return W * BS

@@ -1,8 +1,8 @@
 """GPU parity: the CUDA path (through the C ABI) against the oracle.
 
-Small configurations are compared element by element on every output; the
-five full-size workloads are compared bit-exactly on every routing output
-and on sampled rows / tokens for the quantised rows and the combine output.
+Small configurations and the full-size workloads alike are compared element
+by element on every output (at full size the oracle runs token by token on a
+thread pool and the GPU outputs come back in chunks).
 Tolerances: index, count and code outputs bit-exact; the int8 scale and the
 mx scale bytes bit-exact; combine within 1e-5 of the fp32 oracle value and
 within 1 bf16 ulp after the cast (both kernels use the same fused
@@ -67,34 +67,34 @@ def test_small_full_parity(name):
     _check_combine_full(wl, cfg, out, route)
 
 
-FULL = ["dsv3", "mxfp8", "special", "skew"]
+FULL = ["tiny", "dsv3", "mxfp8", "special", "skew", "perf8", "perf256"]
 
 
 @pytest.mark.parametrize("name", FULL)
-def test_full_size_parity_sampled(name):
+def test_full_size_parity_complete(name):
+    """The five workloads at full size and the two shapes of the performance
+    table ("CANN MoE Dispatch/Combine 通信算子性能优化实践", 性能数据): every
+    routing output, every dispatched row (codes, carried scale, weight) and
+    every combined token (fp32 and bf16) against the oracle."""
     wl = workloads.WORKLOADS[name]()
     cfg, out, status, _ = gh.gpu_dispatch(wl)
     ref = oracle.route(wl.cfg, wl.expert_ids, wl.mask, wl.bs_per_rank)
     assert status == ref.status == 0
     gh.compare_route(wl, cfg, out, ref)
-    rng = np.random.default_rng(7)
-    n = gh.compare_rows(wl, out, ref, gh.sample_rows(ref, rng, 384))
-    assert n >= 256
-    # combine on sampled tokens (first and last of every rank plus random ones)
-    W, BS = wl.cfg["ep_world_size"], wl.cfg["max_bs"]
-    toks = [(r, 0) for r in range(W)] + [(r, BS - 1) for r in range(W)]
-    toks += [(int(a), int(b)) for a, b in zip(rng.integers(0, W, 96), rng.integers(0, BS, 96))]
+    assert gh.compare_rows_complete(wl, out, ref) == ref.rows
     ffn = gh.FfnStandin(wl, cfg.max_rows)
     y32 = gh.gpu_combine(wl, cfg, out, ffn, torch.float32)
-    yb = gh.gpu_combine(wl, cfg, out, ffn, torch.bfloat16)
-    ti = torch.tensor([r * BS + i for r, i in toks], device=gh.DEV)
-    g32 = gh.host(y32.view(W * BS, -1).index_select(0, ti))
-    gb = gh.host(yb.view(W * BS, -1).index_select(0, ti))
-    r32 = gh.oracle_combine_tokens(wl, ref, ffn, toks, out_f32=True)
-    rb = gh.oracle_combine_tokens(wl, ref, ffn, toks, out_f32=False)
-    assert np.max(np.abs(g32 - r32)) <= 1e-5
-    assert np.max(gh.bf16_ulp_diff(gb, rb)) <= 1
-    assert np.array_equal(gb, rb)
+    yb = gh.gpu_combine(wl, cfg, out, ffn, None)
+    assert gh.cq.read_combine_status() == 0
+    inv = ffn.remap_inv(ref.inv)
+
+    def oracle_tokens(toks, out_f32):
+        return oracle.combine_tokens(wl.cfg, toks, ffn.pool, inv, wl.expert_scales, wl.x,
+                                     wl.const_alpha1, wl.const_alpha2, wl.const_v,
+                                     out_f32=out_f32)
+
+    assert gh.compare_combine_complete(wl, y32, yb, oracle_tokens) == \
+        wl.cfg["ep_world_size"] * wl.cfg["max_bs"]
 
 
 def _cfg_case(seed, **kw):

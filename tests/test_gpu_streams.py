@@ -32,7 +32,9 @@ def _run(cfg, args, ws, ffn, steps):
         out = cq.dispatch(cfg, args["x"], args["ids"], smooth_scales=args["sm"],
                           x_active_mask=args["mask"], bs_per_rank=args["bpr"],
                           expert_scales=args["w"], workspace=ws, out=out)
-        y = cq.combine(cfg, ffn.device_rows, out.assist_info, args["w"], out.ep_recv_count, y=y)
+        # each pipeline's combine reports to its own workspace (cq_combine_ws)
+        y = cq.combine(cfg, ffn.device_rows, out.assist_info, args["w"], out.ep_recv_count, y=y,
+                       workspace=ws)
     return out, y
 
 
@@ -65,6 +67,7 @@ def test_two_streams_run_independent_pipelines():
     torch.cuda.synchronize()
     for wl, (cfg, args, ws, ffn), (out, y), s in zip(wls, preps, results, streams):
         with torch.cuda.stream(s):
-            status = cq.read_status(ws)
+            status = cq.read_status(ws)  # this pipeline's dispatch and combine status
         _check(wl, ffn, out, y, status)
-    assert cq.read_combine_status() == 0
+        assert status & cq.CQ_ST_TIMEOUT == 0
+    assert cq.read_combine_status() == 0  # nothing went to the per-device word
