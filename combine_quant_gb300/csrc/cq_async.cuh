@@ -79,6 +79,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   return false;
 }
 
+// Hand a ring slot back to the producer after this warp has read it with
+// ordinary (generic-proxy) shared-memory loads. The next write into the slot
+// is a bulk copy (async proxy), which the release/acquire pair of the empty
+// mbarrier alone does not order after loads still in flight: every lane
+// first fences its reads against the async proxy, then the warp converges
+// and one lane arrives. Without the fence a warp's last loads of a slot were
+// seen returning bytes of the next row copied into it.
+__device__ __forceinline__ void release_slot(uint64_t* empty_bar) {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(empty_bar);
+}
+
 __device__ __forceinline__ uint4 ld_shared_v4(const void* p) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"

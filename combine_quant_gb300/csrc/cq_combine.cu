@@ -381,8 +381,7 @@ __global__ void __launch_bounds__(288) combine_staged_kernel(CombineArgs a, int 
             }
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s_empty[s]);
+        release_slot(&s_empty[s]);
         ++consumed;
       } else if (ck == CQ_INV_COPY || ck <= CQ_INV_CONST_BASE) {
 #pragma unroll

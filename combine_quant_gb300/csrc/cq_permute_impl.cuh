@@ -775,8 +775,7 @@ __global__ void __launch_bounds__(288, 2) smooth_rows_kernel(PermuteArgs a) {
       }
     }
     // This warp is done with the slot (token row and its smooth-row index).
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&s_empty[st]);
+    release_slot(&s_empty[st]);
     const int64_t row = lo + j;
     const float carried = quantise<Q, true, true>(f, U, out + row * H, dyn + row * scale_bytes,
                                                   s_red[j & 1], ncons);
