@@ -83,6 +83,9 @@ def parse_args(argv=None):
                     help="input/output buffer sets of the end-to-end leg (pipeline depth, >= 1)")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch each call directly instead of replaying CUDA graphs")
+    ap.add_argument("--per-workload", action=argparse.BooleanOptionalAction, default=True,
+                    help="with the default workload, also time the other workloads (a few "
+                         "steps each) and report them under per_workload")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="host time budget of the oracle baseline")
     return ap.parse_args(argv)
@@ -430,6 +433,240 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ cq arm ----
 
+class Bench:
+    """Device inputs, outputs and the step of one workload: route, permute and
+    combine through the binding, captured into CUDA graphs (the whole step,
+    and each kernel alone for the breakdown) unless --no-graph."""
+
+    def __init__(self, args, dev, wl, flush):
+        import torch
+
+        import combine_quant_gb300 as cq
+        from combine_quant_gb300 import workloads
+
+        self.args, self.dev, self.wl, self.flush = args, dev, wl, flush
+        cfg = self.cfg = cq.Config.from_dict(wl.cfg)
+        tdev = lambda a, dt: None if a is None else torch.from_numpy(  # noqa: E731
+            np.ascontiguousarray(a)).to(dev).view(dt)
+        self.x = tdev(wl.x, torch.bfloat16)
+        self.ids = tdev(wl.expert_ids, torch.int32)
+        self.w = tdev(wl.expert_scales, torch.float32)
+        self.sm = tdev(wl.smooth, torch.float32) if cfg.quant_mode in (1, 2, 3) else None
+        self.mask = tdev(wl.mask, torch.uint8)
+        self.bpr = tdev(wl.bs_per_rank, torch.int32)
+        self.ws = cq.alloc_workspace(cfg, dev)
+        self.out = cq.alloc_dispatch_outputs(cfg, dev)
+        pool = tdev(workloads.ffn_standin(wl.seed, 4096, cfg.hidden), torch.bfloat16)
+        ridx = (torch.arange(cfg.max_rows, device=dev, dtype=torch.int64) * 7919) % 4096
+        self.ffn = pool.index_select(0, ridx).contiguous()
+        self.y = torch.empty(cfg.ep_world_size, cfg.max_bs, cfg.hidden, dtype=torch.bfloat16,
+                             device=dev)
+        self.ffn_q = self.ffn_s = None
+        if args.combine == "int8":
+            # The expert side's int8 outputs, made once before timing (a producer
+            # would emit them from its own epilogue); the quantiser is timed apart.
+            self.dispatch()
+            self.ffn_q, self.ffn_s = cq.combine_quant(cfg, self.ffn, self.out.assist_info)
+        self.consts = dict(const_alpha1=tdev(wl.const_alpha1, torch.float32),
+                           const_alpha2=tdev(wl.const_alpha2, torch.float32),
+                           const_v=tdev(wl.const_v, torch.bfloat16))
+        self.stream = torch.cuda.current_stream(dev)
+        self.use_graph = not args.no_graph
+        self.parts = [self.route, self.permute, lambda: self.combine()]
+        self.run_step = self.step
+        if self.use_graph:
+            side = torch.cuda.Stream(dev)
+            side.wait_stream(self.stream)
+            graphs = {}
+            with torch.cuda.stream(side):
+                for name, fn in (("step", self.step), ("route", self.route),
+                                 ("permute", self.permute), ("combine", lambda: self.combine())):
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g, stream=side):
+                        fn()
+                    graphs[name] = g
+            self.stream.wait_stream(side)
+            torch.cuda.synchronize()
+            self.graphs = graphs
+            self.run_step = graphs["step"].replay
+            self.parts = [graphs["route"].replay, graphs["permute"].replay,
+                          graphs["combine"].replay]
+
+    def route(self):
+        import combine_quant_gb300 as cq
+        cq.dispatch_route(self.cfg, self.ids, self.mask, self.bpr, workspace=self.ws,
+                          out=self.out)
+
+    def permute(self):
+        import combine_quant_gb300 as cq
+        cq.dispatch_permute(self.cfg, self.x, self.ids, self.sm, self.w, self.mask, self.bpr,
+                            workspace=self.ws, out=self.out)
+
+    def dispatch(self, x=None, ids=None, w=None):
+        import combine_quant_gb300 as cq
+        return cq.dispatch(self.cfg, self.x if x is None else x, self.ids if ids is None else ids,
+                           smooth_scales=self.sm, x_active_mask=self.mask, bs_per_rank=self.bpr,
+                           expert_scales=self.w if w is None else w, workspace=self.ws,
+                           out=self.out)
+
+    def combine(self, assist_info=None, erc=None, w=None, x=None, y=None):
+        import combine_quant_gb300 as cq
+        o = self.out
+        a = (o.assist_info if assist_info is None else assist_info,
+             o.ep_recv_count if erc is None else erc)
+        w = self.w if w is None else w
+        x = self.x if x is None else x
+        y = self.y if y is None else y
+        if self.args.combine == "int8":
+            return cq.combine_q8(self.cfg, self.ffn_q, self.ffn_s, a[0], w, a[1], ori_x=x, y=y,
+                                 **self.consts)
+        return cq.combine(self.cfg, self.ffn, a[0], w, a[1], ori_x=x, y=y, **self.consts)
+
+    def step(self, evs=None):
+        """One pass of the path. With 4 events, each kernel is bracketed (the
+        events between kernels also stop the next kernel from starting early);
+        with 2, only the step's start and end are recorded."""
+        if evs:
+            evs[0].record(self.stream)
+        self.route()
+        if evs and len(evs) == 4:
+            evs[1].record(self.stream)
+        self.permute()
+        if evs and len(evs) == 4:
+            evs[2].record(self.stream)
+        self.combine()
+        if evs:
+            evs[-1].record(self.stream)
+
+    def warm(self, n):
+        import torch
+        for _ in range(n):
+            self.flush.zero_()
+            self.step()
+        torch.cuda.synchronize()
+
+    def breakdown(self, n, barrier):
+        """Per-kernel times (ms lists) from n steps with events between kernels."""
+        import torch
+        evb = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+        barrier()
+        for k in range(n):
+            self.flush.zero_()
+            for j, part in enumerate(self.parts):
+                evb[k][j].record(self.stream)
+                part()
+            evb[k][3].record(self.stream)
+        barrier()
+        return ([e[0].elapsed_time(e[1]) for e in evb], [e[1].elapsed_time(e[2]) for e in evb],
+                [e[2].elapsed_time(e[3]) for e in evb])
+
+    def timed(self, n, barrier, clocks=None):
+        """n steps, L2 flushed between them outside the events: step times (ms)."""
+        import torch
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+        barrier()
+        if clocks:
+            clocks.start()
+        t_wall = time.perf_counter()
+        for k in range(n):
+            self.flush.zero_()
+            ev[k][0].record(self.stream)
+            self.run_step()
+            ev[k][1].record(self.stream)
+        barrier()
+        self.t_wall = time.perf_counter() - t_wall
+        return [e[0].elapsed_time(e[1]) for e in ev]
+
+    def counts(self):
+        """(dispatched rows, active tokens, smooth bytes, tokens with special slots)."""
+        import combine_quant_gb300 as cq
+        cfg, wl = self.cfg, self.wl
+        rows = int(cq.assist_views(cfg, self.out.assist_info)[2][-1].item())
+        tokens = wl.tokens
+        if wl.mask is not None:
+            tokens = int((wl.mask.reshape(cfg.ep_world_size, cfg.max_bs, -1).max(axis=2)
+                          > 0).sum())
+        smooth_bytes = int(self.sm.numel() * 4) if self.sm is not None else 0
+        return rows, tokens, smooth_bytes, special_token_count(wl)
+
+
+# Workloads whose figures the default run adds beside the headline (key
+# "per_workload"): the other four configurations and the two shapes of the
+# performance table ("CANN MoE Dispatch/Combine 通信算子性能优化实践", 性能数据).
+SIDE_WORKLOADS = ("tiny", "mxfp8", "special", "skew", "perf8", "perf256")
+
+
+def side_figures(args, dev, flush, barrier, peak):
+    """Step and per-kernel times of the side workloads, measured as the
+    headline is (graph replay, L2 flushed between steps, CUDA events), with
+    fewer steps."""
+    import torch
+
+    import combine_quant_gb300 as cq
+    from combine_quant_gb300 import workloads
+
+    steps = max(10, min(args.steps, 50))
+    res = {}
+    for name in SIDE_WORKLOADS:
+        wl = workloads.WORKLOADS[name]()
+        b = Bench(args, dev, wl, flush)
+        b.warm(3)
+        if cq.read_status(b.ws) != 0:
+            raise RuntimeError(f"device status reported a bad id or mask on {name}")
+        t_route, t_perm, t_comb = b.breakdown(steps, barrier)
+        t_step = b.timed(steps, barrier)
+        rows, tokens, smooth_bytes, special = b.counts()
+        ab = algorithmic_bytes(b.cfg, rows, tokens, with_scales=True, smooth_bytes=smooth_bytes,
+                               special_tokens=special)
+        us = {"route": 1e3 * statistics.mean(t_route), "permute": 1e3 * statistics.mean(t_perm),
+              "combine": 1e3 * statistics.mean(t_comb)}
+        step_us = 1e3 * statistics.mean(t_step)
+        res[name] = {
+            "workload": workload_desc(wl), "tokens_per_step": tokens, "rows_per_step": rows,
+            "steps": steps, "step_us": step_us, "tokens_per_s": tokens / (step_us * 1e-6),
+            "kernels": {k: {"us": us[k], "alg_bytes": ab[k],
+                            "frac": ab[k] / (us[k] * 1e-6) / 1e9 / peak} for k in us}}
+        if name == "tiny":
+            # latency-bound: the same step with L2 left warm between steps
+            saved = flush.mode
+            flush.mode = "none"
+            t_hot = b.timed(steps, barrier)
+            flush.mode = saved
+            res[name]["step_us_hot_l2"] = 1e3 * statistics.mean(t_hot)
+        del b
+        torch.cuda.empty_cache()
+    return res
+
+
+def cpu_model() -> str:
+    """The host CPU's model name from /proc/cpuinfo (or what is known)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            txt = f.read()
+    except OSError:
+        return "unknown"
+    for key in ("model name", "Model Name", "cpu model", "Hardware"):
+        for line in txt.splitlines():
+            if line.split(":")[0].strip() == key and ":" in line:
+                return line.split(":", 1)[1].strip()
+    parts = {}
+    for line in txt.splitlines():
+        if ":" in line:
+            k, v = line.split(":", 1)
+            parts.setdefault(k.strip(), v.strip())
+    if "CPU implementer" in parts:
+        # Arm cores name no model in /proc/cpuinfo; the part numbers of a few
+        # server cores (implementer 0x41 is Arm Ltd.)
+        arm_parts = {"0xd0c": "Neoverse-N1", "0xd40": "Neoverse-V1", "0xd49": "Neoverse-N2",
+                     "0xd4f": "Neoverse-V2", "0xd84": "Neoverse-V3", "0xd8e": "Neoverse-N3"}
+        name = arm_parts.get(parts.get("CPU part", "")) if parts.get("CPU implementer") == "0x41" \
+            else None
+        return ((f"Arm {name}, " if name else "")
+                + f"CPU implementer {parts.get('CPU implementer')}, part {parts.get('CPU part')}, "
+                f"variant {parts.get('CPU variant')}, revision {parts.get('CPU revision')}")
+    return "unknown"
+
+
 def run_cq(args):
     import torch
 
@@ -451,151 +688,42 @@ def run_cq(args):
             dist.barrier()
         torch.cuda.synchronize()
 
-    wl = workloads.WORKLOADS[args.workload]()
-    if args.quant_mode is not None:
-        wl = wl.with_mode(args.quant_mode)
-    cfg = cq.Config.from_dict(wl.cfg)
-    tdev = lambda a, dt: None if a is None else torch.from_numpy(  # noqa: E731
-        np.ascontiguousarray(a)).to(dev).view(dt)
-    x = tdev(wl.x, torch.bfloat16)
-    ids = tdev(wl.expert_ids, torch.int32)
-    w = tdev(wl.expert_scales, torch.float32)
-    sm = tdev(wl.smooth, torch.float32) if cfg.quant_mode in (1, 2, 3) else None
-    mask = tdev(wl.mask, torch.uint8)
-    bpr = tdev(wl.bs_per_rank, torch.int32)
-    ws = cq.alloc_workspace(cfg, dev)
-    out = cq.alloc_dispatch_outputs(cfg, dev)
-    pool = tdev(workloads.ffn_standin(wl.seed, 4096, cfg.hidden), torch.bfloat16)
-    ridx = (torch.arange(cfg.max_rows, device=dev, dtype=torch.int64) * 7919) % 4096
-    ffn = pool.index_select(0, ridx).contiguous()
-    y = torch.empty(cfg.ep_world_size, cfg.max_bs, cfg.hidden, dtype=torch.bfloat16, device=dev)
-    ffn_q = ffn_s = None
-    if args.combine == "int8":
-        # The expert side's int8 outputs, made once before timing (a producer
-        # would emit them from its own epilogue); the quantiser is timed apart.
-        cq.dispatch(cfg, x, ids, smooth_scales=sm, x_active_mask=mask, bs_per_rank=bpr,
-                    expert_scales=w, workspace=ws, out=out)
-        ffn_q, ffn_s = cq.combine_quant(cfg, ffn, out.assist_info)
-
-    consts = dict(const_alpha1=tdev(wl.const_alpha1, torch.float32),
-                  const_alpha2=tdev(wl.const_alpha2, torch.float32),
-                  const_v=tdev(wl.const_v, torch.bfloat16))
-
-    def combine_call(assist_info, erc, w_, x_, y_):
-        if args.combine == "int8":
-            return cq.combine_q8(cfg, ffn_q, ffn_s, assist_info, w_, erc, ori_x=x_, y=y_,
-                                 **consts)
-        return cq.combine(cfg, ffn, assist_info, w_, erc, ori_x=x_, y=y_, **consts)
     flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
-    stream = torch.cuda.current_stream(dev)
 
     class _Flush:
         """Between steps: write a buffer larger than L2, then (unless
         --flush write) read another one, so that the next step starts with
         no input resident in L2 and no dirty lines left to write back."""
+        mode = args.flush
 
-        @staticmethod
-        def zero_():
-            if args.flush == "none":  # hot-L2 figures only: not a contract number
+        def zero_(self):
+            if self.mode == "none":  # hot-L2 figures only: not a contract number
                 return
             flush_w.zero_()
-            if args.flush == "write+read":
+            if self.mode == "write+read":
                 flush_r.amax()
 
     flush = _Flush()
-
-    def step(evs=None):
-        """One pass of the path. With 4 events, each kernel is bracketed (the
-        events between kernels also stop the next kernel from starting early);
-        with 2, only the step's start and end are recorded."""
-        if evs:
-            evs[0].record(stream)
-        cq.dispatch_route(cfg, ids, mask, bpr, workspace=ws, out=out)
-        if evs and len(evs) == 4:
-            evs[1].record(stream)
-        cq.dispatch_permute(cfg, x, ids, sm, w, mask, bpr, workspace=ws, out=out)
-        if evs and len(evs) == 4:
-            evs[2].record(stream)
-        combine_call(out.assist_info, out.ep_recv_count, w, x, y)
-        if evs:
-            evs[-1].record(stream)
-
-    for _ in range(args.warmup):
-        flush.zero_()
-        step()
-    torch.cuda.synchronize()
-    if cq.read_status(ws) != 0:
+    wl = workloads.WORKLOADS[args.workload]()
+    if args.quant_mode is not None:
+        wl = wl.with_mode(args.quant_mode)
+    b = Bench(args, dev, wl, flush)
+    cfg, stream = b.cfg, b.stream
+    b.warm(args.warmup)
+    if cq.read_status(b.ws) != 0:
         raise RuntimeError("device status reported a bad id or mask on the bench workload")
-    rows = int(cq.assist_views(cfg, out.assist_info)[2][-1].item())
-    tokens = wl.tokens
-    if wl.mask is not None:
-        tokens = int((wl.mask.reshape(cfg.ep_world_size, cfg.max_bs, -1).max(axis=2) > 0).sum())
-    smooth_bytes = int(sm.numel() * 4) if sm is not None else 0
-    special_tokens = special_token_count(wl)
-
-    # The launches of a step are captured into CUDA graphs (the whole step, and
-    # each kernel alone for the breakdown), so host-side enqueue time never
-    # shows up as device idle time inside the timed events.
-    use_graph = not args.no_graph
-    if use_graph:
-        side = torch.cuda.Stream(dev)
-        side.wait_stream(stream)
-        graphs = {}
-        with torch.cuda.stream(side):
-            for name, fn in (
-                    ("step", step),
-                    ("route", lambda: cq.dispatch_route(cfg, ids, mask, bpr, workspace=ws,
-                                                        out=out)),
-                    ("permute", lambda: cq.dispatch_permute(cfg, x, ids, sm, w, mask, bpr,
-                                                            workspace=ws, out=out)),
-                    ("combine", lambda: combine_call(out.assist_info, out.ep_recv_count, w, x,
-                                                     y))):
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=side):
-                    fn()
-                graphs[name] = g
-        stream.wait_stream(side)
-        torch.cuda.synchronize()
-        run_step = graphs["step"].replay
-        parts = [graphs["route"].replay, graphs["permute"].replay, graphs["combine"].replay]
-    else:
-        run_step = step
-        parts = [lambda: cq.dispatch_route(cfg, ids, mask, bpr, workspace=ws, out=out),
-                 lambda: cq.dispatch_permute(cfg, x, ids, sm, w, mask, bpr, workspace=ws,
-                                             out=out),
-                 lambda: combine_call(out.assist_info, out.ep_recv_count, w, x, y)]
+    rows, tokens, smooth_bytes, special_tokens = b.counts()
 
     # Per-kernel breakdown: events between the kernels.
     n_bd = max(3, min(args.steps, 500))
-    evb = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_bd)]
-    barrier()
-    for k in range(n_bd):
-        flush.zero_()
-        for j, part in enumerate(parts):
-            evb[k][j].record(stream)
-            part()
-        evb[k][3].record(stream)
-    barrier()
-    t_route = [e[0].elapsed_time(e[1]) for e in evb]
-    t_perm = [e[1].elapsed_time(e[2]) for e in evb]
-    t_comb = [e[2].elapsed_time(e[3]) for e in evb]
+    t_route, t_perm, t_comb = b.breakdown(n_bd, barrier)
 
     # The timed region: K steps, events only at step boundaries.
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     clocks = ClockSampler(local, enabled=not args.no_clocks)
-    barrier()
-    clocks.start()
-    t_wall = time.perf_counter()
-    for k in range(args.steps):
-        flush.zero_()  # L2 flush between steps, outside the timed events
-        ev[k][0].record(stream)
-        run_step()
-        ev[k][1].record(stream)
-    barrier()
-    t_wall = time.perf_counter() - t_wall
+    t_step = b.timed(args.steps, barrier, clocks)
+    t_wall = b.t_wall
     clk = clocks.stop()
-    t_step = [e[0].elapsed_time(e[1]) for e in ev]
     value, total_ms = job_throughput(sum(t_step), tokens, args.steps, dist, dev)
     ms_per_step = total_ms / args.steps
 
@@ -612,33 +740,32 @@ def run_cq(args):
         # events keep each set's reuse ordered, so copies of neighbouring
         # steps overlap the compute of this one.
         s_up, s_down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        sets = [dict(x=torch.empty_like(x), ids=torch.empty_like(ids), w=torch.empty_like(w),
-                     y=torch.empty_like(y),
-                     hy=torch.empty(y.shape, dtype=torch.bfloat16).pin_memory(),
+        sets = [dict(x=torch.empty_like(b.x), ids=torch.empty_like(b.ids),
+                     w=torch.empty_like(b.w), y=torch.empty_like(b.y),
+                     hy=torch.empty(b.y.shape, dtype=torch.bfloat16).pin_memory(),
                      up=torch.cuda.Event(), done=torch.cuda.Event(), down=torch.cuda.Event())
                 for _ in range(args.e2e_sets)]
-        for b in sets:
-            b["done"].record(stream)
-            b["down"].record(stream)
+        for s in sets:
+            s["done"].record(stream)
+            s["down"].record(stream)
 
         def e2e_step(k):
-            b = sets[k % len(sets)]
+            s = sets[k % len(sets)]
             with torch.cuda.stream(s_up):
-                s_up.wait_event(b["done"])  # the set's inputs are free once its last compute ended
-                b["x"].copy_(hx, non_blocking=True)
-                b["ids"].copy_(hids, non_blocking=True)
-                b["w"].copy_(hw, non_blocking=True)
-                b["up"].record(s_up)
-            stream.wait_event(b["up"])
-            stream.wait_event(b["down"])  # y of this set has been read back
-            o = cq.dispatch(cfg, b["x"], b["ids"], smooth_scales=sm, x_active_mask=mask,
-                            bs_per_rank=bpr, expert_scales=b["w"], workspace=ws, out=out)
-            combine_call(o.assist_info, o.ep_recv_count, b["w"], b["x"], b["y"])
-            b["done"].record(stream)
+                s_up.wait_event(s["done"])  # the set's inputs are free once its last compute ended
+                s["x"].copy_(hx, non_blocking=True)
+                s["ids"].copy_(hids, non_blocking=True)
+                s["w"].copy_(hw, non_blocking=True)
+                s["up"].record(s_up)
+            stream.wait_event(s["up"])
+            stream.wait_event(s["down"])  # y of this set has been read back
+            o = b.dispatch(s["x"], s["ids"], s["w"])
+            b.combine(o.assist_info, o.ep_recv_count, s["w"], s["x"], s["y"])
+            s["done"].record(stream)
             with torch.cuda.stream(s_down):
-                s_down.wait_event(b["done"])
-                b["hy"].copy_(b["y"], non_blocking=True)
-                b["down"].record(s_down)
+                s_down.wait_event(s["done"])
+                s["hy"].copy_(s["y"], non_blocking=True)
+                s["down"].record(s_down)
 
         for k in range(3):
             e2e_step(k)
@@ -676,7 +803,7 @@ def run_cq(args):
         for _ in range(n_q):
             flush.zero_()
             eq0.record(stream)
-            cq.combine_quant(cfg, ffn, out.assist_info, ffn_q, ffn_s)
+            cq.combine_quant(cfg, b.ffn, b.out.assist_info, b.ffn_q, b.ffn_s)
             eq1.record(stream)
             torch.cuda.synchronize()
             t_q.append(eq0.elapsed_time(eq1))
@@ -693,47 +820,63 @@ def run_cq(args):
             "unit": "GB/s", "frac": kernels[dom]["frac"], "traffic": traffic,
             "peak_source": f"hbm_gbs of {peak_kind}"}
 
+    side = None
+    if world == 1 and args.per_workload and args.workload == "dsv3" \
+            and args.quant_mode is None and args.combine == "bf16":
+        del b
+        torch.cuda.empty_cache()
+        side = side_figures(args, dev, flush, barrier, peak)
+
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         v, desc, cores = oracle_sample(wl, args.cpu_seconds)
-        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc,
+               "cpu_model": cpu_model(), "host_cores": os.cpu_count()}
         if args.cpu_all_cores:
             va, na = oracle_all_cores(args.workload, args.quant_mode, args.cpu_seconds)
             cpu["all_cores"] = {"value": va, "unit": UNIT, "cores": na,
                                 "sample": f"the same per-token work on {na} spawned processes, "
                                           "interleaved tokens, each for the same time budget"}
 
-    emit({"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-          "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-          "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-          "config": {"workload": workload_desc(wl), "tokens_per_step": tokens,
-                     "rows_per_step": rows,
-                     "io": "bf16 tokens in; dispatch rows " + {
-                         0: "bf16", 1: "int8 (static)", 2: "int8 + f32 per-row scale",
-                         3: "fp8 + f32 per-128 scales", 4: "fp8 + e8m0 per-32 scales",
-                         5: "fp8 + e8m0 per-32 scales"}[cfg.quant_mode]
-                     + "; combine from " + ("int8 expert outputs + f32 per-8 scales"
-                                            if args.combine == "int8" else "bf16 expert outputs")
-                     + "; bf16 out",
-                     "l2": ("NOT flushed between steps (--flush none: hot-L2 figures, "
-                            "not a valid headline number)") if args.flush == "none" else
-                           "flushed between steps: 256 MiB write" + (
-                               " then 256 MiB read (no dirty lines left)"
-                               if args.flush == "write+read" else ""),
-                     "parallelism": f"{world} independent replica(s), logical ranks on-device",
-                     "launch": "CUDA graph replay of the step's three libcq launches"
-                               if use_graph else "direct launches"},
-          "per_call_us": {"dispatch": 1e3 * (means["route"] + means["permute"]),
-                          "combine": 1e3 * means["combine"],
-                          "step_pipelined": 1e3 * ms_per_step,
-                          "note": "per-kernel figures come from a separate loop of "
-                                  f"{n_bd} steps with events between the kernels"},
-          "kernels": kernels, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-          "gpu_launches": kernels_per_step(cfg, sm is not None) * args.steps, "clocks": clk,
-          "wall_s": t_wall})
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": workload_desc(wl), "tokens_per_step": tokens,
+                       "rows_per_step": rows,
+                       "io": "bf16 tokens in; dispatch rows " + {
+                           0: "bf16", 1: "int8 (static)", 2: "int8 + f32 per-row scale",
+                           3: "fp8 + f32 per-128 scales", 4: "fp8 + e8m0 per-32 scales",
+                           5: "fp8 + e8m0 per-32 scales"}[cfg.quant_mode]
+                       + "; combine from " + ("int8 expert outputs + f32 per-8 scales"
+                                              if args.combine == "int8"
+                                              else "bf16 expert outputs")
+                       + "; bf16 out",
+                       "l2": ("NOT flushed between steps (--flush none: hot-L2 figures, "
+                              "not a valid headline number)") if args.flush == "none" else
+                             "flushed between steps: 256 MiB write" + (
+                                 " then 256 MiB read (no dirty lines left)"
+                                 if args.flush == "write+read" else ""),
+                       "parallelism": f"{world} independent replica(s), logical ranks on-device",
+                       "launch": "CUDA graph replay of the step's three libcq launches"
+                                 if b_use_graph(args) else "direct launches"},
+            "per_call_us": {"dispatch": 1e3 * (means["route"] + means["permute"]),
+                            "combine": 1e3 * means["combine"],
+                            "step_pipelined": 1e3 * ms_per_step,
+                            "note": "per-kernel figures come from a separate loop of "
+                                    f"{n_bd} steps with events between the kernels"},
+            "kernels": kernels, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": kernels_per_step(cfg, smooth_bytes > 0) * args.steps,
+            "clocks": clk, "wall_s": t_wall}
+    if side is not None:
+        line["per_workload"] = side
+    emit(line)
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def b_use_graph(args) -> bool:
+    return not args.no_graph
 
 
 def main(argv=None):

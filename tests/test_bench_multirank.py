@@ -89,3 +89,11 @@ def test_reference_arm_json_line(capsys):
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_cpu_model_is_reported():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    m = bench.cpu_model()
+    assert isinstance(m, str) and m and m != "unknown"
