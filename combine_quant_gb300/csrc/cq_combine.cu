@@ -245,7 +245,7 @@ constexpr int kRingMax = 16;
 // that workspace's status word instead.
 __device__ uint32_t g_combine_status;
 
-constexpr int kUnitsPerThread = 4;  // 8-element units per consumer thread
+constexpr int kUnitsPerThread = 2;  // 8-element units per consumer thread
 
 // Slot k's inverse-map code `code`, with the consistency guard of
 // combine_kernel (a row outside the buffer, a const index outside [0, Q), or
@@ -260,12 +260,27 @@ __device__ __forceinline__ int guard_code(const Dims& d, int code, int k) {
 
 // Lane k's raw slot code of token tok (CQ_INV_NONE past NS or past the last
 // token): loaded one token ahead, guarded when used.
-__device__ __forceinline__ int raw_code(const CombineArgs& a, int64_t tok, int64_t n_tok, int k) {
-  return (tok < n_tok && k < a.d.NS) ? __ldg(a.inv + tok * a.d.NS + k) : CQ_INV_NONE;
+__device__ __forceinline__ int raw_code(const CombineArgs& a, int tok, int n_tok, int k) {
+  return (tok < n_tok && k < a.d.NS) ? __ldg(a.inv + (int64_t)tok * a.d.NS + k) : CQ_INV_NONE;
 }
+
+// Position in a ring of nslots slots: the slot and the parity of the lap
+// (the mbarrier phase a wait on that slot names). Advanced by one per
+// streamed row, with no division.
+struct RingPos {
+  int slot = 0;
+  uint32_t lap = 0;
+  __device__ __forceinline__ void next(int nslots) {
+    if (++slot == nslots) {
+      slot = 0;
+      lap ^= 1u;
+    }
+  }
+};
 
 // Work item = (token, column chunk of `cw` elements); item i is token
 // i / nchunk, chunk i % nchunk. CTA b takes items b, b + gridDim.x, ...
+// (fewer than 2^31 items: W * BS * nchunk <= 768 * 512 * 2).
 template <class T, bool OUT_F32>
 __global__ void __launch_bounds__(288) combine_staged_kernel(CombineArgs a, int nslots, int nchunk,
                                                             int cw) {
@@ -281,8 +296,10 @@ __global__ void __launch_bounds__(288) combine_staged_kernel(CombineArgs a, int 
   const int ncons = (int)blockDim.x - 32;  // consumer threads
   const int nwc = ncons >> 5;              // consumer warps
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t n_tok = (int64_t)d.W * d.BS;
-  const int64_t n_items = n_tok * nchunk;
+  const int n_tok = d.W * d.BS;
+  const int n_items = n_tok * nchunk;
+  const unsigned uchunk = (unsigned)nchunk;
+  auto token_of = [&](int it) { return (int)((unsigned)it / uchunk); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < nslots; ++s) {
@@ -297,30 +314,31 @@ __global__ void __launch_bounds__(288) combine_staged_kernel(CombineArgs a, int 
 
   if (warp == nwc) {
     // Producer warp: lane 0 issues; the warp reads each item's slot codes.
-    int64_t issued = 0;
+    int issued = 0;
+    RingPos pos;
     bool ok = true;
-    int next = raw_code(a, blockIdx.x / nchunk, n_tok, lane);
-    for (int64_t it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
-      const int64_t tok = it / nchunk;
-      const int c0 = (int)(it - tok * nchunk) * cw;
+    int next = raw_code(a, token_of(blockIdx.x), n_tok, lane);
+    for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+      const int tok = token_of(it);
+      const int c0 = (it - tok * nchunk) * cw;
       const uint32_t bytes = 2u * (uint32_t)min(cw, H - c0);
       const int code = guard_code(d, next, lane);
-      next = raw_code(a, (it + gridDim.x) / nchunk, n_tok, lane);
+      next = raw_code(a, token_of(it + gridDim.x), n_tok, lane);
       for (int k = 0; k < d.NS; ++k) {
         const int ck = __shfl_sync(0xffffffffu, code, k);
         if (ck < 0) continue;
         if (lane == 0) {
-          const int s = (int)(issued % nslots);
-          if (issued >= nslots &&
-              !mbar_wait(&s_empty[s], (uint32_t)((issued / nslots) - 1) & 1u)) {
+          // the slot's previous row (one lap earlier) must have been consumed
+          if (issued >= nslots && !mbar_wait(&s_empty[pos.slot], pos.lap ^ 1u)) {
             s_fail = 1;
             atomicOr(st_word, (uint32_t)CQ_ST_TIMEOUT);
           }
           if (!s_fail) {
-            mbar_arrive_expect_tx(&s_full[s], bytes);
-            bulk_load(s_ring + (size_t)s * slot_bytes, a.ffn + (int64_t)ck * H + c0, bytes,
-                      &s_full[s]);
+            mbar_arrive_expect_tx(&s_full[pos.slot], bytes);
+            bulk_load(s_ring + (size_t)pos.slot * slot_bytes, a.ffn + (int64_t)ck * H + c0,
+                      bytes, &s_full[pos.slot]);
             ++issued;
+            pos.next(nslots);
           }
         }
         ok = __shfl_sync(0xffffffffu, s_fail, 0) == 0;
@@ -330,44 +348,45 @@ __global__ void __launch_bounds__(288) combine_staged_kernel(CombineArgs a, int 
     // Wait (bounded) for the last loads to land before this warp ends, so
     // that no copy is in flight once the consumers are gone.
     if (lane == 0)
-      for (int64_t i = issued > nslots ? issued - nslots : 0; i < issued; ++i)
+      for (int i = issued > nslots ? issued - nslots : 0; i < issued; ++i)
         mbar_wait(&s_full[i % nslots], (uint32_t)(i / nslots) & 1u);
     return;
   }
 
   // Consumer warps.
-  int64_t consumed = 0;
-  auto raw_w = [&](int64_t t) {
-    return (t < n_tok && lane < d.K) ? __ldg(a.expert_scales + t * d.K + lane) : 1.f;
+  RingPos pos;
+  auto raw_w = [&](int t) {
+    return (t < n_tok && lane < d.K) ? __ldg(a.expert_scales + (int64_t)t * d.K + lane) : 1.f;
   };
-  int next = raw_code(a, blockIdx.x / nchunk, n_tok, lane);
-  float next_w = raw_w(blockIdx.x / nchunk);
-  for (int64_t it = blockIdx.x; it < n_items; it += gridDim.x) {
-    const int64_t tok = it / nchunk;
-    const int c0 = (int)(it - tok * nchunk) * cw;
+  int next = raw_code(a, token_of(blockIdx.x), n_tok, lane);
+  float next_w = raw_w(token_of(blockIdx.x));
+  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+    const int tok = token_of(it);
+    const int c0 = (it - tok * nchunk) * cw;
     const int cu = min(cw, H - c0) >> 3;  // 8-element units in this chunk
     const int code = guard_code(d, next, lane);
     const float wl = next_w;
-    next = raw_code(a, (it + gridDim.x) / nchunk, n_tok, lane);
-    next_w = raw_w((it + gridDim.x) / nchunk);
+    const int tok_next = token_of(it + gridDim.x);
+    next = raw_code(a, tok_next, n_tok, lane);
+    next_w = raw_w(tok_next);
     float acc[kUnitsPerThread][8];
 #pragma unroll
     for (int i = 0; i < kUnitsPerThread; ++i)
 #pragma unroll
       for (int t = 0; t < 8; ++t) acc[i][t] = 0.f;
-    const uint16_t* xrow = a.ori_x ? a.ori_x + tok * H + c0 : nullptr;
+    const int64_t tok_h = (int64_t)tok * H;
+    const uint16_t* xrow = a.ori_x ? a.ori_x + tok_h + c0 : nullptr;
     for (int k = 0; k < d.NS; ++k) {
       const int ck = __shfl_sync(0xffffffffu, code, k);
       const float w = __shfl_sync(0xffffffffu, wl, k);
       if (ck >= 0) {
-        const int s = (int)(consumed % nslots);
         // The whole warp leaves together if any lane gave up.
-        if (!__all_sync(0xffffffffu, mbar_wait(&s_full[s], (uint32_t)(consumed / nslots) & 1u))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&s_full[pos.slot], pos.lap))) {
           s_fail = 1;
           if (lane == 0) atomicOr(st_word, (uint32_t)CQ_ST_TIMEOUT);
           return;
         }
-        const uint8_t* rowp = s_ring + (size_t)s * slot_bytes;
+        const uint8_t* rowp = s_ring + (size_t)pos.slot * slot_bytes;
 #pragma unroll
         for (int i = 0; i < kUnitsPerThread; ++i) {
           const int u = threadIdx.x + i * ncons;
@@ -381,14 +400,14 @@ __global__ void __launch_bounds__(288) combine_staged_kernel(CombineArgs a, int 
             }
           }
         }
-        release_slot(&s_empty[s]);
-        ++consumed;
+        release_slot(&s_empty[pos.slot]);
+        pos.next(nslots);
       } else if (ck == CQ_INV_COPY || ck <= CQ_INV_CONST_BASE) {
 #pragma unroll
         for (int i = 0; i < kUnitsPerThread; ++i) {
           const int u = threadIdx.x + i * ncons;
           if (u < cu) {
-            const int64_t col = 8 * (int64_t)u;
+            const int col = 8 * u;
             if (ck == CQ_INV_COPY) {
               float f[8];
               unpack8<T>(ld_nc_v4(xrow + col), f);  // Moe(ori_x) = ori_x
@@ -406,7 +425,7 @@ __global__ void __launch_bounds__(288) combine_staged_kernel(CombineArgs a, int 
 #pragma unroll
     for (int i = 0; i < kUnitsPerThread; ++i) {
       const int u = threadIdx.x + i * ncons;
-      if (u < cu) store8<T, OUT_F32>(a.y, tok * H + c0 + 8 * (int64_t)u, acc[i]);
+      if (u < cu) store8<T, OUT_F32>(a.y, tok_h + c0 + 8 * u, acc[i]);
     }
   }
 }
@@ -511,7 +530,7 @@ __global__ void __launch_bounds__(kQThreads) combine_quant_kernel(CombineArgs a)
 // kRingBytes (several CTAs per SM), 2..kRingMax chunks; one CTA per item
 // (kPersistent false) or one wave of CTAs looping over the items.
 constexpr int kChunkCols = 4096;
-constexpr size_t kRingBytes = 29u << 10;
+constexpr size_t kRingBytes = 36u << 10;
 constexpr bool kPersistent = true;
 
 template <class T, bool OUT_F32>
