@@ -43,13 +43,13 @@ L2_FLUSH_BYTES = 256 << 20
 # the SHA-256 of the kernel's source file when it was captured; reported only
 # while the source is unchanged.
 NCU_TRAFFIC = {
-    # profiles/dsv3_kernels_ncu_full.md: read 470.069504 MB + write 48.131328 MB
-    "combine": {"bytes_per_launch": 518200832,
-                "src_sha": "4072fd883502df6feacce830337714eee1f1ab9af5698034ef08736446be89fd"},
-    # read 59.223808 MB + write 175.246848 MB (the permute sources are unchanged
-    # since that capture; a later one read 59.245056 + 175.486976 MB)
-    "permute": {"bytes_per_launch": 234470656,
-                "src_sha": "1761eba0c3696c5285ad7e486c7126b4814c1d1bc8e03bae17c379c740e93269"},
+    # profiles/dsv3_step_launch_list.md: read 470.059593 MB + write 45.949696 MB
+    # per launch (mean of 7 launches of one bench run)
+    "combine": {"bytes_per_launch": 516009289,
+                "src_sha": "c285a3f3ba8db67883c0b717611a745e05cbdd1137c6a7489f7e2785d88f63bd"},
+    # the same capture: read 59.226331 MB + write 172.117687 MB
+    "permute": {"bytes_per_launch": 231344018,
+                "src_sha": "83cb0f35b7a90d4e0ed7254c6d59f39bf945d2373348c2fb56cec1990825c1ca"},
 }
 
 
