@@ -203,6 +203,28 @@ def test_host_errors_before_any_device_work(lib):
 
 
 @needs_no_gpu
+def test_combine_ws_checks_its_workspace(lib):
+    """cq_combine_ws takes the dispatch workspace for its status word: a
+    missing, misaligned or too small one is refused on the host."""
+    cfg = make_config(ep_world_size=4, moe_expert_num=8, max_bs=8, topk=2, hidden=1024,
+                      quant_mode=2)
+    hb = _HostBufs(cfg)
+    need = lib.cq_workspace_size(_c(cfg))
+    args = hb.combine_args()
+    y = hb["y"]
+    assert lib.cq_combine_ws(_c(cfg), *args, 0, y, None, need, None) == _lib.CQ_ERR_WORKSPACE
+    assert lib.cq_combine_ws(_c(cfg), *args, 0, y, hb["ws"], need - 1, None) == \
+        _lib.CQ_ERR_WORKSPACE
+    misaligned = ctypes.c_void_p(hb["ws"].value + 16)
+    assert lib.cq_combine_ws(_c(cfg), *args, 0, y, misaligned, need, None) == \
+        _lib.CQ_ERR_WORKSPACE
+    # argument rules of cq_combine come first
+    assert lib.cq_combine_ws(_c(dict(cfg, topk=0)), *args, 0, y, hb["ws"], need, None) == \
+        _lib.CQ_ERR_ARG
+    assert lib.cq_combine_ws(_c(cfg), *args, 2, y, hb["ws"], need, None) == _lib.CQ_ERR_ARG
+
+
+@needs_no_gpu
 @pytest.mark.parametrize("which", ["x", "expand_x", "assist", "dyn", "smooth"])
 def test_permute_half_errors_before_the_route_half(lib, which):
     """An argument only the permute half uses (a misaligned token row, code
