@@ -15,8 +15,11 @@
 // received-count matrix, transposed to (local expert, source) order and summed
 // row-major (§2.4.1), which is ep_recv_count[d]; it also writes
 // expert_token_nums[d] and each (slot, source) block's first row counted from
-// the start of rank d. The last of these CTAs (one atomic counter, no spin)
-// prefix-sums the W rank totals into the rank bases.
+// the start of rank d. The counts table is slot-major and the slots of a rank
+// are contiguous, so rank d's first row is the sum of the table's entries
+// before its first slot: for tables of up to kDirectBase entries every CTA
+// sums them itself (one parallel reduction); for larger ones the last CTA
+// (one atomic counter, no spin) prefix-sums the W rank totals.
 // Page tags ([DV3], [DSN], [LLD], [PERF]) name the source pages listed at the
 // top of include/cq.h.
 #include "cq_internal.cuh"
@@ -37,6 +40,9 @@ constexpr int kSmallBS = 32;
 constexpr int kMaxSteps = 16;
 constexpr int kOffThreads = 256;
 constexpr int kOffWarps = kOffThreads / 32;
+// Largest counts table (G x W entries) whose prefix each offsets CTA sums
+// itself instead of waiting for the last CTA's scan of the rank totals.
+constexpr int64_t kDirectBase = 1024;
 constexpr unsigned kFull = 0xffffffffu;
 
 __device__ __forceinline__ unsigned lanemask_lt() {
@@ -256,6 +262,16 @@ __global__ void __launch_bounds__(kOffThreads) offsets_kernel(RouteArgs a) {
   int* loc = a.ws.local_off + g0w;
   int* erc = a.ep_recv_count + (int64_t)rank * d.W * d.L;
 
+  // Small tables: this rank's first row is the sum of the counts of all
+  // slots before its first one (ranks are laid out slot-major, shared ranks
+  // first); those loads go out together with this rank's own.
+  const bool direct = (int64_t)d.G * d.W <= kDirectBase;
+  int part = 0;
+  if (direct) {
+    const int n_before = gslot(d, rank, 0) * d.W;
+    for (int t = threadIdx.x; t < n_before; t += kOffThreads) part += __ldcg(a.ws.counts_t + t);
+  }
+
   // Each thread takes <= 8 contiguous entries; one block scan of their sums.
   constexpr int kPer = 8;
   const int per = (n + kOffThreads - 1) / kOffThreads;
@@ -286,6 +302,20 @@ __global__ void __launch_bounds__(kOffThreads) offsets_kernel(RouteArgs a) {
       e = d.etn_type == 1 ? end - loc[le * d.W] : end;  // [DV3] 1: counts, 0: cumsum
     }
     a.expert_token_nums[(int64_t)rank * d.L + le] = e;
+  }
+  if (direct) {
+    int base = 0;
+    block_excl_scan<kOffWarps>(part, s_buf, &base);
+    if (threadIdx.x == 0) {
+      a.ws.rank_base[rank] = base;
+      a.rank_row_base[rank] = base;
+      if (rank == d.W - 1) {
+        a.ws.rank_base[d.W] = base + tot;
+        a.rank_row_base[d.W] = base + tot;
+        *a.ws.total = base + tot;
+      }
+    }
+    return;
   }
   // Last CTA: exclusive prefix of the W rank totals gives each rank's first
   // row. Thread 0 publishes this rank's total with a release increment of the
