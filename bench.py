@@ -22,6 +22,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import inspect
 import json
 import os
 import statistics
@@ -67,6 +68,9 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["cq", "reference"], default="cq")
     ap.add_argument("--workload", default="dsv3")
+    ap.add_argument("--bs", type=_positive_int, default=None,
+                    help="override the per-rank batch of dsv3, mxfp8, special or skew (a "
+                         "reduced case, e.g. for a profiler capture)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-all-cores", action=argparse.BooleanOptionalAction, default=True,
@@ -89,6 +93,26 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="host time budget of the oracle baseline")
     return ap.parse_args(argv)
+
+
+def named_workload(name: str, bs=None, quant_mode=None):
+    """The named workload, with the per-rank batch and quant mode overrides."""
+    from combine_quant_gb300 import workloads
+
+    gen = workloads.WORKLOADS[name]
+    if bs is not None:
+        if "BS" not in inspect.signature(gen).parameters:
+            raise SystemExit(f"--bs: workload {name} has a fixed batch")
+        wl = gen(BS=bs)
+    else:
+        wl = gen()
+    if quant_mode is not None:
+        wl = wl.with_mode(quant_mode)
+    return wl
+
+
+def make_workload(args):
+    return named_workload(args.workload, args.bs, args.quant_mode)
 
 
 def workload_desc(wl) -> str:
@@ -321,14 +345,10 @@ def oracle_sample(wl, budget_s: float, max_tokens: int | None = None):
     return 1.0 / per_tok, desc, 1
 
 
-def _oracle_worker(name, quant_mode, wi, n, budget_s, ready, start, results):
+def _oracle_worker(name, bs, quant_mode, wi, n, budget_s, ready, start, results):
     """One process of the all-cores oracle baseline: tokens wi, wi + n, ..."""
     sys.path.insert(0, ROOT)
-    from combine_quant_gb300 import workloads
-
-    wl = workloads.WORKLOADS[name]()
-    if quant_mode is not None:
-        wl = wl.with_mode(quant_mode)
+    wl = named_workload(name, bs, quant_mode)
     prep = _oracle_prepare(wl)
     W, BS = wl.cfg["ep_world_size"], wl.cfg["max_bs"]
     order = [(r, i) for r in range(W) for i in range(BS)][wi::n]
@@ -338,7 +358,7 @@ def _oracle_worker(name, quant_mode, wi, n, budget_s, ready, start, results):
     results.put((done, secs, prep[3]))
 
 
-def oracle_all_cores(name: str, quant_mode, budget_s: float, n: int | None = None):
+def oracle_all_cores(name: str, quant_mode, budget_s: float, n: int | None = None, bs=None):
     """The same oracle work on every host core: n spawned processes (started
     only after all have built their inputs) take interleaved tokens. Returns
     (tokens/s, cores): all tokens done over the slowest process's time, plus
@@ -349,7 +369,7 @@ def oracle_all_cores(name: str, quant_mode, budget_s: float, n: int | None = Non
     ctx = mp.get_context("spawn")
     ready, results, start = ctx.Queue(), ctx.Queue(), ctx.Event()
     procs = [ctx.Process(target=_oracle_worker,
-                         args=(name, quant_mode, wi, n, budget_s, ready, start, results))
+                         args=(name, bs, quant_mode, wi, n, budget_s, ready, start, results))
              for wi in range(n)]
     for p in procs:
         p.start()
@@ -362,8 +382,7 @@ def oracle_all_cores(name: str, quant_mode, budget_s: float, n: int | None = Non
     done = sum(o[0] for o in out)
     secs = max(o[1] for o in out)
     t_route = out[0][2]
-    from combine_quant_gb300 import workloads
-    c = workloads.WORKLOADS[name]().cfg
+    c = named_workload(name, bs).cfg
     per_tok = secs / done + t_route / (c["ep_world_size"] * c["max_bs"])
     return 1.0 / per_tok, n
 
@@ -402,9 +421,7 @@ def run_reference(args):
         return 0  # the oracle arm runs once, on rank 0
     from combine_quant_gb300 import workloads
 
-    wl = workloads.WORKLOADS[args.workload]()
-    if args.quant_mode is not None:
-        wl = wl.with_mode(args.quant_mode)
+    wl = make_workload(args)
     W, BS = wl.cfg["ep_world_size"], wl.cfg["max_bs"]
     # Each step is a bounded sample: enough tokens that K + W steps take about
     # a minute of host time in total.
@@ -705,9 +722,7 @@ def run_cq(args):
                 flush_r.amax()
 
     flush = _Flush()
-    wl = workloads.WORKLOADS[args.workload]()
-    if args.quant_mode is not None:
-        wl = wl.with_mode(args.quant_mode)
+    wl = make_workload(args)
     b = Bench(args, dev, wl, flush)
     cfg, stream = b.cfg, b.stream
     b.warm(args.warmup)
@@ -814,14 +829,15 @@ def run_cq(args):
                    "frac": ab[k] / (means[k] * 1e-3) / 1e9 / peak} for k in means}
     dom = max(("permute", "combine"), key=lambda k: means[k])
     traffic = None
-    if args.workload == "dsv3" and args.quant_mode in (None, 2) and args.combine == "bf16":
+    if args.workload == "dsv3" and args.bs is None and args.quant_mode in (None, 2) \
+            and args.combine == "bf16":
         traffic = ncu_traffic(dom)  # the captured configuration
     roof = {"kernel": dom, "bound": "hbm", "achieved": kernels[dom]["gbs"], "peak": peak,
             "unit": "GB/s", "frac": kernels[dom]["frac"], "traffic": traffic,
             "peak_source": f"hbm_gbs of {peak_kind}"}
 
     side = None
-    if world == 1 and args.per_workload and args.workload == "dsv3" \
+    if world == 1 and args.per_workload and args.workload == "dsv3" and args.bs is None \
             and args.quant_mode is None and args.combine == "bf16":
         del b
         torch.cuda.empty_cache()
@@ -833,7 +849,8 @@ def run_cq(args):
         cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc,
                "cpu_model": cpu_model(), "host_cores": os.cpu_count()}
         if args.cpu_all_cores:
-            va, na = oracle_all_cores(args.workload, args.quant_mode, args.cpu_seconds)
+            va, na = oracle_all_cores(args.workload, args.quant_mode, args.cpu_seconds,
+                                      bs=args.bs)
             cpu["all_cores"] = {"value": va, "unit": UNIT, "cores": na,
                                 "sample": f"the same per-token work on {na} spawned processes, "
                                           "interleaved tokens, each for the same time budget"}

@@ -97,3 +97,13 @@ def test_cpu_model_is_reported():
 
     m = bench.cpu_model()
     assert isinstance(m, str) and m and m != "unknown"
+
+
+def test_batch_override_reduces_the_workload():
+    import bench
+
+    wl = bench.make_workload(bench.parse_args(["--bs", "16", "--quant-mode", "0"]))
+    assert wl.cfg["max_bs"] == 16 and wl.cfg["quant_mode"] == 0
+    assert wl.x.shape[:2] == (32, 16)
+    with pytest.raises(SystemExit):
+        bench.make_workload(bench.parse_args(["--workload", "perf8", "--bs", "16"]))
