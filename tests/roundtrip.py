@@ -11,8 +11,9 @@ expert_scales-weighted sum of its token row over the routed slots, the shared
 experts' rows unweighted, x for a copy expert and a1*x + a2*v for a const
 expert ("MoeDistributeDispatch和MoeDistributeCombine算子设计介绍" §3.4 and
 "low_latency_dispatch" 特殊专家场景), up to each row's quantisation step and
-the rounding of the accumulation. closed_form() states that sum and its error
-bound from the inputs alone; run_oracle() runs the oracle's own round trip.
+the rounding of the accumulation. closed_form() states that sum from the inputs,
+with an error bound from each row's quantisation step; run_oracle() runs the
+oracle's own round trip.
 """
 from __future__ import annotations
 
