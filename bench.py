@@ -3,9 +3,9 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl cq|reference]
 
-A step is one pass of the whole path over one batch: the routing scan
-(cq_dispatch_route), the fused permute-quantise (cq_dispatch_permute) and the
-combine (cq_combine), on the DeepSeek-V3-shaped workload (32 logical EP ranks,
+A step is one pass of the whole path over one batch: cq_dispatch (the routing
+scan and the fused permute-quantise) and cq_combine, on the DeepSeek-V3-shaped
+workload (32 logical EP ranks,
 256 experts, 8 per rank, top-8, 128 tokens per rank, hidden 7168, per-token
 dynamic int8). The expert FFN between dispatch and combine is outside the path;
 combine consumes a seeded stand-in for its output.
@@ -539,21 +539,13 @@ class Bench:
                                  **self.consts)
         return cq.combine(self.cfg, self.ffn, a[0], w, a[1], ori_x=x, y=y, **self.consts)
 
-    def step(self, evs=None):
-        """One pass of the path. With 4 events, each kernel is bracketed (the
-        events between kernels also stop the next kernel from starting early);
-        with 2, only the step's start and end are recorded."""
-        if evs:
-            evs[0].record(self.stream)
-        self.route()
-        if evs and len(evs) == 4:
-            evs[1].record(self.stream)
-        self.permute()
-        if evs and len(evs) == 4:
-            evs[2].record(self.stream)
+    def step(self):
+        """One pass of the path: cq_dispatch, then cq_combine. (The breakdown
+        times the two dispatch halves, cq_dispatch_route and
+        cq_dispatch_permute, apart; a small batch's cq_dispatch runs both in
+        one kernel.)"""
+        self.dispatch()
         self.combine()
-        if evs:
-            evs[-1].record(self.stream)
 
     def warm(self, n):
         import torch

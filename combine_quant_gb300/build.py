@@ -21,7 +21,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libcq.so")
-SOURCES = ["cq_api.cu", "cq_route.cu", "cq_permute_bf16.cu", "cq_permute_f16.cu",
+SOURCES = ["cq_api.cu", "cq_route.cu", "cq_permute_bf16.cu", "cq_permute_f16.cu", "cq_dispatch_small.cu",
            "cq_combine.cu", "cq_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -142,14 +142,11 @@ int route_impl(const cq_config* cfg, const int32_t* expert_ids, const uint8_t* m
                                                                                  : CQ_ERR_CUDA;
 }
 
-int permute_impl(const cq_config* cfg, const void* x, const int32_t* expert_ids,
-                 const float* smooth, const uint8_t* mask, const int32_t* bs_per_rank,
-                 const float* expert_scales, void* expand_x, void* dynamic_scales,
-                 int32_t* assist_info, float* expand_scales, void* workspace,
-                 size_t workspace_bytes, void* stream) {
-  const int rc = check_permute(cfg, x, expert_ids, smooth, expand_x, dynamic_scales,
-                               assist_info, workspace, workspace_bytes);
-  if (rc != CQ_OK) return rc;
+// The permute half's argument block (arguments already checked).
+cq::PermuteArgs permute_args(const cq_config* cfg, const void* x, const int32_t* expert_ids,
+                             const float* smooth, const uint8_t* mask, const int32_t* bs_per_rank,
+                             const float* expert_scales, void* expand_x, void* dynamic_scales,
+                             int32_t* assist_info, float* expand_scales, void* workspace) {
   const Dims d = dims_of(cfg);
   cq::PermuteArgs a;
   a.d = d;
@@ -168,6 +165,20 @@ int permute_impl(const cq_config* cfg, const void* x, const int32_t* expert_ids,
   const int scale_row_bytes = d.mode == 3 ? 4 * d.G3 : d.SC;
   a.scale_rows_bulk = scale_row_bytes % 16 == 0 && aligned(dynamic_scales, 16);
   a.ws = cq::carve(workspace, d);
+  return a;
+}
+
+int permute_impl(const cq_config* cfg, const void* x, const int32_t* expert_ids,
+                 const float* smooth, const uint8_t* mask, const int32_t* bs_per_rank,
+                 const float* expert_scales, void* expand_x, void* dynamic_scales,
+                 int32_t* assist_info, float* expand_scales, void* workspace,
+                 size_t workspace_bytes, void* stream) {
+  const int rc = check_permute(cfg, x, expert_ids, smooth, expand_x, dynamic_scales,
+                               assist_info, workspace, workspace_bytes);
+  if (rc != CQ_OK) return rc;
+  const cq::PermuteArgs a = permute_args(cfg, x, expert_ids, smooth, mask, bs_per_rank,
+                                         expert_scales, expand_x, dynamic_scales, assist_info,
+                                         expand_scales, workspace);
   return cq::launch_permute(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? CQ_OK
                                                                                    : CQ_ERR_CUDA;
 }
@@ -263,6 +274,17 @@ int cq_dispatch(const cq_config* cfg, const void* x, const int32_t* expert_ids,
                              dynamic_scales, assist_info, ep_recv_count, expert_token_nums,
                              workspace, workspace_bytes);
   if (rc != CQ_OK) return rc;
+  // A small batch: routing and permute in one kernel.
+  const Dims d = dims_of(cfg);
+  if (cq::dispatch_small_fits(d, smooth_scales && cfg->smooth_kind == 0)) {
+    const cq::PermuteArgs a = permute_args(cfg, x, expert_ids, smooth_scales, x_active_mask,
+                                           bs_per_rank, expert_scales, expand_x, dynamic_scales,
+                                           assist_info, expand_scales, workspace);
+    const cudaError_t e = cq::launch_dispatch_small(a, ep_recv_count, expert_token_nums,
+                                                    assist_info + cq::assist_base_off(d),
+                                                    static_cast<cudaStream_t>(stream));
+    if (e != cudaErrorNotSupported) return e == cudaSuccess ? CQ_OK : CQ_ERR_CUDA;
+  }
   rc = route_impl(cfg, expert_ids, x_active_mask, bs_per_rank, assist_info, ep_recv_count,
                   expert_token_nums, workspace, workspace_bytes, stream);
   if (rc != CQ_OK) return rc;

@@ -266,6 +266,13 @@ int dispatch_check(const cq_config* cfg, const void* x, const int32_t* expert_id
 // Launchers (each returns the cudaError_t of its launch).
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s);
 cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t s);
+// The whole dispatch of a small batch in one kernel (cq_dispatch_small.cu):
+// whether the problem qualifies, and the launch (cudaErrorNotSupported for a
+// mode it does not cover).
+bool dispatch_small_fits(const Dims& d, bool per_expert_smooth);
+cudaError_t launch_dispatch_small(const PermuteArgs& a, int32_t* ep_recv_count,
+                                  int64_t* expert_token_nums, int32_t* rank_row_base,
+                                  cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s);     // from bf16 rows
 cudaError_t launch_combine_q8(const CombineArgs& a, cudaStream_t s);  // from int8 rows
 cudaError_t launch_combine_quant(const CombineArgs& a, cudaStream_t s);
