@@ -44,13 +44,13 @@ L2_FLUSH_BYTES = 256 << 20
 # the SHA-256 of the kernel's source file when it was captured; reported only
 # while the source is unchanged.
 NCU_TRAFFIC = {
-    # profiles/dsv3_step_launch_list.md: read 470.059593 MB + write 45.949696 MB
+    # profiles/dsv3_step_launch_list.md: read 470.057216 MB + write 46.016987 MB
     # per launch (mean of 7 launches of one bench run)
-    "combine": {"bytes_per_launch": 516009289,
-                "src_sha": "c285a3f3ba8db67883c0b717611a745e05cbdd1137c6a7489f7e2785d88f63bd"},
-    # the same capture: read 59.226331 MB + write 172.117687 MB
-    "permute": {"bytes_per_launch": 231344018,
-                "src_sha": "83cb0f35b7a90d4e0ed7254c6d59f39bf945d2373348c2fb56cec1990825c1ca"},
+    "combine": {"bytes_per_launch": 516074203,
+                "src_sha": "b090933ecfdde47099116ed07ad89f5a2750ed97451a34af3d81928c84a8df70"},
+    # the same capture: read 59.230208 MB + write 172.213065 MB
+    "permute": {"bytes_per_launch": 231443273,
+                "src_sha": "8aede6438126f7eda6073859216754b2f4f8104c9130e10f548d1319bf5d840d"},
 }
 
 
