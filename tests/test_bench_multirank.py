@@ -107,3 +107,21 @@ def test_batch_override_reduces_the_workload():
     assert wl.x.shape[:2] == (32, 16)
     with pytest.raises(SystemExit):
         bench.make_workload(bench.parse_args(["--workload", "perf8", "--bs", "16"]))
+
+
+def test_kernels_per_step_follows_the_dispatch_path():
+    """The launch count the bench line claims: two kernels for a batch small
+    enough for the one-kernel dispatch, four (five with per-expert smooth
+    rows) otherwise."""
+    import bench
+    import combine_quant_gb300 as cq
+    from combine_quant_gb300 import workloads
+
+    def n(wl):
+        cfg = cq.Config.from_dict(wl.cfg)
+        return bench.kernels_per_step(cfg, wl.smooth is not None and cfg.quant_mode in (1, 2, 3))
+
+    assert n(workloads.tiny()) == 2 and n(workloads.perf_table(8)) == 2
+    assert n(workloads.dsv3()) == 4 and n(workloads.special()) == 4
+    assert n(workloads.skew()) == 5
+    assert n(workloads.mxfp8(W=4, BS=8, M=16, K=4, H=1024)) == 2
