@@ -78,6 +78,16 @@ Dims dims_of(const cq_config* c) {
   d.SC = (blocks + 1) / 2 * 2;
   d.G3 = (d.H + 127) / 128;
   d.R_max = (int64_t)d.W * d.BS * d.NS;
+  // Routing chunks: CH count CTAs per source, about kRouteCtas in all, none
+  // under kRouteMinTokens tokens, and at most 2048 (local expert, source,
+  // chunk) entries per destination rank (L * W <= 2048 holds already).
+  constexpr int kRouteCtas = 128, kRouteMinTokens = 32;
+  int ch = kRouteCtas / d.W;
+  if (ch > d.BS / kRouteMinTokens) ch = d.BS / kRouteMinTokens;
+  if (ch > 2048 / (d.L * d.W)) ch = 2048 / (d.L * d.W);
+  if (ch < 1) ch = 1;
+  d.CH = ch;
+  d.TC = (d.BS + ch - 1) / ch;
   return d;
 }
 

@@ -11,8 +11,9 @@
 // ordinal, expandIdx of §2.2.2), maps its slots to rows and quantises and
 // scatters its token row exactly as permute_kernel does. CTA 0 also writes
 // the routing outputs (ep_recv_count, expert_token_nums, rank_row_base) and
-// the workspace's counts and offsets, so the outputs and the workspace end up
-// as cq_dispatch_route + cq_dispatch_permute leave them. One launch replaces
+// the workspace's total rows, so every output ends up as cq_dispatch_route +
+// cq_dispatch_permute leave it (the routing kernels' own scratch tables in
+// the workspace are neither needed nor written). One launch replaces
 // three (count, offsets, permute) and their two grid hand-offs, which is
 // most of the latency of a batch of a few tokens per rank.
 // Page tags ([DV3], [DSN], [LLD], [PERF]) name the source pages listed at the
@@ -246,7 +247,6 @@ __global__ void __launch_bounds__(kSmallThreads)
       srow = s;
     }
     if (__any_sync(kFull, bad) && lane == 0) atomicOr(a.ws.status, (uint32_t)CQ_ST_BAD_ID);
-    if (k < NS) a.ws.eidx[tok * NS + k] = ord;
     if (row >= 0 && (int64_t)row >= d.R_max) {  // consistency guard: never write outside
       atomicOr(a.ws.status, (uint32_t)CQ_ST_INTERNAL);
       row = -1;
@@ -282,8 +282,6 @@ __global__ void __launch_bounds__(kSmallThreads)
       const int dst = g < d.S_r ? g : d.S_r + (g - d.S_r) / d.L;
       const int g0 = dst < d.S_r ? dst : d.S_r + (dst - d.S_r) * d.L;
       const int base = start[g0 * W];
-      a.ws.counts_t[e] = cnt[e];
-      a.ws.local_off[e] = start[e] - base;
       const int le = g - g0, rr = e - g * W;
       ro.ep_recv_count[(int64_t)dst * W * d.L + le * W + rr] = start[e] + cnt[e] - base;
     }

@@ -22,15 +22,18 @@ struct Dims {
   int32_t y_dtype;                // fp8 codes of modes 3-5: 0 e4m3fn, 1 e5m2
   int32_t SC;                     // mx scale columns: Align2(Ceil(H, 32))
   int32_t G3;                     // mode-3 groups per row: Ceil(H, 128)
+  int32_t CH, TC;                 // routing: each source's tokens in CH chunks of TC
   int64_t R_max;
 };
 
 // Workspace layout (byte offsets, each segment 256-byte aligned).
 //   hdr       : uint32 status, uint32 done counter, int32 total rows, pad
-//   counts_t  : int32 [G][W]  rows per (global expert slot, source rank)
-//   local_off : int32 [G][W]  first row of each (slot, source) block, counted
-//                             from the start of its destination rank
-//   eidx      : int32 [W*BS*NS] arrival ordinal of each slot, or a CQ_INV code
+//   counts_t  : int32 [G][W][CH]  rows per (global expert slot, source rank,
+//                             chunk of the source's tokens)
+//   local_off : int32 [G][W][CH]  first row of each (slot, source, chunk)
+//                             block, counted from the start of its destination rank
+//   eidx      : int32 [W*BS*NS] arrival ordinal of each slot within its
+//                             (slot, source, chunk) block, or a CQ_INV code
 //   rank_tot  : int32 [W]     rows received by each destination rank
 //   rank_base : int32 [W+1]   first global row of each destination rank
 //   row_src   : int2 [R_max]  (source token index r*BS+i, smooth-table row) of
@@ -52,8 +55,8 @@ inline size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
 
 inline size_t workspace_bytes(const Dims& d) {
   size_t b = kHdrBytes;
-  b += align256(sizeof(int32_t) * (size_t)d.G * d.W);
-  b += align256(sizeof(int32_t) * (size_t)d.G * d.W);
+  b += align256(sizeof(int32_t) * (size_t)d.G * d.W * d.CH);
+  b += align256(sizeof(int32_t) * (size_t)d.G * d.W * d.CH);
   b += align256(sizeof(int32_t) * (size_t)d.W * d.BS * d.NS);
   b += align256(sizeof(int32_t) * (size_t)d.W);
   b += align256(sizeof(int32_t) * (size_t)(d.W + 1));
@@ -69,9 +72,9 @@ inline Workspace carve(void* base, const Dims& d) {
   w.total = reinterpret_cast<int32_t*>(p + 8);
   p += kHdrBytes;
   w.counts_t = reinterpret_cast<int32_t*>(p);
-  p += align256(sizeof(int32_t) * (size_t)d.G * d.W);
+  p += align256(sizeof(int32_t) * (size_t)d.G * d.W * d.CH);
   w.local_off = reinterpret_cast<int32_t*>(p);
-  p += align256(sizeof(int32_t) * (size_t)d.G * d.W);
+  p += align256(sizeof(int32_t) * (size_t)d.G * d.W * d.CH);
   w.eidx = reinterpret_cast<int32_t*>(p);
   p += align256(sizeof(int32_t) * (size_t)d.W * d.BS * d.NS);
   w.rank_tot = reinterpret_cast<int32_t*>(p);

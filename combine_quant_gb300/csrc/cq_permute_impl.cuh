@@ -445,14 +445,14 @@ __device__ __forceinline__ int map_slot(const PermuteArgs& a, int64_t tok, int r
       g = dst = s * d.R_rep + r % d.R_rep;  // a shared-expert rank hosts one slot
       srow = s;
     }
-    row = a.ws.rank_base[dst] + a.ws.local_off[(int64_t)g * d.W + r] + e;
+    const int i = (int)(tok - (int64_t)r * d.BS);
+    row = a.ws.rank_base[dst] + a.ws.local_off[((int64_t)g * d.W + r) * d.CH + i / d.TC] + e;
     if (row < 0 || (int64_t)row >= d.R_max) {  // consistency guard: never write outside
       atomicOr(a.ws.status, (uint32_t)CQ_ST_INTERNAL);
       row = -1;
       code = CQ_INV_NONE;
     } else {
       code = row;
-      const int i = (int)(tok - (int64_t)r * d.BS);
       reinterpret_cast<int4*>(a.assist_rows)[row] = make_int4(r, i, k, 0);
       if (a.expand_scales)
         a.expand_scales[row] =

@@ -1,21 +1,23 @@
 // cq_route.cu -- routing scan on the device: two kernels, no serial tail.
 //
-// count_kernel (one CTA per source rank r) walks expert_ids[r] in row-major
-// (token, then k) order and gives every MoE pair its arrival ordinal at its
-// expert ("expandIdx", the sendStatus counter of "MoeDistributeDispatch和
-// MoeDistributeCombine算子设计介绍" §2.2.2) and every active token its ordinal
-// among active tokens (the shared-expert slots). The tokens of a source are
-// split into contiguous per-warp ranges (4, 16 or 32 warps by batch size);
+// count_kernel (one CTA per chunk of a source rank r's tokens; the chunks of
+// a source are counted side by side and offsets_kernel chains them) walks
+// its tokens in row-major (token, then k) order and gives every MoE pair its
+// arrival ordinal at its expert within the chunk ("expandIdx", the sendStatus
+// counter of "MoeDistributeDispatch和MoeDistributeCombine算子设计介绍" §2.2.2,
+// once the chunk's first row is added) and every active token its ordinal
+// among the chunk's active tokens (the shared-expert slots). A chunk's tokens
+// are split into contiguous per-warp ranges (4, 16 or 32 warps by size);
 // one walk with warp match_any (equal ids grouped, ranked by lane) gives
 // each pair its ordinal inside its warp's range and per-warp counts; a
 // per-expert scan over the warps then turns those into the serial scan's
-// ordinals and this source's counts.
+// ordinals within the chunk and the chunk's counts.
 //
 // offsets_kernel (one CTA per destination rank d) prefix-sums rank d's
 // received-count matrix, transposed to (local expert, source) order and summed
-// row-major (§2.4.1), which is ep_recv_count[d]; it also writes
-// expert_token_nums[d] and each (slot, source) block's first row counted from
-// the start of rank d. The counts table is slot-major and the slots of a rank
+// row-major (§2.4.1), which is ep_recv_count[d]; the counts come per (local
+// expert, source, chunk), so the same scan gives each chunk's block its first
+// row counted from the start of rank d. It also writes expert_token_nums[d]. The counts table is slot-major and the slots of a rank
 // are contiguous, so rank d's first row is the sum of the table's entries
 // before its first slot: for tables of up to kDirectBase entries every CTA
 // sums them itself (one parallel reduction); for larger ones the last CTA
@@ -27,9 +29,10 @@
 namespace cq {
 namespace {
 
-// The count kernel runs kCountWarps warps per source rank, or kCountWarpsWide
-// for batches of at least kWideBS tokens per rank (shorter per-warp ranges;
-// measured faster from BS = 256 on, slower for small batches).
+// The count kernel runs kCountWarps warps per CTA (one chunk of a source's
+// tokens), kCountWarpsWide for chunks of at least kWideBS tokens (shorter
+// per-warp ranges; measured faster from 256 tokens on, slower for fewer) and
+// kCountWarpsSmall for chunks of at most kSmallBS.
 constexpr int kCountWarps = 16;
 constexpr int kCountWarpsWide = 32;
 constexpr int kWideBS = 256;
@@ -102,8 +105,12 @@ __device__ int block_excl_scan(int v, int* buf, int* total) {
   return res;
 }
 
-// trigger_early: every CTA of this grid is resident at once (W <= SM count),
-// so the dependent kernels may launch right away without starving it.
+// CTA r * CH + c counts chunk c of source r: tokens [c * TC, (c + 1) * TC).
+// Its ordinals run within the chunk; offsets_kernel gives every (slot,
+// source, chunk) block its first row, so the chunks of a source follow one
+// another in arrival order.
+// trigger_early: every CTA of this grid is resident at once (W * CH <= SM
+// count), so the dependent kernels may launch right away without starving it.
 // STEPS >= the 32-pair steps of a warp's range: the unrolled loops hold only
 // as many steps as the problem needs (the kernel's code is fetched cold from
 // DRAM when L2 holds other data, so its size shows in the latency).
@@ -116,13 +123,14 @@ __global__ void __launch_bounds__(NW * 32) count_kernel(RouteArgs a, int trigger
 
   if (trigger_early) griddep_launch_dependents();
   const Dims& d = a.d;
-  const int r = blockIdx.x;
+  const int r = blockIdx.x / d.CH, chunk = blockIdx.x - r * d.CH;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int M = d.M, K = d.K, BS = d.BS, NS = d.NS;
   int n_r = BS;
   if (a.bs_per_rank) n_r = min(max(a.bs_per_rank[r], 0), BS);
-  const int tpw = (BS + NW - 1) / NW;
-  const int t0 = min(warp * tpw, BS), t1 = min(t0 + tpw, BS);
+  const int lo = min(chunk * d.TC, BS), hi = min(lo + d.TC, BS);  // this CTA's tokens
+  const int tpw = (hi - lo + NW - 1) / NW;
+  const int t0 = min(lo + warp * tpw, hi), t1 = min(t0 + tpw, hi);
   const int p0 = t0 * K, p1 = t1 * K;
   const int nsteps = (p1 - p0 + 31) >> 5;
   uint16_t* mytbl = tbl + warp * M;
@@ -153,7 +161,7 @@ __global__ void __launch_bounds__(NW * 32) count_kernel(RouteArgs a, int trigger
   for (int t = threadIdx.x; t < NW * M; t += kThreads) tbl[t] = 0;
   // [DV3] x_active_mask: in 1-D form every true entry precedes every false one.
   if (d.mask_ndim == 1 && a.mask) {
-    for (int i = threadIdx.x + 1; i < n_r; i += kThreads) {
+    for (int i = max(lo, 1) + (int)threadIdx.x; i < min(hi, n_r); i += kThreads) {
       const int64_t tok = (int64_t)r * BS + i;
       if (a.mask[tok] && !a.mask[tok - 1]) atomicOr(a.ws.status, (uint32_t)CQ_ST_BAD_MASK);
     }
@@ -188,7 +196,7 @@ __global__ void __launch_bounds__(NW * 32) count_kernel(RouteArgs a, int trigger
   __syncthreads();
 
   // Per expert: exclusive scan over the warps (warp bases); the total is
-  // this source's count for the expert.
+  // this chunk's count for the expert.
   for (int e = threadIdx.x; e < M; e += kThreads) {
     int run = 0;
     for (int w = 0; w < NW; ++w) {
@@ -196,7 +204,7 @@ __global__ void __launch_bounds__(NW * 32) count_kernel(RouteArgs a, int trigger
       tbl[w * M + e] = (uint16_t)run;
       run += c;
     }
-    a.ws.counts_t[(int64_t)(d.S_r + e) * d.W + r] = run;
+    a.ws.counts_t[((int64_t)(d.S_r + e) * d.W + r) * d.CH + chunk] = run;
   }
   if (threadIdx.x == 0) {
     int run = 0;
@@ -204,15 +212,16 @@ __global__ void __launch_bounds__(NW * 32) count_kernel(RouteArgs a, int trigger
       s_tokbase[w] = run;
       run += s_tokcnt[w];
     }
-    s_tokbase[NW] = run;  // active tokens of this source
+    s_tokbase[NW] = run;  // active tokens of this chunk
   }
   __syncthreads();
   // Shared-expert rank g hosts replica g % R of shared expert g / R; source r
-  // sends every active token to replica r % R of each shared expert.
+  // sends every active token to replica r % R of each shared expert. (The
+  // active tokens of this chunk.)
   const int n_act = s_tokbase[NW];
   for (int g = threadIdx.x; g < d.S_r; g += kThreads) {
     const bool mine = d.S_eff > 0 && (g % d.R_rep) == (r % d.R_rep);
-    a.ws.counts_t[(int64_t)g * d.W + r] = mine ? n_act : 0;
+    a.ws.counts_t[((int64_t)g * d.W + r) * d.CH + chunk] = mine ? n_act : 0;
   }
 
   // Final ordinals: the warp's base for the expert plus the in-warp ordinal.
@@ -227,7 +236,7 @@ __global__ void __launch_bounds__(NW * 32) count_kernel(RouteArgs a, int trigger
     }
   }
   if (__any_sync(kFull, bad_id) && lane == 0) atomicOr(a.ws.status, (uint32_t)CQ_ST_BAD_ID);
-  // Shared slots: ordinal of the token among this source's active tokens.
+  // Shared slots: ordinal of the token among this chunk's active tokens.
   int run = s_tokbase[warp];
   for (int base = t0; base < t1; base += 32) {
     const int i = base + lane;
@@ -256,8 +265,9 @@ __global__ void __launch_bounds__(kOffThreads) offsets_kernel(RouteArgs a) {
   const Dims& d = a.d;
   const int rank = blockIdx.x;
   const int Ld = rank < d.S_r ? 1 : d.L;
-  const int n = Ld * d.W;  // this rank's (local expert, source) entries, <= 2048
-  const int64_t g0w = (int64_t)gslot(d, rank, 0) * d.W;
+  const int WC = d.W * d.CH;
+  const int n = Ld * WC;  // this rank's (local expert, source, chunk) entries, <= 2048
+  const int64_t g0w = (int64_t)gslot(d, rank, 0) * WC;
   const int* cnt = a.ws.counts_t + g0w;
   int* loc = a.ws.local_off + g0w;
   int* erc = a.ep_recv_count + (int64_t)rank * d.W * d.L;
@@ -265,10 +275,10 @@ __global__ void __launch_bounds__(kOffThreads) offsets_kernel(RouteArgs a) {
   // Small tables: this rank's first row is the sum of the counts of all
   // slots before its first one (ranks are laid out slot-major, shared ranks
   // first); those loads go out together with this rank's own.
-  const bool direct = (int64_t)d.G * d.W <= kDirectBase;
+  const bool direct = (int64_t)d.G * WC <= kDirectBase;
   int part = 0;
   if (direct) {
-    const int n_before = gslot(d, rank, 0) * d.W;
+    const int n_before = gslot(d, rank, 0) * WC;
     for (int t = threadIdx.x; t < n_before; t += kOffThreads) part += __ldcg(a.ws.counts_t + t);
   }
 
@@ -290,16 +300,18 @@ __global__ void __launch_bounds__(kOffThreads) offsets_kernel(RouteArgs a) {
     if (c0 + q < c1) {
       loc[c0 + q] = run;  // exclusive: first row of the block within rank d
       run += v[q];
-      erc[c0 + q] = run;  // inclusive running count (ep_recv_count)
+      // inclusive running count (ep_recv_count) at the end of a (local
+      // expert, source) pair's chunks
+      if ((c0 + q) % d.CH == d.CH - 1) erc[(c0 + q) / d.CH] = run;
     }
   }
-  for (int t = n + threadIdx.x; t < d.W * d.L; t += kOffThreads) erc[t] = 0;  // shared-rank padding
+  for (int t = Ld * d.W + threadIdx.x; t < d.W * d.L; t += kOffThreads) erc[t] = 0;  // shared-rank padding
   __syncthreads();
   for (int le = threadIdx.x; le < d.L; le += kOffThreads) {
     int64_t e = 0;
     if (le < Ld) {
       const int end = erc[le * d.W + d.W - 1];
-      e = d.etn_type == 1 ? end - loc[le * d.W] : end;  // [DV3] 1: counts, 0: cumsum
+      e = d.etn_type == 1 ? end - loc[le * WC] : end;  // [DV3] 1: counts, 0: cumsum
     }
     a.expert_token_nums[(int64_t)rank * d.L + le] = e;
   }
@@ -364,21 +376,21 @@ cudaError_t launch_count(const RouteArgs& a, size_t table, int trigger, cudaStre
     const cudaError_t e = prepare_kernel<count_kernel<STEPS, NW>>(table);
     if (e != cudaSuccess) return e;
   }
-  count_kernel<STEPS, NW><<<a.d.W, NW * 32, table, s>>>(a, trigger);
+  count_kernel<STEPS, NW><<<a.d.W * a.d.CH, NW * 32, table, s>>>(a, trigger);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s) {
-  const bool wide = a.d.BS >= kWideBS, small = a.d.BS <= kSmallBS;
+  const bool wide = a.d.TC >= kWideBS, small = a.d.TC <= kSmallBS;
   const int nw = wide ? kCountWarpsWide : small ? kCountWarpsSmall : kCountWarps;
   const size_t table = sizeof(uint16_t) * nw * (size_t)a.d.M;  // <= 64 KB
   const int sms = sm_count();
   if (sms < 1) return cudaErrorInvalidDevice;
-  const int tpw = (a.d.BS + nw - 1) / nw;
+  const int tpw = (a.d.TC + nw - 1) / nw;
   const int steps = (tpw * a.d.K + 31) / 32;
-  const int trigger = a.d.W <= sms ? 1 : 0;
+  const int trigger = a.d.W * a.d.CH <= sms ? 1 : 0;
   cudaError_t e;
   if (small) {  // at most 8 tokens x 16 slots per warp: 4 steps
     e = steps <= 2 ? launch_count<2, kCountWarpsSmall>(a, table, trigger, s)
