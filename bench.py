@@ -44,13 +44,13 @@ L2_FLUSH_BYTES = 256 << 20
 # the SHA-256 of the kernel's source file when it was captured; reported only
 # while the source is unchanged.
 NCU_TRAFFIC = {
-    # profiles/dsv3_step_launch_list.md: read 470.057216 MB + write 46.016987 MB
+    # profiles/dsv3_step_launch_list.md: read 470.060069 MB + write 45.994167 MB
     # per launch (mean of 7 launches of one bench run)
-    "combine": {"bytes_per_launch": 516074203,
-                "src_sha": "b090933ecfdde47099116ed07ad89f5a2750ed97451a34af3d81928c84a8df70"},
-    # the same capture: read 59.230208 MB + write 172.213065 MB
-    "permute": {"bytes_per_launch": 231443273,
-                "src_sha": "8aede6438126f7eda6073859216754b2f4f8104c9130e10f548d1319bf5d840d"},
+    "combine": {"bytes_per_launch": 516054236,
+                "src_sha": "8d741c14ee26fb8fde975f730b613fe458654c983cd497c6568d0fd62465aefd"},
+    # the same capture: read 59.322661 MB + write 172.101522 MB
+    "permute": {"bytes_per_launch": 231424183,
+                "src_sha": "95ab111c9597c66d182baecd09406efc4d0683505aec9a5a9dd53414b9c30f72"},
 }
 
 
