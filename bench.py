@@ -25,6 +25,7 @@ import hashlib
 import inspect
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -41,16 +42,16 @@ UNIT = "tokens/s"
 L2_FLUSH_BYTES = 256 << 20
 
 # DRAM bytes per launch read from an ncu capture of the named kernel, keyed by
-# the SHA-256 of the kernel's source file when it was captured; reported only
-# while the source is unchanged.
+# the SHA-256 of the code of the kernel's source files (comments left out)
+# when it was captured; reported only while that code is unchanged.
 NCU_TRAFFIC = {
     # profiles/dsv3_step_launch_list.md: read 470.060069 MB + write 45.994167 MB
     # per launch (mean of 7 launches of one bench run)
     "combine": {"bytes_per_launch": 516054236,
-                "src_sha": "8d741c14ee26fb8fde975f730b613fe458654c983cd497c6568d0fd62465aefd"},
+                "src_sha": "ab714ab07af6631bbe2af8a6047bc243a9f72b3dcad8eba7ff6b890926efe122"},
     # the same capture: read 59.322661 MB + write 172.101522 MB
     "permute": {"bytes_per_launch": 231424183,
-                "src_sha": "95ab111c9597c66d182baecd09406efc4d0683505aec9a5a9dd53414b9c30f72"},
+                "src_sha": "3c5fdb061f4710990c312e87909514cdcdc753afa41dec103d302908e9c86e6e"},
 }
 
 
@@ -258,12 +259,21 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(text: str) -> str:
+    """C/CUDA source without comments and with whitespace collapsed (the
+    kernel sources hold no string literal with a comment marker in it)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def source_sha(kernel: str) -> str:
-    """SHA-256 over the source files that define the kernel."""
+    """SHA-256 over the code (comments left out) of the source files that
+    define the kernel."""
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "combine_quant_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "combine_quant_gb300", "csrc", name), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()
 
 

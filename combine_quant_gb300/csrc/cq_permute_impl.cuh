@@ -3,10 +3,11 @@
 // and fp16 by cq_permute_bf16.cu / cq_permute_f16.cu.
 //
 // permute_kernel: one CTA per source token (r, i). Warp 0 turns each slot's arrival ordinal
-// into its global row (rank base + first row of the (expert slot, source)
-// block within the rank + ordinal: the address rule of "MoeDistributeDispatch
-// 和MoeDistributeCombine算子设计介绍" §3.4.2 with the source block folded into the
-// expert offset), writes the inverse map, the (src, token, slot) row record and
+// into its global row (rank base + first row of the (expert slot, source,
+// chunk of the source's tokens) block within the rank + ordinal within the
+// chunk: the address rule of "MoeDistributeDispatch和MoeDistributeCombine算子
+// 设计介绍" §3.4.2 with the source block folded into the expert offset),
+// writes the inverse map, the (src, token, slot) row record and
 // the carried weight. All threads load the token row once with 128-bit loads
 // (started before the routing kernels finish), quantise it in registers and
 // stage the code row in shared memory; one thread then writes it to every
