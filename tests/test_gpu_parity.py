@@ -249,10 +249,11 @@ def test_edge_max_bs():
 
 
 def test_edge_count_kernel_widths():
-    """The routing scan runs 32 warps per source from 256 tokens per rank on
-    (with M = 1024 its per-warp table is 64 KB of shared memory) and 4 warps
-    up to 32 tokens per rank; both against the oracle at those edges."""
-    _full_check(_cfg_case(15, W=8, M=1024, BS=256, K=16, H=1024))
+    """The routing scan runs 32 warps per CTA from 256 tokens a CTA on (with
+    M = 1024 its per-warp table is 64 KB of shared memory: W = 2, BS = 512
+    gives two chunks of 256 tokens per source) and 4 warps up to 32; both
+    against the oracle at those edges."""
+    _full_check(_cfg_case(15, W=2, M=1024, BS=512, K=16, H=1024))
     _full_check(_cfg_case(16, W=4, M=16, BS=32, K=16, H=1024))
 
 
