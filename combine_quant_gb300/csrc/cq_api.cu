@@ -78,12 +78,15 @@ Dims dims_of(const cq_config* c) {
   d.SC = (blocks + 1) / 2 * 2;
   d.G3 = (d.H + 127) / 128;
   d.R_max = (int64_t)d.W * d.BS * d.NS;
-  // Routing chunks: CH count CTAs per source, about kRouteCtas in all, none
-  // under kRouteMinTokens tokens, and at most 2048 (local expert, source,
-  // chunk) entries per destination rank (L * W <= 2048 holds already).
-  constexpr int kRouteCtas = 128, kRouteMinTokens = 32;
-  int ch = kRouteCtas / d.W;
-  if (ch > d.BS / kRouteMinTokens) ch = d.BS / kRouteMinTokens;
+  // Routing chunks: CH count CTAs per source, chunks of about
+  // kRouteChunkTokens tokens (16 warps of 4 tokens), at most kRouteCtas
+  // count CTAs in all, and at most 2048 (local expert, source, chunk) entries
+  // per destination rank (L * W <= 2048 holds already). Measured best among
+  // 32-512 tokens a chunk and 64-256 CTAs on the DSV3, skew, mxfp8, special
+  // and perf256 workloads.
+  constexpr int kRouteCtas = 128, kRouteChunkTokens = 64;
+  int ch = d.BS / kRouteChunkTokens;
+  if (ch > kRouteCtas / d.W) ch = kRouteCtas / d.W;
   if (ch > 2048 / (d.L * d.W)) ch = 2048 / (d.L * d.W);
   if (ch < 1) ch = 1;
   d.CH = ch;

@@ -1,6 +1,6 @@
 """The routing scan counts each source's tokens in chunks, one count CTA
-per chunk (CH = 128 / W chunks of at least 32 tokens, and at most 2048
-(local expert, source, chunk) entries per rank); offsets_kernel chains the
+per chunk (chunks of about 64 tokens, at most 128 count CTAs and at most
+2048 (local expert, source, chunk) entries per rank); offsets_kernel chains the
 chunks of a source. These cases put chunk boundaries where they matter and
 compare every dispatch output of cq_dispatch_route + cq_dispatch_permute
 (always the chunked kernels) with the oracle: per-rank batch sizes ending inside, at
@@ -41,7 +41,7 @@ def _case(seed, W, M, BS, K, H=1024, mode=2, **kw):
 
 def _cases():
     out = {}
-    # 4 sources x 8 chunks of 32 tokens; batch sizes ending inside, at and
+    # 4 sources x 4 chunks of 64 tokens; batch sizes ending inside, at and
     # before chunk boundaries, and an empty source
     wl, rng = _case(71, W=4, M=16, BS=256, K=4)
     wl.bs_per_rank = np.array([77, 256, 0, 32], np.int32)
@@ -53,10 +53,10 @@ def _cases():
         wl.mask[r, :n] = 1
     out["mask1d_prefixes"] = wl
     # 2-D mask with duplicate and invalid ids
-    wl, rng = _case(73, W=4, M=12, BS=96, K=6, mask_ndim=2, zero_expert_num=1,
+    wl, rng = _case(73, W=4, M=12, BS=192, K=6, mask_ndim=2, zero_expert_num=1,
                     copy_expert_num=1, const_expert_num=1)
-    wl.expert_ids = rng.integers(-1, 16, (4, 96, 6)).astype(np.int32)  # 15, -1: invalid
-    wl.mask = (rng.random((4, 96, 6)) < 0.6).astype(np.uint8)
+    wl.expert_ids = rng.integers(-1, 16, (4, 192, 6)).astype(np.int32)  # 15, -1: invalid
+    wl.mask = (rng.random((4, 192, 6)) < 0.6).astype(np.uint8)
     out["mask2d_duplicates_invalid_special"] = wl
     # shared experts with replicas; per-rank batch sizes
     wl, rng = _case(74, W=8, M=24, BS=192, K=4, shared_expert_num=2, shared_expert_rank_num=4,
