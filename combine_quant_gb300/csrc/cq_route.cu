@@ -17,9 +17,9 @@
 // received-count matrix, transposed to (local expert, source) order and summed
 // row-major (§2.4.1), which is ep_recv_count[d]; the counts come per (local
 // expert, source, chunk), so the same scan gives each chunk's block its first
-// row counted from the start of rank d. It also writes expert_token_nums[d]. The counts table is slot-major and the slots of a rank
-// are contiguous, so rank d's first row is the sum of the table's entries
-// before its first slot: for tables of up to kDirectBase entries every CTA
+// row counted from the start of rank d. It also writes expert_token_nums[d].
+// The counts table is slot-major and the slots of a rank are contiguous, so
+// rank d's first row is the sum of the table's entries before its first slot: for tables of up to kDirectBase entries every CTA
 // sums them itself (one parallel reduction); for larger ones the last CTA
 // (one atomic counter, no spin) prefix-sums the W rank totals.
 // Page tags ([DV3], [DSN], [LLD], [PERF]) name the source pages listed at the
