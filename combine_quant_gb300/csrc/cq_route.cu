@@ -19,9 +19,10 @@
 // expert, source, chunk), so the same scan gives each chunk's block its first
 // row counted from the start of rank d. It also writes expert_token_nums[d].
 // The counts table is slot-major and the slots of a rank are contiguous, so
-// rank d's first row is the sum of the table's entries before its first slot: for tables of up to kDirectBase entries every CTA
-// sums them itself (one parallel reduction); for larger ones the last CTA
-// (one atomic counter, no spin) prefix-sums the W rank totals.
+// rank d's first row is the sum of the table's entries before its first
+// slot: for tables of up to kDirectBase entries every CTA sums them itself
+// (one parallel reduction); for larger ones the last CTA (one atomic
+// counter, no spin) prefix-sums the W rank totals.
 // Page tags ([DV3], [DSN], [LLD], [PERF]) name the source pages listed at the
 // top of include/cq.h.
 #include "cq_internal.cuh"
