@@ -33,7 +33,43 @@ def uses_smooth(wl) -> bool:
     return wl.smooth is not None and wl.cfg["quant_mode"] in (1, 2, 3)
 
 
+def one_kernel_dispatch(wl) -> bool:
+    """Whether cq_dispatch runs this problem as one kernel (the limits of
+    dispatch_small_fits in cq_dispatch_small.cu)."""
+    c = wl.cfg
+    mode, W, BS, K = c["quant_mode"], c["ep_world_size"], c["max_bs"], c["topk"]
+    per_expert = uses_smooth(wl) and c.get("smooth_kind", 0) == 0
+    if per_expert and mode != 2:
+        return False
+    if not (mode in (0, 2) or (mode == 5 and c.get("y_dtype", 0) == 0)):
+        return False
+    return (W * BS * K <= 4096 and (c["shared_expert_rank_num"] + c["moe_expert_num"]) * W <= 2048
+            and W <= 768 and K <= 16)
+
+
+def _same_outputs(cfg, a, b) -> None:
+    """Every defined output equal (rows past the total are left untouched)."""
+    rows_a, inv_a, base_a = cq.assist_views(cfg, a.assist_info)
+    rows_b, inv_b, base_b = cq.assist_views(cfg, b.assist_info)
+    R = int(host(base_a)[-1])
+    assert torch.equal(base_a, base_b) and torch.equal(inv_a, inv_b)
+    assert torch.equal(rows_a[:R], rows_b[:R])
+    for name in ("ep_recv_count", "expert_token_nums"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name
+    assert torch.equal(a.expand_x[:R].view(torch.uint8), b.expand_x[:R].view(torch.uint8))
+    if a.expand_scales is not None:
+        assert torch.equal(a.expand_scales[:R], b.expand_scales[:R])
+    if a.dynamic_scales is not None:
+        assert torch.equal(a.dynamic_scales[:R].view(torch.uint8),
+                           b.dynamic_scales[:R].view(torch.uint8))
+
+
 def gpu_dispatch(wl: workloads.Workload):
+    """cq_dispatch on the workload. Where that runs as one kernel, the two
+    halves (cq_dispatch_route + cq_dispatch_permute: the routing, permute and
+    per-expert-smooth kernels that larger problems run) run too and must give
+    the same outputs and status, so every caller's oracle comparison covers
+    both paths."""
     cfg = cq.Config.from_dict(wl.cfg)
     x = dev(wl.x, cfg.token_dtype)
     ids = dev(wl.expert_ids, torch.int32)
@@ -45,6 +81,13 @@ def gpu_dispatch(wl: workloads.Workload):
     out = cq.dispatch(cfg, x, ids, smooth_scales=sm, x_active_mask=mask, bs_per_rank=bpr,
                       expert_scales=w, workspace=ws)
     status = cq.read_status(ws)
+    if one_kernel_dispatch(wl):
+        ws2 = cq.alloc_workspace(cfg, DEV)
+        out2 = cq.alloc_dispatch_outputs(cfg, DEV)
+        cq.dispatch_route(cfg, ids, mask, bpr, workspace=ws2, out=out2)
+        cq.dispatch_permute(cfg, x, ids, sm, w, mask, bpr, workspace=ws2, out=out2)
+        assert cq.read_status(ws2) == status
+        _same_outputs(cfg, out, out2)
     return cfg, out, status, ws
 
 
