@@ -148,6 +148,19 @@ struct SrcQ8 {
   }
 };
 
+// Expert-output rows of the token type (bf16 or fp16), read directly.
+template <class T>
+struct Src16 {
+  const uint16_t* rows;
+  struct Item {
+    uint4 v;
+  };
+  __device__ Item load(int64_t row, int H, int u) const {
+    return {ld_nc_v4(rows + row * H + 8 * (int64_t)u)};
+  }
+  __device__ void floats(const Item& it, float (&f)[8]) const { unpack8<T>(it.v, f); }
+};
+
 // One CTA per (token, chunk of kThreads 8-element units); one unit per thread.
 constexpr int kThreads = 128;
 
@@ -530,6 +543,7 @@ __global__ void __launch_bounds__(kQThreads) combine_quant_kernel(CombineArgs a)
 // kRingBytes (several CTAs per SM), 2..kRingMax chunks; one CTA per item
 // (kPersistent false) or one wave of CTAs looping over the items.
 constexpr int kChunkCols = 4096;
+constexpr int kWaveCtasPerSm = 3;  // about the staged kernel's CTAs per SM
 constexpr size_t kRingBytes = 36u << 10;
 constexpr bool kPersistent = true;
 
@@ -574,7 +588,16 @@ cudaError_t launch_combine_t(const CombineArgs& a, const Src& src, cudaStream_t 
 
 }  // namespace
 
+// A batch too small to give every CTA of the staged kernel's wave a work
+// item runs one CTA per (token, 1024 columns) instead, each thread loading
+// its unit of every routed row at once (one round trip instead of the
+// ring's laps). Both sum in the same order.
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) {
+  const int64_t items = (int64_t)a.d.W * a.d.BS * ((a.d.H + kChunkCols - 1) / kChunkCols);
+  if (items < (int64_t)kWaveCtasPerSm * sm_count()) {
+    if (a.d.x_dtype == 1) return launch_combine_t<F16>(a, Src16<F16>{a.ffn}, s);
+    return launch_combine_t<BF16>(a, Src16<BF16>{a.ffn}, s);
+  }
   if (a.d.x_dtype == 1)
     return a.out_f32 ? launch_staged<F16, true>(a, s) : launch_staged<F16, false>(a, s);
   return a.out_f32 ? launch_staged<BF16, true>(a, s) : launch_staged<BF16, false>(a, s);
