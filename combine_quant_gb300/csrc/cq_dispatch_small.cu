@@ -98,6 +98,8 @@ __global__ void __launch_bounds__(kSmallThreads)
   __shared__ int s_nrows;
   __shared__ float s_red[2][64];
   __shared__ int s_id[kMaxSlots];   // this token's expert ids (-1: pair off)
+  __shared__ int s_on[kMaxSlots];   // its pairs switched on
+  __shared__ float s_w[kMaxSlots];  // its routing weights
   __shared__ int s_ord[kMaxSlots];  // their ordinals; [K]: the token's ordinal among active ones
   __shared__ int s_act[kSmallMaxW];  // active tokens per source
   __shared__ int s_buf[kSmallWarps + 1];
@@ -137,15 +139,15 @@ __global__ void __launch_bounds__(kSmallThreads)
     }
   }
 
+  // This token's slots (thread k < K holds slot k): its id and weight, loaded
+  // now and used once the counts are in.
+  const bool my_on = (int)threadIdx.x < K && active && pair_on(a, tok, threadIdx.x);
+  const int my_id = my_on ? a.expert_ids[tok * K + threadIdx.x] : -1;
+  const float my_w = (int)threadIdx.x < K && a.expert_scales
+                         ? a.expert_scales[tok * K + threadIdx.x] : 0.f;
   for (int t = threadIdx.x; t < nE; t += nt) cnt[t] = 0;
   for (int t = threadIdx.x; t < W; t += nt) s_act[t] = 0;
-  if (threadIdx.x < kMaxSlots) {
-    s_ord[threadIdx.x] = 0;
-    int id = -1;
-    if (threadIdx.x < K && active && pair_on(a, tok, threadIdx.x))
-      id = a.expert_ids[tok * K + threadIdx.x];
-    s_id[threadIdx.x] = id;
-  }
+  if (threadIdx.x < kMaxSlots) s_ord[threadIdx.x] = 0;
   __syncthreads();
 
   // Every MoE pair of every source: rows per (slot, source); active tokens per source.
@@ -165,12 +167,16 @@ __global__ void __launch_bounds__(kSmallThreads)
       if (rr == r && ii < i) atomicAdd(&s_ord[K], 1);  // this token's shared-slot ordinal
     }
   }
+  if (threadIdx.x < kMaxSlots) {
+    s_id[threadIdx.x] = my_id;
+    s_on[threadIdx.x] = my_on;
+    s_w[threadIdx.x] = my_w;
+  }
+  __syncthreads();
   // Arrival ordinals of this token's MoE pairs: the earlier pairs of source r
-  // (token-major, then slot) with the same expert.
+  // (token-major, then slot) with the same expert, one shared-memory count
+  // per match.
   {
-    int c[16];  // K <= 16
-#pragma unroll
-    for (int k = 0; k < 16; ++k) c[k] = 0;
     const int p0 = r * d.BS * K, p1 = (int)tok * K + K;
     for (int p = p0 + threadIdx.x; p < p1; p += nt) {
       const int t = p / K, j = p - t * K;
@@ -178,16 +184,7 @@ __global__ void __launch_bounds__(kSmallThreads)
         const int id = a.expert_ids[p];
 #pragma unroll
         for (int k = 0; k < 16; ++k)
-          if (k < K && p < (int)tok * K + k && id == s_id[k]) ++c[k];
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      if (k < K) {
-        int v = c[k];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-        if (lane == 0 && v) atomicAdd(&s_ord[k], v);
+          if (k < K && p < (int)tok * K + k && id == s_id[k]) atomicAdd(&s_ord[k], 1);
       }
     }
   }
@@ -222,9 +219,9 @@ __global__ void __launch_bounds__(kSmallThreads)
     bool bad = false;
     if (k < K) {
       const int id = s_id[k];
-      if (k < K && active && pair_on(a, tok, k)) {
+      if (s_on[k]) {
         const int64_t Z0 = d.M, C0 = Z0 + d.Z, Q0 = C0 + d.C, Q1 = Q0 + d.Q;
-        const int64_t id64 = a.expert_ids[tok * K + k];
+        const int64_t id64 = id;
         if (id64 >= 0 && id64 < d.M) {
           ord = s_ord[k];
           row = start[(d.S_r + id) * W + r] + ord;
@@ -254,9 +251,7 @@ __global__ void __launch_bounds__(kSmallThreads)
     if (row >= 0) {
       code = row;
       reinterpret_cast<int4*>(a.assist_rows)[row] = make_int4(r, i, k, 0);
-      if (a.expand_scales)
-        a.expand_scales[row] =
-            k < K ? (a.expert_scales ? a.expert_scales[tok * K + k] : 0.f) : 1.f;
+      if (a.expand_scales) a.expand_scales[row] = k < K ? s_w[k] : 1.f;
     }
     if (k < NS) a.inv[tok * NS + k] = code;
     const unsigned bal = __ballot_sync(kFull, row >= 0);
