@@ -87,11 +87,15 @@ struct RouteOut {
 
 // trigger_early: every CTA of this grid is resident at once, so the next
 // kernel may launch right away without starving it.
+// halves (1 or 2): CTAs per token. With 2, both CTAs of a token route and
+// quantise the whole row, and each writes one half of every routed row's
+// bytes (so a batch of few tokens spreads its stores over twice the SMs);
+// the first writes the row records and scales.
 // SM == kRowPerSlot: each routed row is quantised with its own smooth row
 // (one expert's, or one shared expert's), one row after another.
 template <class T, int Q, int SM>
 __global__ void __launch_bounds__(kSmallThreads)
-    dispatch_small_kernel(PermuteArgs a, RouteOut ro, int trigger_early) {
+    dispatch_small_kernel(PermuteArgs a, RouteOut ro, int trigger_early, int halves) {
   constexpr int MODE = q_mode(Q);
   __shared__ int s_row[kMaxSlots];
   __shared__ int s_srow[kMaxSlots];  // the routed rows' smooth-table rows (kRowPerSlot)
@@ -106,7 +110,8 @@ __global__ void __launch_bounds__(kSmallThreads)
   extern __shared__ __align__(128) uint8_t s_dyn[];  // staged row, then counts, then prefix
 
   const Dims& d = a.d;
-  const int64_t tok = blockIdx.x;
+  const int64_t tok = blockIdx.x / halves;
+  const int half = blockIdx.x - (int)tok * halves;
   const int r = (int)(tok / d.BS), i = (int)(tok - (int64_t)r * d.BS);
   const int lane = threadIdx.x & 31;
   const int H = d.H, units = H >> 4, nt = blockDim.x;
@@ -115,6 +120,7 @@ __global__ void __launch_bounds__(kSmallThreads)
   const int code_bytes = MODE == 0 ? 2 * H : H;
   const int scale_bytes = MODE == 3 ? 4 * d.G3 : ((MODE == 4 || MODE == 5) ? d.SC : 0);
   const int stage_bytes = (code_bytes + ((scale_bytes + 15) & ~15) + 15) & ~15;
+  const int cpart = code_bytes / halves, spart = scale_bytes / halves;  // this CTA's bytes of a row
   uint8_t* const s_stage = s_dyn;
   int* const cnt = reinterpret_cast<int*>(s_dyn + stage_bytes);  // [G][W] rows per block
   int* const start = cnt + nE;                                  // [G][W] first global row
@@ -250,10 +256,12 @@ __global__ void __launch_bounds__(kSmallThreads)
     }
     if (row >= 0) {
       code = row;
-      reinterpret_cast<int4*>(a.assist_rows)[row] = make_int4(r, i, k, 0);
-      if (a.expand_scales) a.expand_scales[row] = k < K ? s_w[k] : 1.f;
+      if (half == 0) {
+        reinterpret_cast<int4*>(a.assist_rows)[row] = make_int4(r, i, k, 0);
+        if (a.expand_scales) a.expand_scales[row] = k < K ? s_w[k] : 1.f;
+      }
     }
-    if (k < NS) a.inv[tok * NS + k] = code;
+    if (k < NS && half == 0) a.inv[tok * NS + k] = code;
     const unsigned bal = __ballot_sync(kFull, row >= 0);
     if (row >= 0) {
       const int pos = __popc(bal & ((1u << lane) - 1u));
@@ -330,14 +338,15 @@ __global__ void __launch_bounds__(kSmallThreads)
       __syncthreads();
       const int64_t row = s_row[n];
       if (threadIdx.x == 0) {
-        bulk_store(out + row * code_bytes, s_stage, (uint32_t)code_bytes);
+        bulk_store(out + row * code_bytes + half * cpart, s_stage + half * cpart, (uint32_t)cpart);
         if (scale_bytes && a.scale_rows_bulk)
-          bulk_store(dyn + row * scale_bytes, s_stage + code_bytes, (uint32_t)scale_bytes);
+          bulk_store(dyn + row * scale_bytes + half * spart, s_stage + code_bytes + half * spart,
+                     (uint32_t)spart);
         bulk_commit();
         bulk_wait_read<0>();
       }
-      if (MODE == 2 && threadIdx.x == 0) reinterpret_cast<float*>(dyn)[row] = carried;
-      if (scale_bytes && !a.scale_rows_bulk)
+      if (MODE == 2 && threadIdx.x == 0 && half == 0) reinterpret_cast<float*>(dyn)[row] = carried;
+      if (scale_bytes && !a.scale_rows_bulk && half == 0)
         for (int b = threadIdx.x; b < scale_bytes; b += nt) dyn[row * scale_bytes + b] = s_stage[code_bytes + b];
       __syncthreads();  // the staging buffer is free for the next row
     }
@@ -378,14 +387,15 @@ __global__ void __launch_bounds__(kSmallThreads)
   if (threadIdx.x == 0) {
     for (int n = 0; n < nrows; ++n) {
       const int64_t row = s_row[n];
-      bulk_store(out + row * code_bytes, s_stage, (uint32_t)code_bytes);
+      bulk_store(out + row * code_bytes + half * cpart, s_stage + half * cpart, (uint32_t)cpart);
       if (scale_bytes && a.scale_rows_bulk)
-        bulk_store(dyn + row * scale_bytes, s_stage + code_bytes, (uint32_t)scale_bytes);
+        bulk_store(dyn + row * scale_bytes + half * spart, s_stage + code_bytes + half * spart,
+                   (uint32_t)spart);
     }
     bulk_commit();
     bulk_wait_read<0>();
   }
-  if (MODE != 0) {
+  if (MODE != 0 && half == 0) {
     if (MODE == 2 && threadIdx.x < nrows)
       reinterpret_cast<float*>(dyn)[s_row[threadIdx.x]] = carried;
     if (scale_bytes && !a.scale_rows_bulk) {
@@ -411,8 +421,15 @@ cudaError_t launch_small(const PermuteArgs& a, const RouteOut& ro, cudaStream_t 
   e = occupancy_blocks<dispatch_small_kernel<T, Q, SM>>(kSmallThreads, smem, &blocks);
   if (e != cudaSuccess) return e;
   const int64_t tokens = (int64_t)a.d.W * a.d.BS;
-  const int trigger = tokens <= (int64_t)sm_count() * blocks ? 1 : 0;
-  dispatch_small_kernel<T, Q, SM><<<(unsigned)tokens, kSmallThreads, smem, s>>>(a, ro, trigger);
+  const int64_t wave = (int64_t)sm_count() * blocks;
+  // Two CTAs per token while they still fit in one wave and a row's halves
+  // keep the bulk copies' 16-byte granularity.
+  const bool split = 2 * tokens <= wave && code_bytes % 32 == 0 &&
+                     (scale_bytes == 0 || !a.scale_rows_bulk || scale_bytes % 32 == 0);
+  const int halves = split ? 2 : 1;
+  const int trigger = tokens * halves <= wave ? 1 : 0;
+  dispatch_small_kernel<T, Q, SM>
+      <<<(unsigned)(tokens * halves), kSmallThreads, smem, s>>>(a, ro, trigger, halves);
   return cudaGetLastError();
 }
 
