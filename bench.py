@@ -54,6 +54,7 @@ NCU_TRAFFIC = {
                 "src_sha": "3c5fdb061f4710990c312e87909514cdcdc753afa41dec103d302908e9c86e6e"},
 }
 
+
 def _positive_int(text: str) -> int:
     v = int(text)
     if v < 1:
