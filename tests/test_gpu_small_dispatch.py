@@ -70,6 +70,8 @@ def _cases():
     out["K16_W2"], _ = _case(59, W=2, M=16, BS=128, K=16, H=1024, mode=5)
     out["K1_BS1"], _ = _case(60, W=16, M=32, BS=1, K=1, H=8192, mode=0)
     out["dsv3_small_at_the_limit"] = workloads.dsv3(seed=61, W=8, BS=64, M=64, K=8, H=2048)
+    # both limits at once: 4096 pairs and (S_r + M) * W = 2048 block counts
+    out["pairs_and_blocks_at_the_limit"], _ = _case(62, W=32, M=64, BS=16, K=8, H=7168, mode=0)
     return out
 
 
