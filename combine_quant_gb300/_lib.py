@@ -36,7 +36,8 @@ CQ_INV_CONST_BASE = -3
 # Every symbol include/cq.h declares.
 EXPORTS = (
     "cq_check_config", "cq_local_expert_num", "cq_num_slots", "cq_max_rows", "cq_scale_cols",
-    "cq_assist_info_size", "cq_workspace_size", "cq_workspace_init", "cq_dispatch",
+    "cq_assist_info_size", "cq_workspace_size", "cq_dispatch_workspace_size",
+    "cq_workspace_init", "cq_dispatch",
     "cq_dispatch_route", "cq_dispatch_permute", "cq_combine", "moe_dispatch", "moe_combine",
     "cq_read_status", "cq_strerror", "cq_dispatch_noalloc", "cq_combine_quant", "cq_combine_q8",
     "cq_read_combine_status", "cq_check_bounded_wait", "cq_combine_ws",
@@ -76,6 +77,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "cq_scale_cols": ([cfgp], i32),
         "cq_assist_info_size": ([cfgp], i64),
         "cq_workspace_size": ([cfgp], sz),
+        "cq_dispatch_workspace_size": ([cfgp], sz),
         "cq_workspace_init": ([P, sz, P], ctypes.c_int),
         "cq_dispatch": ([cfgp] + [P] * 13 + [sz, P], ctypes.c_int),
         "moe_dispatch": ([cfgp] + [P] * 13 + [sz, P], ctypes.c_int),

@@ -448,7 +448,14 @@ def assist_views(cfg: Config, assist_info: torch.Tensor):
 
 
 # The C ABI's names (include/cq.h) for the same calls.
+def dispatch_workspace_size(cfg: Config) -> int:
+    """Bytes of the dispatch workspace (cq_dispatch_workspace_size, the same
+    as Config.workspace_size)."""
+    return int(_lib.load().cq_dispatch_workspace_size(ctypes.byref(cfg.as_c())))
+
+
 cq_dispatch = moe_dispatch = dispatch
+cq_dispatch_workspace_size = dispatch_workspace_size
 cq_dispatch_route = dispatch_route
 cq_dispatch_permute = dispatch_permute
 cq_dispatch_noalloc = dispatch_noalloc

@@ -249,6 +249,8 @@ size_t cq_workspace_size(const cq_config* c) {
   return cq::workspace_bytes(dims_of(c));
 }
 
+size_t cq_dispatch_workspace_size(const cq_config* c) { return cq_workspace_size(c); }
+
 int cq_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
   if (!workspace || !aligned(workspace, 256)) return CQ_ERR_ARG;
   return cudaMemsetAsync(workspace, 0, workspace_bytes, static_cast<cudaStream_t>(stream)) ==

@@ -111,6 +111,7 @@ int64_t cq_max_rows(const cq_config* cfg);         /* R_max */
 int32_t cq_scale_cols(const cq_config* cfg);       /* SC */
 int64_t cq_assist_info_size(const cq_config* cfg); /* int32 elements of assist_info */
 size_t cq_workspace_size(const cq_config* cfg);    /* bytes */
+size_t cq_dispatch_workspace_size(const cq_config* cfg); /* the same size, by its other name */
 
 /* Zero-fill a freshly allocated workspace (enqueued on `stream`). Required
  * once before its first use; the library keeps it consistent afterwards.

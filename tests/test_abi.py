@@ -52,6 +52,15 @@ def test_binding_has_every_call_under_its_c_name():
         assert callable(getattr(cq, name, None)), f"binding lacks {name}"
 
 
+def test_workspace_size_under_both_names(lib):
+    """cq_dispatch_workspace_size and cq_workspace_size are one size; the
+    binding's size query gives it too."""
+    import combine_quant_gb300 as cq
+    cfg = cq.Config(ep_world_size=32, moe_expert_num=256, max_bs=128, topk=8, hidden=7168,
+                    quant_mode=2)
+    assert cq.cq_dispatch_workspace_size(cfg) == cfg.workspace_size > 0
+
+
 def _c(cfg):
     return ctypes.byref(_lib.CqConfig(**cfg))
 
@@ -116,6 +125,7 @@ def test_derived_sizes(lib, oracle_lib, name):
     W, BS, NS = cfg["ep_world_size"], cfg["max_bs"], oracle.num_slots(cfg)
     assert lib.cq_assist_info_size(c) == 4 * oracle.max_rows(cfg) + W * BS * NS + W + 1
     assert lib.cq_workspace_size(c) > 0
+    assert lib.cq_dispatch_workspace_size(c) == lib.cq_workspace_size(c)
 
 
 def _no_gpu_visible():
