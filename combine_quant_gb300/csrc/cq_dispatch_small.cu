@@ -6,10 +6,11 @@
 // shared memory, the rows of every (expert slot, source) block and their
 // exclusive prefix in slot-major order, which is each block's first global
 // row (rank base + the block's offset within the rank, "MoeDistributeDispatch
-// 和MoeDistributeCombine算子设计介绍" §2.4 and §3.4.2). It then counts the
-// earlier pairs of its own source with each of its experts (the arrival
-// ordinal, expandIdx of §2.2.2), maps its slots to rows and quantises and
-// scatters its token row exactly as permute_kernel does. CTA 0 also writes
+// 和MoeDistributeCombine算子设计介绍" §2.4 and §3.4.2). In the same pass over
+// the pairs it counts the earlier pairs of its own source with each of its
+// experts (the arrival ordinal, expandIdx of §2.2.2); it then maps its slots
+// to rows and quantises and scatters its token row exactly as permute_kernel
+// does. CTA 0 also writes
 // the routing outputs (ep_recv_count, expert_token_nums, rank_row_base) and
 // the workspace's total rows, so every output ends up as cq_dispatch_route +
 // cq_dispatch_permute leave it (the routing kernels' own scratch tables in
@@ -145,25 +146,39 @@ __global__ void __launch_bounds__(kSmallThreads)
     }
   }
 
-  // This token's slots (thread k < K holds slot k): its id and weight, loaded
-  // now and used once the counts are in.
+  // This token's slots (thread k < K holds slot k): its id and weight, in
+  // shared memory before the pass over all pairs below.
+  const int n_pairs = W * d.BS * K;
   const bool my_on = (int)threadIdx.x < K && active && pair_on(a, tok, threadIdx.x);
-  const int my_id = my_on ? a.expert_ids[tok * K + threadIdx.x] : -1;
+  const int my_id = (int)threadIdx.x < K ? a.expert_ids[tok * K + threadIdx.x] : -1;
   const float my_w = (int)threadIdx.x < K && a.expert_scales
                          ? a.expert_scales[tok * K + threadIdx.x] : 0.f;
   for (int t = threadIdx.x; t < nE; t += nt) cnt[t] = 0;
   for (int t = threadIdx.x; t < W; t += nt) s_act[t] = 0;
-  if (threadIdx.x < kMaxSlots) s_ord[threadIdx.x] = 0;
+  if (threadIdx.x < kMaxSlots) {
+    s_ord[threadIdx.x] = 0;
+    s_id[threadIdx.x] = my_on ? my_id : -1;
+    s_on[threadIdx.x] = my_on;
+    s_w[threadIdx.x] = my_w;
+  }
   __syncthreads();
 
-  // Every MoE pair of every source: rows per (slot, source); active tokens per source.
-  const int n_pairs = W * d.BS * K;
+  // Every MoE pair of every source: rows per (slot, source). In the same
+  // pass, the arrival ordinals of this token's MoE pairs: the earlier pairs
+  // of source r (token-major, then slot) with the same expert, one
+  // shared-memory count per match.
+  const int p_lo = r * d.BS * K, p_hi = (int)tok * K + K;
   for (int p = threadIdx.x; p < n_pairs; p += nt) {
     const int t = p / K, j = p - t * K;
     const int rr = t / d.BS, ii = t - rr * d.BS;
     if (ii < tokens_of(a, rr) && pair_on(a, t, j)) {
       const int id = a.expert_ids[p];
       if (id >= 0 && id < d.M) atomicAdd(&cnt[(d.S_r + id) * W + rr], 1);
+      if (p >= p_lo && p < p_hi) {
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          if (k < K && p < (int)tok * K + k && id == s_id[k]) atomicAdd(&s_ord[k], 1);
+      }
     }
   }
   for (int t = threadIdx.x; t < W * d.BS; t += nt) {
@@ -171,27 +186,6 @@ __global__ void __launch_bounds__(kSmallThreads)
     if (ii < tokens_of(a, rr) && token_on(a, t)) {
       atomicAdd(&s_act[rr], 1);
       if (rr == r && ii < i) atomicAdd(&s_ord[K], 1);  // this token's shared-slot ordinal
-    }
-  }
-  if (threadIdx.x < kMaxSlots) {
-    s_id[threadIdx.x] = my_id;
-    s_on[threadIdx.x] = my_on;
-    s_w[threadIdx.x] = my_w;
-  }
-  __syncthreads();
-  // Arrival ordinals of this token's MoE pairs: the earlier pairs of source r
-  // (token-major, then slot) with the same expert, one shared-memory count
-  // per match.
-  {
-    const int p0 = r * d.BS * K, p1 = (int)tok * K + K;
-    for (int p = p0 + threadIdx.x; p < p1; p += nt) {
-      const int t = p / K, j = p - t * K;
-      if (t - r * d.BS < n_r && pair_on(a, t, j)) {
-        const int id = a.expert_ids[p];
-#pragma unroll
-        for (int k = 0; k < 16; ++k)
-          if (k < K && p < (int)tok * K + k && id == s_id[k]) atomicAdd(&s_ord[k], 1);
-      }
     }
   }
   __syncthreads();
