@@ -50,7 +50,10 @@ __device__ __forceinline__ bool token_on(const PermuteArgs& a, int64_t tok) {
   return false;
 }
 
-// Block-wide exclusive scan of one int per thread; `buf` holds kSmallWarps + 1.
+// Block-wide exclusive scan of one int per thread, with one barrier: every
+// warp reads all the warp totals from `buf` (kSmallWarps ints) and sums the
+// ones before it. `buf` must not be written again before the caller's next
+// barrier.
 __device__ int small_excl_scan(int v, int* buf, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int incl = v;
@@ -61,22 +64,9 @@ __device__ int small_excl_scan(int v, int* buf, int* total) {
   }
   if (lane == 31) buf[warp] = incl;
   __syncthreads();
-  if (warp == 0) {
-    const int w = lane < kSmallWarps ? buf[lane] : 0;
-    int wi = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(kFull, wi, o);
-      if (lane >= o) wi += t;
-    }
-    if (lane < kSmallWarps) buf[lane] = wi - w;
-    if (lane == kSmallWarps - 1) buf[kSmallWarps] = wi;
-  }
-  __syncthreads();
-  const int res = buf[warp] + incl - v;
-  *total = buf[kSmallWarps];
-  __syncthreads();
-  return res;
+  const int w = lane < kSmallWarps ? buf[lane] : 0;
+  *total = __reduce_add_sync(kFull, w);
+  return __reduce_add_sync(kFull, lane < warp ? w : 0) + incl - v;
 }
 
 // Outputs of the routing half that no permute kernel writes.
@@ -191,11 +181,13 @@ __global__ void __launch_bounds__(kSmallThreads)
   __syncthreads();
   // Shared-expert rank g hosts replica g % R_rep; source rr sends every
   // active token to replica rr % R_rep of each shared expert.
-  for (int t = threadIdx.x; t < d.S_r * W; t += nt) {
-    const int g = t / W, rr = t - g * W;
-    cnt[t] = (d.S_eff > 0 && (g % d.R_rep) == (rr % d.R_rep)) ? s_act[rr] : 0;
+  if (d.S_r > 0) {
+    for (int t = threadIdx.x; t < d.S_r * W; t += nt) {
+      const int g = t / W, rr = t - g * W;
+      cnt[t] = (d.S_eff > 0 && (g % d.R_rep) == (rr % d.R_rep)) ? s_act[rr] : 0;
+    }
+    __syncthreads();
   }
-  __syncthreads();
   // Exclusive prefix of the counts in slot-major order: each block's first row.
   int total = 0;
   {
