@@ -75,8 +75,10 @@ __device__ __forceinline__ int gslot(const Dims& d, int rank, int le) {
   return rank < d.S_r ? rank : d.S_r + (rank - d.S_r) * d.L + le;
 }
 
-// Block-wide exclusive scan of one int per thread (NW warps); returns the
-// prefix and the block total. `buf` holds NW + 1 ints.
+// Block-wide exclusive scan of one int per thread (NW <= 32 warps); returns
+// the prefix and the block total. One barrier: every warp reads all the warp
+// totals from `buf` (NW ints) and sums the ones before it, so `buf` must not
+// be written again before the caller's next barrier.
 template <int NW>
 __device__ int block_excl_scan(int v, int* buf, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -88,22 +90,9 @@ __device__ int block_excl_scan(int v, int* buf, int* total) {
   }
   if (lane == 31) buf[warp] = incl;
   __syncthreads();
-  if (warp == 0) {
-    const int w = lane < NW ? buf[lane] : 0;
-    int wi = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(kFull, wi, o);
-      if (lane >= o) wi += t;
-    }
-    if (lane < NW) buf[lane] = wi - w;
-    if (lane == NW - 1) buf[NW] = wi;
-  }
-  __syncthreads();
-  const int res = buf[warp] + incl - v;
-  *total = buf[NW];
-  __syncthreads();
-  return res;
+  const int w = lane < NW ? buf[lane] : 0;
+  *total = __reduce_add_sync(kFull, w);
+  return __reduce_add_sync(kFull, lane < warp ? w : 0) + incl - v;
 }
 
 // CTA r * CH + c counts chunk c of source r: tokens [c * TC, (c + 1) * TC).
