@@ -127,7 +127,12 @@ def workload_desc(wl) -> str:
 # ---------------------------------------------------------------- clocks ----
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+    """nvidia-smi samples of SM clock and throttle reasons during a region.
+    The region starts `lead_s` seconds before the timed steps, with the GPU
+    running the same step meanwhile (Bench.load_for): nvidia-smi's first
+    sample comes only after its start-up, and the timed steps may last a few
+    milliseconds."""
+    lead_s = 0.5
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -154,7 +159,6 @@ class ClockSampler:
     def stop(self) -> dict:
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        time.sleep(0.15)
         self.proc.terminate()
         self.proc.wait()
         sm, smax, reasons = [], [], set()
@@ -174,7 +178,9 @@ class ClockSampler:
         os.unlink(self.path)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None, "samples": len(sm),
-                "reasons": sorted(reasons)}
+                "reasons": sorted(reasons),
+                "window": f"the timed steps and the {self.lead_s:g} s of the same step "
+                          "just before them"}
 
 
 # -------------------------------------------------------- byte accounting ----
@@ -589,13 +595,25 @@ class Bench:
         return ([e[0].elapsed_time(e[1]) for e in evb], [e[1].elapsed_time(e[2]) for e in evb],
                 [e[2].elapsed_time(e[3]) for e in evb])
 
+    def load_for(self, seconds):
+        """The step (L2 flushed between steps, as in the timed loop) repeated
+        for about `seconds`, untimed."""
+        import torch
+        t_end = time.perf_counter() + seconds
+        while time.perf_counter() < t_end:
+            for _ in range(20):
+                self.flush.zero_()
+                self.run_step()
+            torch.cuda.synchronize()
+
     def timed(self, n, barrier, clocks=None):
         """n steps, L2 flushed between them outside the events: step times (ms)."""
         import torch
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
-        barrier()
-        if clocks:
+        if clocks and clocks.enabled:
             clocks.start()
+            self.load_for(clocks.lead_s)
+        barrier()
         t_wall = time.perf_counter()
         for k in range(n):
             self.flush.zero_()
