@@ -83,7 +83,8 @@ struct RouteOut {
 // bytes (so a batch of few tokens spreads its stores over twice the SMs);
 // the first writes the row records and scales.
 // SM == kRowPerSlot: each routed row is quantised with its own smooth row
-// (one expert's, or one shared expert's), one row after another.
+// (one expert's, or one shared expert's), one row after another; with two
+// CTAs per token each quantises and writes every other routed row whole.
 template <class T, int Q, int SM>
 __global__ void __launch_bounds__(kSmallThreads)
     dispatch_small_kernel(PermuteArgs a, RouteOut ro, int trigger_early, int halves) {
@@ -111,9 +112,10 @@ __global__ void __launch_bounds__(kSmallThreads)
   const int code_bytes = MODE == 0 ? 2 * H : H;
   const int scale_bytes = MODE == 3 ? 4 * d.G3 : ((MODE == 4 || MODE == 5) ? d.SC : 0);
   const int stage_bytes = (code_bytes + ((scale_bytes + 15) & ~15) + 15) & ~15;
+  const int n_stages = SM == kRowPerSlot ? 2 : 1;  // row after row: two staging buffers
   const int cpart = code_bytes / halves, spart = scale_bytes / halves;  // this CTA's bytes of a row
   uint8_t* const s_stage = s_dyn;
-  int* const cnt = reinterpret_cast<int*>(s_dyn + stage_bytes);  // [G][W] rows per block
+  int* const cnt = reinterpret_cast<int*>(s_dyn + n_stages * stage_bytes);  // [G][W] rows per block
   int* const start = cnt + nE;                                  // [G][W] first global row
   char* const dyn = static_cast<char*>(a.dynamic_scales);
   char* const out = static_cast<char*>(a.expand_x);
@@ -305,8 +307,16 @@ __global__ void __launch_bounds__(kSmallThreads)
     return;
   }
   if (SM == kRowPerSlot) {
-    // One quantisation per routed row, each with its own smooth row.
-    for (int n = 0; n < nrows; ++n) {
+    // One quantisation per routed row, each with its own smooth row, into
+    // the two staging buffers in turn: a row's bulk stores drain while the
+    // next row is quantised. With two CTAs per token each takes every other
+    // row and writes it whole.
+    int it = 0;
+    for (int n = half; n < nrows; n += halves, ++it) {
+      uint8_t* const stg = s_stage + (it & 1) * stage_bytes;
+      // The stores of this buffer's previous row have read it before any
+      // thread passes the barrier inside quantise and writes it again.
+      if (threadIdx.x == 0 && it >= 2) bulk_wait_read<1>();
       const float* srow = a.smooth + (int64_t)s_srow[n] * H;
       float f[2][16];
 #pragma unroll
@@ -319,23 +329,21 @@ __global__ void __launch_bounds__(kSmallThreads)
           for (int t = 0; t < 16; ++t) f[q][t] = 0.f;
         }
       }
-      carried = quantise<Q>(f, U, s_stage, s_stage + code_bytes, s_red[0], nt);
+      carried = quantise<Q>(f, U, stg, stg + code_bytes, s_red[0], nt);
       fence_proxy_async_smem();  // staging writes before the bulk copies read them
       __syncthreads();
       const int64_t row = s_row[n];
       if (threadIdx.x == 0) {
-        bulk_store(out + row * code_bytes + half * cpart, s_stage + half * cpart, (uint32_t)cpart);
+        bulk_store(out + row * code_bytes, stg, (uint32_t)code_bytes);
         if (scale_bytes && a.scale_rows_bulk)
-          bulk_store(dyn + row * scale_bytes + half * spart, s_stage + code_bytes + half * spart,
-                     (uint32_t)spart);
+          bulk_store(dyn + row * scale_bytes, stg + code_bytes, (uint32_t)scale_bytes);
         bulk_commit();
-        bulk_wait_read<0>();
       }
-      if (MODE == 2 && threadIdx.x == 0 && half == 0) reinterpret_cast<float*>(dyn)[row] = carried;
-      if (scale_bytes && !a.scale_rows_bulk && half == 0)
-        for (int b = threadIdx.x; b < scale_bytes; b += nt) dyn[row * scale_bytes + b] = s_stage[code_bytes + b];
-      __syncthreads();  // the staging buffer is free for the next row
+      if (MODE == 2 && threadIdx.x == 0) reinterpret_cast<float*>(dyn)[row] = carried;
+      if (scale_bytes && !a.scale_rows_bulk)
+        for (int b = threadIdx.x; b < scale_bytes; b += nt) dyn[row * scale_bytes + b] = stg[code_bytes + b];
     }
+    if (threadIdx.x == 0) bulk_wait_read<0>();
     if (!trigger_early) griddep_launch_dependents();
     return;
   }
@@ -400,7 +408,7 @@ cudaError_t launch_small(const PermuteArgs& a, const RouteOut& ro, cudaStream_t 
   const size_t scale_bytes =
       MODE == 3 ? 4 * (size_t)a.d.G3 : ((MODE == 4 || MODE == 5) ? (size_t)a.d.SC : 0);
   const size_t stage = (code_bytes + ((scale_bytes + 15) & ~size_t(15)) + 15) & ~size_t(15);
-  const size_t smem = stage + 2 * sizeof(int) * (size_t)a.d.G * a.d.W;
+  const size_t smem = (SM == kRowPerSlot ? 2 : 1) * stage + 2 * sizeof(int) * (size_t)a.d.G * a.d.W;
   cudaError_t e = prepare_kernel<dispatch_small_kernel<T, Q, SM>>(smem);
   if (e != cudaSuccess) return e;
   int blocks = 0;
