@@ -30,6 +30,10 @@ constexpr int kSmallWarps = kSmallThreads / 32;
 constexpr int kSmallMaxPairs = 4096;    // W * BS * K
 constexpr int kSmallMaxEntries = 2048;  // G * W (counts and prefix in shared memory)
 constexpr int kSmallMaxW = 768;
+// With one smooth row per expert every routed row is quantised on its own,
+// one after another in its token's CTA(s): past about this many values
+// (W * BS * NS * H) the expert-major kernels are faster.
+constexpr int64_t kSmallMaxSmoothValues = int64_t(1) << 23;
 
 // Is token tok (source r, index i) active, and is its pair j switched on?
 __device__ __forceinline__ int tokens_of(const PermuteArgs& a, int r) {
@@ -449,7 +453,9 @@ cudaError_t launch_small_typed(const PermuteArgs& a, const RouteOut& ro, cudaStr
 
 bool dispatch_small_fits(const Dims& d, bool per_expert_smooth) {
   using namespace permute_detail;
-  if (per_expert_smooth && d.mode != 2) return false;
+  if (per_expert_smooth &&
+      (d.mode != 2 || (int64_t)d.W * d.BS * d.NS * d.H > kSmallMaxSmoothValues))
+    return false;
   if (d.mode != 0 && d.mode != 2 && !(d.mode == 5 && d.y_dtype == 0)) return false;
   return (int64_t)d.W * d.BS * d.K <= kSmallMaxPairs && (int64_t)d.G * d.W <= kSmallMaxEntries &&
          d.W <= kSmallMaxW && d.K <= 16;

@@ -39,7 +39,8 @@ def one_kernel_dispatch(wl) -> bool:
     c = wl.cfg
     mode, W, BS, K = c["quant_mode"], c["ep_world_size"], c["max_bs"], c["topk"]
     per_expert = uses_smooth(wl) and c.get("smooth_kind", 0) == 0
-    if per_expert and mode != 2:
+    NS = K + (c["shared_expert_num"] if c["shared_expert_rank_num"] > 0 else 0)
+    if per_expert and (mode != 2 or W * BS * NS * c["hidden"] > 1 << 23):
         return False
     if not (mode in (0, 2) or (mode == 5 and c.get("y_dtype", 0) == 0)):
         return False

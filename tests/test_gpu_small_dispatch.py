@@ -3,7 +3,8 @@
 cq_dispatch_permute, always run the three-kernel path. Both must leave every
 output and the status word identical. The cases sit inside the one-kernel
 path's limits (W * BS * K <= 4096, (S_r + M) * W <= 2048, quant_mode 0, 2 or
-5 with e4m3 codes) and cover each of its branches: masks of both shapes,
+5 with e4m3 codes, W * BS * NS * H <= 2^23 with per-expert smooth rows;
+each case asserts it) and cover each of its branches: masks of both shapes,
 per-rank batch sizes, shared, zero, copy and const experts, invalid and
 duplicate ids, every smooth shape of mode 2, fp16 tokens and the extremes of
 K, BS and W. The oracle parity tests cover the same path on their own small
@@ -84,6 +85,7 @@ def test_one_kernel_dispatch_matches_the_two_halves(name):
     wl = _cases()[name]
     cfg = cq.Config.from_dict(wl.cfg)
     assert cfg.check() == 0
+    assert gh.one_kernel_dispatch(wl), "the case lies outside the one-kernel path"
     x = gh.dev(wl.x, cfg.token_dtype)
     ids = gh.dev(wl.expert_ids, torch.int32)
     sm, mask = gh.dev(_uses(wl), torch.float32), gh.dev(wl.mask, torch.uint8)
