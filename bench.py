@@ -223,9 +223,10 @@ def kernels_per_step(cfg, smooth_given: bool) -> int:
     mode = cfg.quant_mode
     per_expert_smooth = smooth_given and cfg.smooth_kind == 0 and mode in (1, 2, 3)
     W, BS, K = cfg.ep_world_size, cfg.max_bs, cfg.topk
+    smooth_values = W * BS * cfg.num_slots * cfg.hidden  # rows quantised one by one
     small = ((mode in (0, 2) or (mode == 5 and cfg.y_dtype == 0))
-             and (not per_expert_smooth or mode == 2)
-             and W * BS * K <= 4096 and (cfg.shared_expert_rank_num + cfg.moe_expert_num) * W <= 2048
+             and (not per_expert_smooth or (mode == 2 and smooth_values <= 1 << 23))
+             and W * BS * K <= 2048 and (cfg.shared_expert_rank_num + cfg.moe_expert_num) * W <= 2048
              and W <= 768 and K <= 16)
     if small:
         return 2

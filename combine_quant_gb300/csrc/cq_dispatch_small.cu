@@ -1,6 +1,6 @@
 // cq_dispatch_small.cu -- the whole dispatch of a small batch in one launch.
 //
-// For a few thousand (token, slot) pairs the routing scan is cheaper to
+// For up to 2048 (token, slot) pairs the routing scan is cheaper to
 // repeat than to hand over: every CTA of dispatch_small_kernel (one per
 // source token, as permute_kernel) reads all of expert_ids and builds, in
 // shared memory, the rows of every (expert slot, source) block and their
@@ -27,7 +27,9 @@ namespace {
 
 constexpr int kSmallThreads = 256;
 constexpr int kSmallWarps = kSmallThreads / 32;
-constexpr int kSmallMaxPairs = 4096;    // W * BS * K
+// W * BS * K: every CTA repeats the scan over all pairs; from about this
+// many on the routing kernels (one scan) are as fast or faster.
+constexpr int kSmallMaxPairs = 2048;
 constexpr int kSmallMaxEntries = 2048;  // G * W (counts and prefix in shared memory)
 constexpr int kSmallMaxW = 768;
 // With one smooth row per expert every routed row is quantised on its own,

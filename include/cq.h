@@ -172,9 +172,10 @@ int cq_dispatch(const cq_config* cfg, const void* x, const int32_t* expert_ids,
 
 /* The two halves of cq_dispatch, same arguments; calling cq_dispatch_route
  * then cq_dispatch_permute on one stream gives exactly cq_dispatch's outputs
- * and status. (For a small batch, W * BS * K <= 4096 pairs and
- * (S_r + M) * W <= 2048 with quant_mode 0, 2 or 5 with e4m3 codes,
- * cq_dispatch itself runs both halves in one kernel.)
+ * and status. (For a small batch, W * BS * K <= 2048 pairs and
+ * (S_r + M) * W <= 2048 with quant_mode 0, 2 or 5 with e4m3 codes, and with
+ * one smooth row per expert W * BS * NS * H <= 2^23, cq_dispatch itself runs
+ * both halves in one kernel.)
  * route: scan, counts, prefix sums (writes ep_recv_count, expert_token_nums,
  *        the rank_row_base part of assist_info, and the workspace);
  * permute: row placement and quantisation (writes expand_x, dynamic_scales,

@@ -44,7 +44,7 @@ def one_kernel_dispatch(wl) -> bool:
         return False
     if not (mode in (0, 2) or (mode == 5 and c.get("y_dtype", 0) == 0)):
         return False
-    return (W * BS * K <= 4096 and (c["shared_expert_rank_num"] + c["moe_expert_num"]) * W <= 2048
+    return (W * BS * K <= 2048 and (c["shared_expert_rank_num"] + c["moe_expert_num"]) * W <= 2048
             and W <= 768 and K <= 16)
 
 

@@ -125,3 +125,7 @@ def test_kernels_per_step_follows_the_dispatch_path():
     assert n(workloads.dsv3()) == 4 and n(workloads.special()) == 4
     assert n(workloads.skew()) == 5
     assert n(workloads.mxfp8(W=4, BS=8, M=16, K=4, H=1024)) == 2
+    # the one-kernel dispatch's limits: 2048 (token, slot) pairs, and with one
+    # smooth row per expert 2^23 values quantised row by row
+    assert n(workloads.perf_table(32)) == 2 and n(workloads.perf_table(64)) == 4
+    assert n(workloads.skew(BS=4)) == 2 and n(workloads.skew(BS=8)) == 5

@@ -2,7 +2,7 @@
 (dispatch_small_kernel); its two halves, cq_dispatch_route and
 cq_dispatch_permute, always run the three-kernel path. Both must leave every
 output and the status word identical. The cases sit inside the one-kernel
-path's limits (W * BS * K <= 4096, (S_r + M) * W <= 2048, quant_mode 0, 2 or
+path's limits (W * BS * K <= 2048, (S_r + M) * W <= 2048, quant_mode 0, 2 or
 5 with e4m3 codes, W * BS * NS * H <= 2^23 with per-expert smooth rows;
 each case asserts it) and cover each of its branches: masks of both shapes,
 per-rank batch sizes, shared, zero, copy and const experts, invalid and
@@ -45,8 +45,9 @@ def _cases():
     out["tiny_m2_per_expert_smooth"] = workloads.tiny(0, 2)
     out["tiny_m5"] = workloads.tiny(0, 5)
     out["special_small"] = workloads.special(seed=51, W=8, BS=20, H=1024, M=48)
-    out["skew_small_per_expert_smooth"] = workloads.skew(seed=52, W=4, BS=64, M=32, K=16,
-                                                         H=2048)
+    # at both the pair limit and the per-expert-smooth limit (W * BS * NS * H = 2^23)
+    out["skew_small_per_expert_smooth"] = workloads.skew(seed=52, W=4, BS=32, M=32, K=16,
+                                                         H=4096)
     wl, rng = _case(53, W=3, M=6, BS=9, K=4, mask_ndim=2, zero_expert_num=1, copy_expert_num=1)
     wl.expert_ids = rng.integers(0, 9, (3, 9, 4)).astype(np.int32)  # 8: invalid; duplicates
     wl.mask = (rng.random((3, 9, 4)) < 0.7).astype(np.uint8)
@@ -68,11 +69,11 @@ def _cases():
     wl.smooth = np.array([3.0], np.float32)
     out["smooth_scalar"] = wl
     out["fp16_m2"] = workloads.as_fp16(workloads.dsv3(seed=58, W=8, BS=12, M=32, K=8, H=1536))
-    out["K16_W2"], _ = _case(59, W=2, M=16, BS=128, K=16, H=1024, mode=5)
+    out["K16_W2"], _ = _case(59, W=2, M=16, BS=64, K=16, H=1024, mode=5)
     out["K1_BS1"], _ = _case(60, W=16, M=32, BS=1, K=1, H=8192, mode=0)
-    out["dsv3_small_at_the_limit"] = workloads.dsv3(seed=61, W=8, BS=64, M=64, K=8, H=2048)
-    # both limits at once: 4096 pairs and (S_r + M) * W = 2048 block counts
-    out["pairs_and_blocks_at_the_limit"], _ = _case(62, W=32, M=64, BS=16, K=8, H=7168, mode=0)
+    out["dsv3_small_at_the_limit"] = workloads.dsv3(seed=61, W=8, BS=32, M=64, K=8, H=2048)
+    # both limits at once: 2048 pairs and (S_r + M) * W = 2048 block counts
+    out["pairs_and_blocks_at_the_limit"], _ = _case(62, W=32, M=64, BS=8, K=8, H=7168, mode=0)
     return out
 
 
