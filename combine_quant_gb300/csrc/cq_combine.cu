@@ -591,10 +591,10 @@ cudaError_t launch_combine_t(const CombineArgs& a, const Src& src, cudaStream_t 
 
 }  // namespace
 
-// A batch of few work items (a few per SM, about as many as the staged
-// kernel has CTAs) runs one CTA per (token, 1024 columns) instead, each
-// thread loading its unit of every routed row at once (one round trip
-// instead of the ring's laps). Both sum in the same order.
+// A batch of fewer than kDirectItemsPerSm work items per SM runs one CTA per
+// (token, 1024 columns) instead of the staged ring, each thread loading its
+// unit of every routed row at once (one round trip instead of the ring's
+// laps). Both sum in the same order.
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t s) {
   const int64_t items = (int64_t)a.d.W * a.d.BS * ((a.d.H + kChunkCols - 1) / kChunkCols);
   if (items < (int64_t)kDirectItemsPerSm * sm_count()) {
