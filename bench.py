@@ -517,6 +517,7 @@ class Bench:
         self.stream = torch.cuda.current_stream(dev)
         self.use_graph = not args.no_graph
         self.parts = [self.route, self.permute, lambda: self.combine()]
+        self.run_dispatch = self.dispatch
         self.run_step = self.step
         if self.use_graph:
             side = torch.cuda.Stream(dev)
@@ -524,7 +525,8 @@ class Bench:
             graphs = {}
             with torch.cuda.stream(side):
                 for name, fn in (("step", self.step), ("route", self.route),
-                                 ("permute", self.permute), ("combine", lambda: self.combine())):
+                                 ("permute", self.permute), ("combine", lambda: self.combine()),
+                                 ("dispatch", self.dispatch)):
                     g = torch.cuda.CUDAGraph()
                     with torch.cuda.graph(g, stream=side):
                         fn()
@@ -533,6 +535,7 @@ class Bench:
             torch.cuda.synchronize()
             self.graphs = graphs
             self.run_step = graphs["step"].replay
+            self.run_dispatch = graphs["dispatch"].replay
             self.parts = [graphs["route"].replay, graphs["permute"].replay,
                           graphs["combine"].replay]
 
@@ -595,6 +598,19 @@ class Bench:
         barrier()
         return ([e[0].elapsed_time(e[1]) for e in evb], [e[1].elapsed_time(e[2]) for e in evb],
                 [e[2].elapsed_time(e[3]) for e in evb])
+
+    def dispatch_alone(self, n, barrier):
+        """cq_dispatch alone, L2 flushed before each call: times (ms)."""
+        import torch
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+        barrier()
+        for k in range(n):
+            self.flush.zero_()
+            ev[k][0].record(self.stream)
+            self.run_dispatch()
+            ev[k][1].record(self.stream)
+        barrier()
+        return [e[0].elapsed_time(e[1]) for e in ev]
 
     def load_for(self, seconds):
         """The step (L2 flushed between steps, as in the timed loop) repeated
@@ -674,6 +690,16 @@ def side_figures(args, dev, flush, barrier, peak):
             "steps": steps, "step_us": step_us, "tokens_per_s": tokens / (step_us * 1e-6),
             "kernels": {k: {"us": us[k], "alg_bytes": ab[k],
                             "frac": ab[k] / (us[k] * 1e-6) / 1e9 / peak} for k in us}}
+        if kernels_per_step(b.cfg, b.sm is not None) == 2:
+            # The step's cq_dispatch is one kernel (routing and permute
+            # together); the route and permute figures above time the two
+            # dispatch halves, which that kernel replaces.
+            t_one = b.dispatch_alone(steps, barrier)
+            res[name]["dispatch_one_kernel"] = {
+                "us": 1e3 * statistics.mean(t_one),
+                "alg_bytes": ab["route"] + ab["permute"],
+                "note": "cq_dispatch as the step runs it (dispatch_small_kernel); route and "
+                        "permute above are the two dispatch halves"}
         if name == "tiny":
             # latency-bound: the same step with L2 left warm between steps
             saved = flush.mode
