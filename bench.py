@@ -216,20 +216,14 @@ def algorithmic_bytes(cfg, rows: int, tokens_active: int, with_scales: bool,
 
 def kernels_per_step(cfg, smooth_given: bool) -> int:
     """libcq kernels one step launches: cq_dispatch (one kernel for a small
-    batch, the same limits as dispatch_small_fits in cq_dispatch_small.cu;
-    else routing (count, offsets) and the permute: index + smooth-rows
-    kernels for per-expert smooth scales in modes 1-3, else one kernel) and
-    the combine."""
-    mode = cfg.quant_mode
-    per_expert_smooth = smooth_given and cfg.smooth_kind == 0 and mode in (1, 2, 3)
-    W, BS, K = cfg.ep_world_size, cfg.max_bs, cfg.topk
-    smooth_values = W * BS * cfg.num_slots * cfg.hidden  # rows quantised one by one
-    small = ((mode in (0, 2) or (mode == 5 and cfg.y_dtype == 0))
-             and (not per_expert_smooth or (mode == 2 and smooth_values <= 1 << 23))
-             and W * BS * K <= 2048 and (cfg.shared_expert_rank_num + cfg.moe_expert_num) * W <= 2048
-             and W <= 768 and K <= 16)
-    if small:
+    batch, as the library reports through cq_dispatch_one_kernel; else
+    routing (count, offsets) and the permute: index + smooth-rows kernels for
+    per-expert smooth scales in modes 1-3, else one kernel) and the combine."""
+    import combine_quant_gb300 as cq
+
+    if cq.dispatch_one_kernel(cfg, smooth_given):
         return 2
+    per_expert_smooth = smooth_given and cfg.smooth_kind == 0 and cfg.quant_mode in (1, 2, 3)
     return 2 + (2 if per_expert_smooth else 1) + 1
 
 

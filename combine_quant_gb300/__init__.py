@@ -10,9 +10,9 @@ from .api import (Config, DispatchResult, alloc_dispatch_outputs, alloc_workspac
                   assist_views, check_bounded_wait, combine, combine_q8, combine_quant,
                   combine_ws, cq_check_bounded_wait, cq_combine, cq_combine_q8,
                   cq_combine_quant, cq_combine_ws, cq_dispatch, cq_dispatch_noalloc, cq_dispatch_permute,
-                  cq_dispatch_route, cq_dispatch_workspace_size, cq_read_combine_status,
-                  cq_read_status, dispatch, dispatch_noalloc, dispatch_permute, dispatch_route,
-                  dispatch_workspace_size, moe_combine, moe_dispatch, read_combine_status,
-                  read_status)
+                  cq_dispatch_one_kernel, cq_dispatch_route, cq_dispatch_workspace_size,
+                  cq_read_combine_status, cq_read_status, dispatch, dispatch_noalloc,
+                  dispatch_one_kernel, dispatch_permute, dispatch_route, dispatch_workspace_size,
+                  moe_combine, moe_dispatch, read_combine_status, read_status)
 from ._lib import (CQ_ST_BAD_ID, CQ_ST_BAD_MASK, CQ_ST_INTERNAL, CQ_ST_TIMEOUT,  # noqa: F401
                    CqError)

@@ -40,7 +40,7 @@ EXPORTS = (
     "cq_workspace_init", "cq_dispatch",
     "cq_dispatch_route", "cq_dispatch_permute", "cq_combine", "moe_dispatch", "moe_combine",
     "cq_read_status", "cq_strerror", "cq_dispatch_noalloc", "cq_combine_quant", "cq_combine_q8",
-    "cq_read_combine_status", "cq_check_bounded_wait", "cq_combine_ws",
+    "cq_read_combine_status", "cq_check_bounded_wait", "cq_combine_ws", "cq_dispatch_one_kernel",
 )
 
 
@@ -78,6 +78,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         "cq_assist_info_size": ([cfgp], i64),
         "cq_workspace_size": ([cfgp], sz),
         "cq_dispatch_workspace_size": ([cfgp], sz),
+        "cq_dispatch_one_kernel": ([cfgp, ctypes.c_int], ctypes.c_int),
         "cq_workspace_init": ([P, sz, P], ctypes.c_int),
         "cq_dispatch": ([cfgp] + [P] * 13 + [sz, P], ctypes.c_int),
         "moe_dispatch": ([cfgp] + [P] * 13 + [sz, P], ctypes.c_int),

@@ -454,8 +454,18 @@ def dispatch_workspace_size(cfg: Config) -> int:
     return int(_lib.load().cq_dispatch_workspace_size(ctypes.byref(cfg.as_c())))
 
 
+def dispatch_one_kernel(cfg: Config, with_smooth_scales: bool = False) -> bool:
+    """Whether cq_dispatch runs this config's routing and permute as one
+    kernel (cq_dispatch_one_kernel; host only)."""
+    rc = _lib.load().cq_dispatch_one_kernel(ctypes.byref(cfg.as_c()), int(bool(with_smooth_scales)))
+    if rc < 0:
+        _lib.check(rc, "cq_dispatch_one_kernel")
+    return rc == 1
+
+
 cq_dispatch = moe_dispatch = dispatch
 cq_dispatch_workspace_size = dispatch_workspace_size
+cq_dispatch_one_kernel = dispatch_one_kernel
 cq_dispatch_route = dispatch_route
 cq_dispatch_permute = dispatch_permute
 cq_dispatch_noalloc = dispatch_noalloc

@@ -218,6 +218,13 @@ extern "C" {
 
 int cq_check_config(const cq_config* cfg) { return validate(cfg); }
 
+int cq_dispatch_one_kernel(const cq_config* cfg, int with_smooth_scales) {
+  const int rc = validate(cfg);
+  if (rc != CQ_OK) return rc;
+  return cq::dispatch_small_fits(dims_of(cfg), with_smooth_scales && cfg->smooth_kind == 0) ? 1
+                                                                                              : 0;
+}
+
 int32_t cq_local_expert_num(const cq_config* c) {
   if (!c || c->ep_world_size <= c->shared_expert_rank_num) return 0;
   return c->moe_expert_num / (c->ep_world_size - c->shared_expert_rank_num);

@@ -327,6 +327,15 @@ int cq_read_combine_status(uint32_t* status, void* stream);
  * device stays usable afterwards. CQ_ERR_ARG for NULL outputs. */
 int cq_check_bounded_wait(uint32_t* gave_up, double* seconds, void* stream);
 
+/* Which kernels cq_dispatch runs for a config (no counterpart in the pages;
+ * host only, nothing is enqueued): 1 when it runs routing and permute as one
+ * kernel (a small batch: W * BS * K <= 2048, (S_r + M) * W <= 2048,
+ * quant_mode 0, 2 or 5 with e4m3 codes, and with one smooth row per expert
+ * W * BS * NS * H <= 2^23), 0 when it runs the routing kernels and the
+ * permute kernels, or a negative CQ_ERR_* code for an invalid config.
+ * with_smooth_scales: nonzero when the call passes smooth_scales. */
+int cq_dispatch_one_kernel(const cq_config* cfg, int with_smooth_scales);
+
 /* Static description of an error code. */
 const char* cq_strerror(int code);
 

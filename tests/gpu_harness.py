@@ -34,18 +34,9 @@ def uses_smooth(wl) -> bool:
 
 
 def one_kernel_dispatch(wl) -> bool:
-    """Whether cq_dispatch runs this problem as one kernel (the limits of
-    dispatch_small_fits in cq_dispatch_small.cu)."""
-    c = wl.cfg
-    mode, W, BS, K = c["quant_mode"], c["ep_world_size"], c["max_bs"], c["topk"]
-    per_expert = uses_smooth(wl) and c.get("smooth_kind", 0) == 0
-    NS = K + (c["shared_expert_num"] if c["shared_expert_rank_num"] > 0 else 0)
-    if per_expert and (mode != 2 or W * BS * NS * c["hidden"] > 1 << 23):
-        return False
-    if not (mode in (0, 2) or (mode == 5 and c.get("y_dtype", 0) == 0)):
-        return False
-    return (W * BS * K <= 2048 and (c["shared_expert_rank_num"] + c["moe_expert_num"]) * W <= 2048
-            and W <= 768 and K <= 16)
+    """Whether cq_dispatch runs this problem as one kernel (the library's own
+    decision, cq_dispatch_one_kernel)."""
+    return cq.dispatch_one_kernel(cq.Config.from_dict(wl.cfg), uses_smooth(wl))
 
 
 def _same_outputs(cfg, a, b) -> None:

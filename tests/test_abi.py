@@ -61,6 +61,28 @@ def test_workspace_size_under_both_names(lib):
     assert cq.cq_dispatch_workspace_size(cfg) == cfg.workspace_size > 0
 
 
+def test_dispatch_one_kernel_limits(lib):
+    """cq_dispatch_one_kernel: the small-batch path's limits, on both sides of
+    each (2048 pairs, 2048 block counts, 2^23 per-expert-smooth values, the
+    quant modes it covers), and an invalid config's error code."""
+    from combine_quant_gb300 import workloads
+
+    def one(wl, smooth=None):
+        smooth = wl.smooth is not None if smooth is None else smooth
+        return lib.cq_dispatch_one_kernel(_c(wl.cfg), int(smooth))
+
+    assert one(workloads.tiny()) == 1 and one(workloads.perf_table(8)) == 1
+    assert one(workloads.perf_table(32)) == 1 and one(workloads.perf_table(64)) == 0
+    assert one(workloads.dsv3(BS=2)) == 0  # (S_r + M) * W = 8192 block counts
+    assert one(workloads.skew(BS=4)) == 1 and one(workloads.skew(BS=8)) == 0  # 2^23 values
+    assert one(workloads.skew(BS=8), smooth=False) == 1  # the same without smooth rows
+    assert one(workloads.tiny(0, 5)) == 1
+    mode3 = dict(workloads.tiny().cfg, quant_mode=3)
+    assert lib.cq_dispatch_one_kernel(_c(mode3), 0) == 0
+    bad = dict(workloads.tiny().cfg, ep_world_size=1)
+    assert lib.cq_dispatch_one_kernel(_c(bad), 0) == _lib.CQ_ERR_ARG
+
+
 def _c(cfg):
     return ctypes.byref(_lib.CqConfig(**cfg))
 

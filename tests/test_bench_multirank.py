@@ -115,7 +115,10 @@ def test_kernels_per_step_follows_the_dispatch_path():
     rows) otherwise."""
     import bench
     import combine_quant_gb300 as cq
+    from combine_quant_gb300 import build as cqbuild
     from combine_quant_gb300 import workloads
+
+    cqbuild.build()  # the decision is the library's (cq_dispatch_one_kernel, host only)
 
     def n(wl):
         cfg = cq.Config.from_dict(wl.cfg)
